@@ -1,0 +1,194 @@
+/*
+ * pisa.h -- C ABI of the GB300 (sm_103a) PISA pyramid Top-K block selector.
+ *
+ * The operation (web pages about arXiv 2609.31093, "Block Sparse Attention
+ * with Log-Linear Complexity"):
+ *  - agihunt.info summary, pyramid paragraph: keys are mean-pooled into leaf
+ *    blocks of C keys, and coarser levels mean-pool adjacent nodes with
+ *    branching factor g = 2, giving O(log N) levels; selection starts at the
+ *    coarsest level, scores a bounded candidate set with LogSumExp, keeps
+ *    Top-K and expands only the kept nodes; decode routing is O(log N) a step.
+ *  - same page, LSE paragraph: the first, previous and current leaf blocks are
+ *    always selected; kernel paragraph: query heads of one GQA group share the
+ *    selected blocks; leaf blocks are scored by LSE over their raw keys.
+ *  - rcap.io post, "Selection walks the tree top-down" and "The scoring rule
+ *    matters": at most g*K candidates per level; a candidate's score is the
+ *    LogSumExp over its child summaries.
+ *
+ * Readings fixed by this library where the pages are silent: the walk starts
+ * at the root and keeps all candidates while a level has at most K; a node is
+ * eligible when its leaf range meets E = [1, qb-2] (qb = t / C); summaries are
+ * plain means of the keys present in a node's span (not masked by the query
+ * position); the group score is the sum of the heads' natural-log LSEs; the
+ * scale is 1/sqrt(d) unless given; Top-K ties go to the lower node index;
+ * the forced blocks F = {0, qb-1, qb} are added to the Top-K of E.
+ *
+ * Conventions shared by every call
+ *  - All tensors are caller-owned DEVICE memory, contiguous, row-major.
+ *    q      prefill [B, H_q, N, d];   decode [B, H_q, d]
+ *    k      prefill [B, H_kv, N, d];  decode: key cache [B, H_kv, N, d] with
+ *           N the capacity (N_max)
+ *    pyramid fp32 [B, H_kv, P, d], P = pisa_pyramid_nodes(); node (l, j) of
+ *           level l >= 1 sits at row off_l + j, off_1 = 0, off_{l+1} = off_l +
+ *           n_l, n_1 = ceil(N / C), n_{l+1} = ceil(n_l / 2), up to n_L = 1.
+ *           Node (l, j) covers leaves [j 2^(l-1), (j+1) 2^(l-1)).
+ *    out_idx int32 [.., K+3]: Top-K leaf blocks of E together with F, in
+ *           ascending order, padded with -1.
+ *    out_score fp32 [.., K+3] (nullable): the group-summed leaf LSE of each
+ *           Top-K block, +INFINITY for forced blocks, -INFINITY for padding.
+ *  - q, k, pyramid and the workspace must be 16-byte aligned.
+ *  - dtype PISA_BF16 or PISA_FP32 (q and k alike); d in {64, 128}; C = 64;
+ *    g = 2; 1 <= K <= 32; H_q % H_kv == 0 with G = H_q / H_kv in {1,2,4,8};
+ *    qtile >= 1 (it only changes data reuse, never results).
+ *  - Every call validates its arguments on the host before any launch and,
+ *    on failure, returns a negative status and launches nothing.  Launch
+ *    failures return PISA_ERR_CUDA.  Calls are asynchronous on `stream`
+ *    (a cudaStream_t; NULL is the legacy default stream), never allocate
+ *    memory and never synchronise, except pisa_read_device_status.
+ *  - The workspace is caller-owned scratch of at least
+ *    pisa_workspace_bytes(params, mode) bytes.  Its first 256 bytes hold a
+ *    device status word that kernels set on faults they detect (a decode
+ *    sequence length outside [1, N], an exhausted bounded wait); each call
+ *    clears it first.  Calls that share a workspace must not overlap.
+ *  - The library holds no global state besides the loaded kernels and a
+ *    per-device cache of SM counts; it is safe to call from several threads
+ *    on different streams with different workspaces.
+ */
+#ifndef PISA_H_
+#define PISA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PISA_ABI_VERSION 1
+
+typedef enum {
+  PISA_OK = 0,
+  PISA_ERR_INVALID_ARG = -1,  /* null pointer, bad size or shape */
+  PISA_ERR_UNSUPPORTED = -2,  /* valid but not built: d, C, g, G, K, dtype */
+  PISA_ERR_MISALIGNED = -3,   /* a pointer is not 16-byte aligned */
+  PISA_ERR_WORKSPACE = -4,    /* workspace smaller than required */
+  PISA_ERR_CUDA = -5,         /* a CUDA runtime call or launch failed */
+  PISA_ERR_DEVICE = -6        /* a kernel reported a fault (status word) */
+} pisa_status;
+
+typedef enum { PISA_BF16 = 0, PISA_FP32 = 1 } pisa_dtype;
+
+typedef enum {
+  PISA_MODE_PREFILL = 0,
+  PISA_MODE_DECODE = 1,
+  PISA_MODE_FLAT = 2
+} pisa_mode;
+
+/* Device status codes written into the workspace status word. */
+#define PISA_DEV_OK 0
+#define PISA_DEV_BAD_SEQ_LEN 1   /* decode: seq_lens[b] outside [1, N] */
+#define PISA_DEV_TIMEOUT 2       /* a bounded device wait ran out */
+#define PISA_DEV_BAD_INDEX 3     /* an internal index check failed */
+
+typedef struct {
+  uint32_t struct_size; /* sizeof(pisa_params), for forward compatibility */
+  int32_t dtype;        /* pisa_dtype of q and k */
+  int64_t B;            /* sequences */
+  int64_t N;            /* prefill: tokens per sequence; decode: capacity */
+  int32_t H_q;          /* query heads */
+  int32_t H_kv;         /* key heads */
+  int32_t d;            /* head dimension */
+  int32_t C;            /* leaf block size (keys per leaf) */
+  int32_t g;            /* branching factor */
+  int32_t K;            /* blocks kept per level */
+  int32_t qtile;        /* queries sharing one leaf tile (reuse only) */
+  float scale;          /* score scale inside exp(); 0 means 1/sqrt(d) */
+} pisa_params;
+
+/* ABI version of the loaded library (PISA_ABI_VERSION). */
+int pisa_abi_version(void);
+
+/* Human-readable name of a status. */
+const char* pisa_status_string(pisa_status s);
+
+/* Number of pyramid levels L and nodes P per (sequence, key head); 0 on bad
+ * params.  Host only. */
+int32_t pisa_pyramid_levels(const pisa_params* p);
+int64_t pisa_pyramid_nodes(const pisa_params* p);
+
+/* Bytes of the fp32 pyramid [B, H_kv, P, d]; 0 on bad params. */
+size_t pisa_pyramid_bytes(const pisa_params* p);
+
+/* Workspace bytes needed by pisa_select_prefill (PISA_MODE_PREFILL),
+ * pisa_select_decode (PISA_MODE_DECODE) or pisa_select_flat
+ * (PISA_MODE_FLAT); 0 on bad params. */
+size_t pisa_workspace_bytes(const pisa_params* p, int32_t mode);
+
+/* Key pyramid (agihunt.info summary, pyramid paragraph; rcap.io, "Think of
+ * the keys as leaves of a tree").  Writes every node of the capacity-N layout:
+ * node (l, j) = mean of the keys k[b, h, i], i in its span and below
+ * len_b = seq_lens[b] (or N when seq_lens is NULL); a node with no key is
+ * zero.  seq_lens: DEVICE int32 [B] or NULL; values outside [0, N] are
+ * clamped.  Leaves are sums over keys in index order divided by the count;
+ * each parent is (n0 m0 + n1 m1) / (n0 + n1) of its children, all in
+ * IEEE round-to-nearest fp32, so pisa_select_decode's incremental update
+ * reproduces it bit for bit. */
+pisa_status pisa_build_pyramid(const pisa_params* p, const void* k,
+                               const int32_t* seq_lens, float* pyramid,
+                               void* stream);
+
+/* Prefill / training selection for every query position t in [0, N) of every
+ * sequence and key head (agihunt.info summary, kernel paragraph: the
+ * two-stage prefill kernel; rcap.io, the pisa_select sketch).  `pyramid`
+ * must hold pisa_build_pyramid(p, k, NULL, ...).  Outputs:
+ *   out_idx   int32 [B, H_kv, N, K+3] (required)
+ *   out_score fp32  [B, H_kv, N, K+3] (nullable)
+ *   trace     int32 [B, H_kv, N, L, K] (nullable, for tests): for each level
+ *             l = 2..L the kept node set (ascending, -1 padded) of the walk,
+ *             row l-1; rows of levels above the first level with more than
+ *             K eligible nodes hold all eligible nodes; row 0 is left -1. */
+pisa_status pisa_select_prefill(const pisa_params* p, const void* q,
+                                const void* k, const float* pyramid, void* ws,
+                                size_t ws_bytes, int32_t* out_idx,
+                                float* out_score, int32_t* trace, void* stream);
+
+/* One decode step (agihunt.info summary: "Decode routing is O(log N) per
+ * step"; kernel paragraph: a single-stage decode kernel).  For each sequence
+ * b the caller has already written its new key at position seq_lens[b]-1 of
+ * k_cache.  In one launch the call first updates `pyramid` in place along the
+ * path of that position (the leaf from its raw keys, every ancestor from its
+ * two children), then selects for the query at position seq_lens[b]-1.
+ *   q        [B, H_q, d];  seq_lens DEVICE int32 [B], each in [1, N]
+ *   pyramid  must hold the pyramid of the keys [0, seq_lens[b]-1) (e.g. from
+ *            pisa_build_pyramid with those lengths, or from the previous step)
+ *   out_idx  int32 [B, H_kv, K+3];  out_score fp32 [B, H_kv, K+3] (nullable)
+ *   trace    int32 [B, H_kv, L, K] (nullable): the kept sets of the walk, as
+ *            for pisa_select_prefill, with L the levels of capacity N.
+ * A sequence length outside [1, N] sets PISA_DEV_BAD_SEQ_LEN in the status
+ * word and leaves that sequence's outputs at -1 / -INFINITY. */
+pisa_status pisa_select_decode(const pisa_params* p, const void* q,
+                               const void* k_cache, const int32_t* seq_lens,
+                               float* pyramid, void* ws, size_t ws_bytes,
+                               int32_t* out_idx, float* out_score,
+                               int32_t* trace, void* stream);
+
+/* Flat BSA-style comparator (agihunt.info summary, model paragraph: "BSA
+ * (NSA's selected branch with mean summaries)"; rcap.io: "scores every query
+ * against every block summary", O(N^2/C)).  Every query head h' scores every
+ * complete past block i in [0, qb-1] by softmax_i(s q_h' . mu(1, i)); a block's
+ * score is the sum over the group's heads; Top-K over E plus F, output as
+ * pisa_select_prefill.  Reads only level 1 (the leaf means) of `pyramid`;
+ * uses them rounded to bf16 on the tensor-core path. */
+pisa_status pisa_select_flat(const pisa_params* p, const void* q,
+                             const float* pyramid, void* ws, size_t ws_bytes,
+                             int32_t* out_idx, float* out_score, void* stream);
+
+/* Synchronises `stream`, then copies the workspace status word into
+ * *device_code (PISA_DEV_*).  Returns PISA_ERR_DEVICE when it is non-zero. */
+pisa_status pisa_read_device_status(const void* ws, int32_t* device_code,
+                                    void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PISA_H_ */

@@ -123,9 +123,10 @@ class Oracle:
         return out
 
     def select(self, q, k, pyr=None, sel=None, seq_lens=None, decode=False,
-               trace=False):
+               trace=False, qrows=False):
         """Returns dict(idx [nq, K+3] int32, score [nq, K+3], margin [nq],
-        trace [nq, L, K] or None, counters {...})."""
+        trace [nq, L, K] or None, counters {...}).
+        qrows: q holds only the selected queries' head rows [nsel, G, d]."""
         q = _f64(q); k = _f64(k)
         if pyr is None:
             pyr = self.pyramid(k, seq_lens)
@@ -148,7 +149,8 @@ class Oracle:
         tr = np.empty((nq, L, self.K), np.int32) if trace else None
         cnt = np.zeros(4, np.int64)
         rc = lib().po_select(ctypes.byref(self.p), _ptr(q, _dp), _ptr(k, _dp), _ptr(pyr, _dp),
-                             None if sl is None else _ptr(sl, _i32p), 1 if decode else 0,
+                             None if sl is None else _ptr(sl, _i32p),
+                             1 if decode else (2 if qrows else 0),
                              nq, None if selp is None else _ptr(selp, _i64p),
                              _ptr(idx, _i32p), _ptr(score, _dp), _ptr(margin, _dp),
                              None if tr is None else _ptr(tr, _i32p), _ptr(cnt, _i64p))
@@ -158,12 +160,14 @@ class Oracle:
                     counters=dict(levels_scored=int(cnt[0]), child_dots=int(cnt[1]),
                                   leaf_keys=int(cnt[2]), cands_scored=int(cnt[3])))
 
-    def score_nodes(self, q, k, pyr, b, h, t, level, nodes, len_=None, decode=False):
+    def score_nodes(self, q, k, pyr, b, h, t, level, nodes, len_=None, decode=False, qrows=False):
+        """decode: q is [B, Hq, d]; qrows: q is this query's [G, d] rows."""
         q = _f64(q); k = _f64(k); pyr = _f64(pyr)
         nodes = np.ascontiguousarray(nodes, np.int64)
         out = np.empty(len(nodes), np.float64)
         rc = lib().po_score_nodes(ctypes.byref(self.p), _ptr(q, _dp), _ptr(k, _dp), _ptr(pyr, _dp),
-                                  self.N if len_ is None else len_, 1 if decode else 0,
+                                  self.N if len_ is None else len_,
+                                  1 if decode else (2 if qrows else 0),
                                   b, h, t, level, len(nodes), _ptr(nodes, _i64p), _ptr(out, _dp))
         if rc != 0:
             raise ValueError("oracle score_nodes: bad arguments")

@@ -243,9 +243,11 @@ static int po_cmp_idx(const void* a, const void* b) {
   return (x > y) - (x < y);
 }
 
+/* q_mode 0: q is [B, Hq, N, d]; 1: q is [B, Hq, d] (one decode query per
+ * sequence); 2: q points at this query's own [G, d] head rows. */
 static int po_setup(po_query* Q, const po_params* p, const double* q,
                     const double* k, const double* pyr, int64_t b, int32_t h,
-                    int64_t t, int64_t len, int q_rows_decode) {
+                    int64_t t, int64_t len, int q_mode) {
   Q->p = p; Q->q = q; Q->k = k; Q->pyr = pyr;
   Q->b = b; Q->h = h; Q->t = t; Q->len = len;
   Q->G = p->Hq / p->Hkv;
@@ -261,9 +263,11 @@ static int po_setup(po_query* Q, const po_params* p, const double* q,
   Q->s = po_scale(p);
   for (int g = 0; g < Q->G; ++g) {
     const int64_t hq = (int64_t)h * Q->G + g;
-    if (q_rows_decode) /* q is [B, Hq, d] */
+    if (q_mode == 1)
       Q->qrow[g] = q + (b * p->Hq + hq) * p->d;
-    else               /* q is [B, Hq, N, d] */
+    else if (q_mode == 2)
+      Q->qrow[g] = q + (int64_t)g * p->d;
+    else
       Q->qrow[g] = q + ((b * p->Hq + hq) * p->N + t) * p->d;
   }
   return 0;
@@ -370,6 +374,8 @@ static int po_select_one(po_query* Q, int32_t* out_idx, double* out_score,
  * mode 1 (decode):  q is [B, Hq, d]; sequence b holds keys [0, seq_lens[b]),
  *                   and its query sits at position seq_lens[b]-1 (sel is
  *                   ignored; one query per (b, h) in (b, h) order).
+ * mode 2 (rows):    like prefill with a sel list, but q holds only the
+ *                   selected queries' head rows, [nsel, G, d].
  * Outputs per query: out_idx[K+3] (int32), out_score[K+3], margin;
  * trace (nullable) [nq, L_cap, K]; counters (nullable) int64[4] =
  * {levels scored, child dots, leaf keys, candidates scored}. */
@@ -385,6 +391,7 @@ int po_select(const po_params* p, const double* q, const double* k,
     return -1;
   if (mode == 1) nq = p->B * p->Hkv;
   else nq = sel ? nsel : p->B * p->Hkv * p->N;
+  if (mode == 2 && !sel) return -1;
   int64_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
   int err = 0;
 #pragma omp parallel for schedule(dynamic, 64) reduction(+ : c0, c1, c2, c3)
@@ -407,7 +414,8 @@ int po_select(const po_params* p, const double* q, const double* k,
     if (t < 0 || t >= len || len > p->N) { err = 1; continue; }
     po_query Q;
     int64_t cnt[4] = {0, 0, 0, 0};
-    if (po_setup(&Q, p, q, k, pyr, b, h, t, len, mode == 1) != 0) { err = 1; continue; }
+    const double* qbase = mode == 2 ? q + i * (int64_t)(p->Hq / p->Hkv) * p->d : q;
+    if (po_setup(&Q, p, qbase, k, pyr, b, h, t, len, mode) != 0) { err = 1; continue; }
     po_select_one(&Q, out_idx + i * W, out_score + i * W, out_margin + i,
                   trace ? trace + i * (int64_t)L_cap * p->K : NULL, cnt);
     c0 += cnt[0]; c1 += cnt[1]; c2 += cnt[2]; c3 += cnt[3];
@@ -424,7 +432,7 @@ int po_score_nodes(const po_params* p, const double* q, const double* k,
                    const int64_t* nodes, double* out) {
   po_query Q;
   if (t < 0 || t >= len || len > p->N) return -1;
-  if (po_setup(&Q, p, q, k, pyr, b, h, t, len, mode == 1) != 0) return -1;
+  if (po_setup(&Q, p, q, k, pyr, b, h, t, len, mode) != 0) return -1;
   if (level < 1 || level > Q.L_cap) return -1;
   for (int64_t i = 0; i < n; ++i) {
     if (nodes[i] < 0 || nodes[i] >= Q.sizes[level - 1]) return -1;

@@ -1,0 +1,46 @@
+// pisa_internal.h -- host-side declarations shared by the library's units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pisa_common.cuh"
+
+namespace pisa {
+
+// Workspace layout of one call (byte offsets from the workspace base).
+struct PrefillWs {
+  size_t status;      // int32 status word (first 256 bytes)
+  size_t kept2;       // int32 [B, Hkv, N, K] kept level-2 nodes (-1 padded)
+  size_t leaf_score;  // fp32  [B, Hkv, N, K, 2] group LSE (log2 units)
+  size_t counts;      // int32 [nbuckets + 1] pairs per level-2 node
+  size_t offsets;     // int32 [nbuckets + 1] exclusive scan of counts
+  size_t cursor;      // int32 [nbuckets]
+  size_t tile_off;    // int32 [nbuckets + 1] exclusive scan of tiles per bucket
+  size_t pairs;       // int32 [B * Hkv * N * K] (t * K + slot) grouped by bucket
+  size_t total;
+  int64_t nbuckets;   // B * Hkv * n_2
+};
+
+bool make_pyr(int64_t N, int32_t C, Pyr* s);
+PrefillWs prefill_ws_layout(const Prob& pr, const Pyr& s);
+size_t decode_ws_bytes(const Prob& pr, const Pyr& s);
+size_t flat_ws_bytes(const Prob& pr, const Pyr& s);
+
+int sm_count(int device);
+
+cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, const int32_t* seq_lens,
+                                 float* pyr, cudaStream_t st);
+cudaError_t launch_route(const Prob& pr, const Pyr& s, const void* q, const float* pyr, int32_t* kept2,
+                         int32_t* trace, int32_t* status, cudaStream_t st);
+cudaError_t launch_leaf_simt(const Prob& pr, const Pyr& s, const void* q, const void* k, const int32_t* kept2,
+                             int32_t* out_idx, float* out_score, cudaStream_t st);
+cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, char* ws, const void* q,
+                           const void* k, int32_t* out_idx, float* out_score, int num_sms, cudaStream_t st);
+cudaError_t launch_decode(const Prob& pr, const Pyr& s, const void* q, const void* kc, const int32_t* seq_lens,
+                          float* pyr, int32_t* status, int32_t* out_idx, float* out_score, int32_t* trace,
+                          cudaStream_t st);
+cudaError_t launch_flat(const Prob& pr, const Pyr& s, const void* q, const float* pyr, char* ws,
+                        int32_t* out_idx, float* out_score, int num_sms, cudaStream_t st);
+
+}  // namespace pisa

@@ -1,0 +1,181 @@
+"""Parity checks of the GPU selector against the fp64 CPU oracle.
+
+Rule (applied per query):
+  * If the GPU's index set equals the oracle's, every finite score must be
+    within SCORE_TOL of the oracle's, and the +inf / -inf slots must match.
+  * Otherwise the query must be tie-exempt: on some level of the oracle's walk
+    the K-th and (K+1)-th candidate scores differ by less than TIE (1e-3).
+    An exempt query is still verified, level by level, from the GPU's own
+    trace: at every level its kept set must be a valid Top-K of the oracle's
+    scores for the candidates that the GPU's previous level implies (every
+    kept score >= every dropped score - TIE), and its final leaves must carry
+    scores within SCORE_TOL of the oracle's exact leaf LSE.
+The tolerances are the ones the selector is specified to meet for bf16 inputs
+with fp32 accumulation: index sets identical except where the oracle's K-th
+and (K+1)-th scores differ by < 1e-3, scores within 2e-3 absolute.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+SCORE_TOL = 2e-3
+TIE = 1e-3
+
+
+def level_sizes(nb):
+    sizes = [nb]
+    while sizes[-1] > 1:
+        sizes.append(-(-sizes[-1] // 2))
+    return sizes
+
+
+def eligible(level, j, qb):
+    if qb - 2 < 1:
+        return False
+    lo = j << (level - 1)
+    hi = ((j + 1) << (level - 1)) - 1
+    return lo <= qb - 2 and hi >= 1
+
+
+@dataclass
+class Report:
+    n: int = 0
+    exact: int = 0
+    exempt: int = 0
+    failures: list = field(default_factory=list)
+
+    def fail(self, msg):
+        if len(self.failures) < 20:
+            self.failures.append(msg)
+
+    def ok(self):
+        return not self.failures
+
+    def __str__(self):
+        return (f"{self.n} queries, {self.exact} identical, {self.exempt} tie-exempt "
+                f"({100.0 * self.exempt / max(1, self.n):.2f}%), failures: {self.failures}")
+
+
+def check_structure(idx, score, t, C, K, rep, tag):
+    qb = t // C
+    real = idx[idx >= 0]
+    F = {0, qb - 1, qb} & set(range(qb + 1))
+    n_e = max(0, qb - 2)
+    if (idx[len(real):] != -1).any() or (np.diff(real) <= 0).any():
+        rep.fail(f"{tag}: not ascending/-1 padded: {idx}")
+        return False
+    if len(real) and real.max() > qb:
+        rep.fail(f"{tag}: non-causal block {real.max()} > qb={qb}")
+        return False
+    if not F <= set(real.tolist()):
+        rep.fail(f"{tag}: forced blocks {F} missing from {real}")
+        return False
+    if len(real) != len(F) + min(K, n_e):
+        rep.fail(f"{tag}: {len(real)} blocks, want {len(F) + min(K, n_e)}")
+        return False
+    if score is not None:
+        for j, x in zip(real, score[:len(real)]):
+            if (x == math.inf) != (j in F):
+                rep.fail(f"{tag}: forced/score mismatch at block {j}: {x}")
+                return False
+        if (score[len(real):] != -math.inf).any():
+            rep.fail(f"{tag}: padding scores not -inf")
+            return False
+    return True
+
+
+def check_trace(o, qn, kn, pyr, b, h, t, trace_row, gpu_idx, gpu_score, rep, tag, qmode="full",
+                length=None):
+    """Level-by-level validation of one query from the GPU's trace.
+    qmode: "full" (qn is [B, Hq, N, d]), "decode" (qn is [B, Hq, d]) or
+    "rows" (qn is this query's [G, d] head rows)."""
+    C, K = o.C, o.K
+    N = o.N if length is None else length
+    qb = t // C
+    sizes = level_sizes(-(-N // C))
+    L = len(sizes)
+    kw = {}
+    if qmode == "decode":
+        kw = dict(len_=length, decode=True)
+    elif qmode == "rows":
+        kw = dict(qrows=True)
+    prev = None
+    for level in range(L, 1, -1):
+        kept = [int(x) for x in trace_row[level - 1] if x >= 0]
+        if prev is None:
+            cands = [j for j in range(sizes[level - 1]) if eligible(level, j, qb)]
+        else:
+            cands = [c for p in prev for c in (2 * p, 2 * p + 1)
+                     if c < sizes[level - 1] and eligible(level, c, qb)]
+        if len(cands) <= K:
+            if sorted(kept) != sorted(cands):
+                rep.fail(f"{tag}: level {level} keep-all set {kept} != {cands}")
+                return False
+        else:
+            if len(kept) != K or not set(kept) <= set(cands):
+                rep.fail(f"{tag}: level {level} kept {kept} not K of {cands}")
+                return False
+            sc = dict(zip(cands, o.score_nodes(qn, kn, pyr, b, h, t, level, cands, **kw)))
+            lo = min(sc[j] for j in kept)
+            hi = max(sc[j] for j in cands if j not in kept)
+            if lo < hi - TIE:
+                rep.fail(f"{tag}: level {level} kept score {lo:.6f} < dropped {hi:.6f} - tie")
+                return False
+        prev = kept
+    # leaves
+    cands = [c for p in prev for c in (2 * p, 2 * p + 1) if c < sizes[0] and eligible(1, c, qb)]
+    F = {0, qb - 1, qb} & set(range(qb + 1))
+    top = [int(j) for j in gpu_idx if j >= 0 and j not in F]
+    if not set(top) <= set(cands) or len(top) != min(K, len(cands)):
+        rep.fail(f"{tag}: leaves {top} not Top-{K} of candidates {cands}")
+        return False
+    if cands:
+        sc = dict(zip(cands, o.score_nodes(qn, kn, pyr, b, h, t, 1, cands, **kw)))
+        if len(cands) > K:
+            lo = min(sc[j] for j in top)
+            hi = max(sc[j] for j in cands if j not in top)
+            if lo < hi - TIE:
+                rep.fail(f"{tag}: leaf kept {lo:.6f} < dropped {hi:.6f} - tie")
+                return False
+        if gpu_score is not None:
+            for j, x in zip(gpu_idx, gpu_score):
+                if j >= 0 and j not in F and abs(x - sc[int(j)]) > SCORE_TOL:
+                    rep.fail(f"{tag}: leaf {j} score {x:.6f} vs oracle {sc[int(j)]:.6f}")
+                    return False
+    return True
+
+
+def compare(o, qn, kn, pyr, ref, gpu_idx, gpu_score, gpu_trace, keys, rep, qmode="full", lengths=None):
+    """keys: list of (b, h, t) for the rows of ref / gpu arrays.  In "rows"
+    mode qn is [len(keys), G, d], the head rows of each key's query."""
+    for i, (b, h, t) in enumerate(keys):
+        rep.n += 1
+        tag = f"(b={b},h={h},t={t})"
+        gi = np.asarray(gpu_idx[i])
+        gs = None if gpu_score is None else np.asarray(gpu_score[i], np.float64)
+        if not check_structure(gi, gs, t, o.C, o.K, rep, tag):
+            continue
+        if (gi == ref["idx"][i]).all():
+            rep.exact += 1
+            if gs is not None:
+                want = ref["score"][i]
+                fin = np.isfinite(want)
+                if not (np.isinf(gs) == ~fin).all() or (np.abs(gs[fin] - want[fin]) > SCORE_TOL).any():
+                    rep.fail(f"{tag}: scores {gs} vs oracle {want}")
+            continue
+        if ref["margin"][i] >= TIE:
+            rep.fail(f"{tag}: index set {gi.tolist()} != oracle {ref['idx'][i].tolist()} "
+                     f"with margin {ref['margin'][i]:.3g}")
+            continue
+        rep.exempt += 1
+        if gpu_trace is None:
+            rep.fail(f"{tag}: tie-exempt query without a trace")
+            continue
+        length = None if lengths is None else lengths[b]
+        qsrc = qn[i] if qmode == "rows" else qn
+        check_trace(o, qsrc, kn, pyr, b, h, t, gpu_trace[i], gi, gs, rep, tag, qmode=qmode,
+                    length=length)
+    return rep

@@ -1,0 +1,93 @@
+"""The C-ABI library loads, exports every entry point that include/pisa.h
+declares, and rejects bad arguments on the host before any launch (these
+calls never reach the GPU, so they run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pisa():
+    from pyramid_top_block_mean_gb300 import build
+    build.build()
+    from pyramid_top_block_mean_gb300 import pisa as m
+    return m
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "pisa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pisa_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(pisa):
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(pisa.lib(), n), n
+    assert set(names) == set(pisa.EXPORTED)
+
+
+def test_abi_version_and_status_strings(pisa):
+    assert pisa.abi_version() == 1
+    for code in range(-6, 1):
+        assert pisa.status_string(code).startswith(pisa.STATUS_NAMES[code])
+
+
+def test_size_queries_match_the_pyramid_shape(pisa):
+    import oracle
+    for N in [1, 63, 64, 65, 1000, 4096, 4096 + 37, 16384, 262144]:
+        p = pisa.make_params(2, N, 16, 4, 128, K=8)
+        assert pisa.pyramid_nodes(p) == oracle.lib().po_num_nodes(N, 64)
+        assert pisa.pyramid_levels(p) == oracle.lib().po_num_levels(N, 64)
+        assert pisa.pyramid_bytes(p) == 2 * 4 * pisa.pyramid_nodes(p) * 128 * 4
+        for mode in (0, 1, 2):
+            assert pisa.workspace_bytes(p, mode) >= 256
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("H_q", 15, -1), ("H_kv", 0, -1), ("K", 0, -1), ("N", -1, -1), ("B", -1, -1), ("qtile", 0, -1),
+    ("scale", -1.0, -1), ("d", 96, -2), ("C", 32, -2), ("g", 3, -2), ("K", 33, -2), ("dtype", 7, -2),
+    ("H_q", 48, -2),  # G = 12
+    ("N", (1 << 26) + 1, -2), ("struct_size", 8, -1),
+])
+def test_bad_params_are_rejected(pisa, field, value, code):
+    p = pisa.make_params(1, 4096, 16, 4, 128, K=8)
+    setattr(p, field, value)
+    assert pisa.workspace_bytes(p, 0) == 0
+    assert pisa.pyramid_nodes(p) == 0
+    fake = ctypes.c_void_p(0x10000)
+    rc = pisa.lib().pisa_select_prefill(ctypes.byref(p), fake, fake, fake, fake, 1 << 40, fake, None, None, None)
+    assert rc == code
+
+
+def test_null_misaligned_and_small_workspace_rejected_before_launch(pisa):
+    L = pisa.lib()
+    p = pisa.make_params(1, 4096, 16, 4, 128, K=8)
+    a = ctypes.c_void_p(0x10000)
+    mis = ctypes.c_void_p(0x10008)
+    big = 1 << 40
+    ws_need = pisa.workspace_bytes(p, 0)
+    assert L.pisa_select_prefill(ctypes.byref(p), None, a, a, a, big, a, None, None, None) == -1
+    assert L.pisa_select_prefill(ctypes.byref(p), mis, a, a, a, big, a, None, None, None) == -3
+    assert L.pisa_select_prefill(ctypes.byref(p), a, a, a, a, ws_need - 1, a, None, None, None) == -4
+    assert L.pisa_build_pyramid(ctypes.byref(p), None, None, a, None) == -1
+    assert L.pisa_build_pyramid(ctypes.byref(p), mis, None, a, None) == -3
+    assert L.pisa_select_decode(ctypes.byref(p), a, a, None, a, a, big, a, None, None, None) == -1
+    assert L.pisa_select_decode(ctypes.byref(p), a, a, a, a, a, 16, a, None, None, None) == -4
+    assert L.pisa_select_flat(ctypes.byref(p), a, a, a, 16, a, None, None) == -4
+    assert L.pisa_select_flat(ctypes.byref(p), a, mis, a, big, a, None, None) == -3
+    code = ctypes.c_int32(0)
+    assert L.pisa_read_device_status(None, ctypes.byref(code), None) == -1
+
+
+def test_empty_problems_are_no_ops(pisa):
+    L = pisa.lib()
+    for B, N in [(0, 4096), (1, 0)]:
+        p = pisa.make_params(B, N, 16, 4, 128, K=8)
+        assert L.pisa_select_prefill(ctypes.byref(p), None, None, None, None, 0, None, None, None, None) == 0
+        assert L.pisa_build_pyramid(ctypes.byref(p), None, None, None, None) == 0
