@@ -1,9 +1,504 @@
-// leaf_tc.cu -- (placeholder while the tensor-core leaf kernel is written)
+// leaf_tc.cu -- leaf LSE scoring on the tcgen05 tensor cores, and the final
+// Top-K.  agihunt.info summary of "Block Sparse Attention with Log-Linear
+// Complexity", kernel paragraph: stage 2 of prefill scores the leaves with
+// LSE over their raw keys, grouping the queries that need the same leaf so
+// each leaf key tile is loaded once (Qtile), without materialising a dense
+// score matrix; rcap.io post, kernel paragraph (two-stage prefill).
+//
+// GB300 design.  A query's leaf candidates come in sibling pairs: the two
+// leaves under each kept level-2 node.  Pairs (query, kept level-2 node p)
+// are counting-sorted by (sequence, key head, query chunk, p).  One tile is
+// 128 rows = 128/G queries x G heads of one bucket against the 128 keys of
+// leaves 2p and 2p+1:
+//   - TMA brings the 128 x d bf16 key tile into shared memory (128-byte
+//     swizzle) once per bucket and it stays there for all of that bucket's
+//     consecutive tiles;
+//   - the producer warp gathers the 128 query-head rows with cp.async into
+//     the same swizzled K-major layout;
+//   - one thread issues tcgen05.mma (M = 128, N = 128, K = d) into a TMEM
+//     accumulator (two accumulators alternate);
+//   - four epilogue warps read their 32 TMEM lanes each, take the per-row
+//     log2-sum-exp2 over each leaf's 64 columns, sum the G head rows of a
+//     query, and write two scores per pair.  No score matrix reaches HBM.
+// Persistent CTAs (one per SM) walk the tile list in interleaved groups of
+// four consecutive tiles, so all SMs sweep the same query chunk together.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "pisa_common.cuh"
 #include "pisa_internal.h"
+#include "tc_ptx.cuh"
+
 namespace pisa {
-cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, char* ws, const void* q,
-                           const void* k, int32_t* out_idx, float* out_score, int, cudaStream_t st) {
-  return launch_leaf_simt(pr, s, q, k, (const int32_t*)(ws + w.kept2), out_idx, out_score, st);
+
+constexpr int kTileRows = 128;  // MMA M: queries x heads
+constexpr int kTileKeys = 128;  // MMA N: leaves 2p and 2p+1
+constexpr int kStages = 2;
+constexpr int kGroup = 4;
+constexpr int kLeafTcThreads = 192;  // warp 0 loads, warp 1 MMA, warps 2-5 epilogue
+constexpr uint32_t kTmemCols = 256;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+template <int D>
+struct LeafTcSmem {
+  uint8_t a[kStages][kTileRows * D * 2];
+  uint8_t b[kStages][kTileKeys * D * 2];
+  uint64_t full_a[kStages], empty_a[kStages], full_b[kStages], empty_b[kStages];
+  uint64_t tfull[2], tempty[2], done;
+  uint32_t tmem_base;
+  int32_t abort;
+  int32_t zero;  // stays 0: a wait that must not give up early on abort
+};
+
+// ---------------------------------------------------------------- bucketing
+struct BucketArgs {
+  int64_t nq, N, n2, nchunk;
+  int32_t K;
+};
+
+__device__ __forceinline__ int64_t bucket_of(const BucketArgs& a, int64_t qi, int32_t p) {
+  const int64_t t = qi % a.N, bh = qi / a.N;
+  return ((bh * a.nchunk) + (t >> kChunkShift)) * a.n2 + p;
 }
+
+__global__ void count_kernel(BucketArgs a, const int32_t* __restrict__ kept2, int32_t* __restrict__ counts) {
+  const int64_t n = a.nq * a.K;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t p = kept2[i];
+    if (p >= 0) atomicAdd(&counts[bucket_of(a, i / a.K, p)], 1);
+  }
+}
+
+// Exclusive scans of the pair counts and of the tiles per bucket (one CTA).
+__global__ void __launch_bounds__(1024) scan_kernel(int64_t nb, int32_t Q, const int32_t* __restrict__ counts,
+                                                    int32_t* __restrict__ offsets, int32_t* __restrict__ tile_off) {
+  __shared__ int32_t sp[1024], st[1024];
+  const int tid = threadIdx.x;
+  const int64_t per = ceil_div64(nb, 1024);
+  const int64_t lo = tid * per, hi = lo + per < nb ? lo + per : nb;
+  int32_t ps = 0, ts = 0;
+  for (int64_t i = lo; i < hi; ++i) { ps += counts[i]; ts += (counts[i] + Q - 1) / Q; }
+  sp[tid] = ps; st[tid] = ts;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {
+    const int32_t a = tid >= o ? sp[tid - o] : 0, b = tid >= o ? st[tid - o] : 0;
+    __syncthreads();
+    sp[tid] += a; st[tid] += b;
+    __syncthreads();
+  }
+  int32_t pb = sp[tid] - ps, tb = st[tid] - ts;
+  for (int64_t i = lo; i < hi; ++i) {
+    offsets[i] = pb; tile_off[i] = tb;
+    pb += counts[i]; tb += (counts[i] + Q - 1) / Q;
+  }
+  if (tid == 1023) { offsets[nb] = sp[1023]; tile_off[nb] = st[1023]; }
+}
+
+__global__ void scatter_kernel(BucketArgs a, const int32_t* __restrict__ kept2, const int32_t* __restrict__ offsets,
+                               int32_t* __restrict__ cursor, int32_t* __restrict__ pairs) {
+  const int64_t n = a.nq * a.K;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t p = kept2[i];
+    if (p < 0) continue;
+    const int64_t qi = i / a.K;
+    const int64_t bk = bucket_of(a, qi, p);
+    const int32_t pos = offsets[bk] + atomicAdd(&cursor[bk], 1);
+    pairs[pos] = (int32_t)(((qi % a.N) << 5) | (i % a.K));
+  }
+}
+
+__global__ void tiles_kernel(int64_t nb, int32_t Q, const int32_t* __restrict__ counts,
+                             const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_off,
+                             int4* __restrict__ tile_info) {
+  for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < nb; j += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t n = counts[j], t0 = tile_off[j], p0 = offsets[j];
+    for (int32_t i = 0; i * Q < n; ++i)
+      tile_info[t0 + i] = make_int4((int32_t)j, p0 + i * Q, min(Q, n - i * Q), 0);
+  }
+}
+
+// ------------------------------------------------------------ tile schedule
+struct TileIter {
+  int T, i, gend, g;
+  __device__ TileIter(int total) : T(total), g(blockIdx.x) {
+    i = g * kGroup;
+    gend = min(T, i + kGroup);
+  }
+  __device__ bool valid() const { return i < T; }
+  __device__ void next() {
+    if (++i >= gend) {
+      g += gridDim.x;
+      i = g * kGroup;
+      gend = min(T, i + kGroup);
+    }
+  }
+  __device__ int peek() const {  // the tile after this one, or -1
+    if (i + 1 < gend) return i + 1;
+    const int j = (g + (int)gridDim.x) * kGroup;
+    return j < T ? j : -1;
+  }
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kLeafTcThreads, 1)
+    leaf_tc_kernel(Prob pr, int64_t n2, int64_t nchunk, const __grid_constant__ CUtensorMap kmap,
+                   const uint16_t* __restrict__ q, const int4* __restrict__ tile_info,
+                   const int32_t* __restrict__ tile_total, const int32_t* __restrict__ pairs,
+                   float* __restrict__ leaf_score, int32_t* __restrict__ status) {
+  extern __shared__ unsigned char smem_raw[];
+  LeafTcSmem<D>& sm = *reinterpret_cast<LeafTcSmem<D>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int kHalf = kTileRows * 128;  // bytes of one 64-element K slice
+  constexpr uint32_t kBBytes = kTileKeys * D * 2;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileRows, kTileKeys);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  volatile int32_t* abort = &sm.abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&sm.full_a[s]), 32);
+      ptx::mbar_init(ptx::smem_u32(&sm.empty_a[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sm.full_b[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sm.empty_b[s]), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&sm.tfull[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sm.tempty[s]), 4);
+    }
+    ptx::mbar_init(ptx::smem_u32(&sm.done), 1);
+    sm.abort = 0;
+    sm.zero = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&sm.tmem_base), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const int T = *tile_total;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    constexpr int CPR = D / 8;     // 16-byte chunks per row
+    constexpr int RPI = 32 / CPR;  // rows per warp instruction
+    const int ch = lane % CPR;
+    int it = 0, bcount = 0, last_bucket = -1, prev_sa = -1;
+    bool ok = true;
+    for (TileIter ti(T); ti.valid() && ok; ti.next()) {
+      const int4 info = tile_info[ti.i];
+      const int64_t bucket = info.x;
+      const int64_t p = bucket % n2;
+      const int64_t bh = (bucket / n2) / nchunk;
+      const int64_t b = bh / pr.Hkv, h = bh % pr.Hkv;
+      const int sa = it & 1, use = it >> 1;
+      ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_a[sa]), (use & 1) ^ 1, abort, kWaitLimitNs);
+      if (!ok) break;
+      if (info.x != last_bucket) {
+        const int sb = bcount & 1, ub = bcount >> 1;
+        int okb = 1;
+        if (lane == 0) {
+          okb = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_b[sb]), (ub & 1) ^ 1, abort, kWaitLimitNs);
+          if (okb) {
+            const uint32_t fb = ptx::smem_u32(&sm.full_b[sb]);
+            ptx::mbar_arrive_expect_tx(fb, kBBytes);
+            const int32_t y = (int32_t)(bh * pr.N + 128 * p);
+#pragma unroll
+            for (int hh = 0; hh < D / 64; ++hh)
+              ptx::tma_load_2d(ptx::smem_u32(sm.b[sb]) + hh * kHalf, &kmap, 64 * hh, y, fb);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, okb, 0) != 0;
+        if (!ok) break;
+        ++bcount;
+        last_bucket = info.x;
+      }
+      // gather the tile's 128 query-head rows
+      const uint32_t abase = ptx::smem_u32(sm.a[sa]);
+      const int cnt = info.z;
+      for (int r0 = 0; r0 < kTileRows; r0 += RPI) {
+        const int r = r0 + lane / CPR;
+        const int qr = r / G;
+        if (qr < cnt) {
+          const int32_t pe = pairs[info.y + qr];
+          const int64_t t = pe >> 5;
+          const int g = r % G;
+          const uint16_t* src = q + (((b * pr.Hq + h * G + g) * pr.N + t) * D + ch * 8);
+          const uint32_t dst = abase + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+          ptx::cp_async_16(dst, src);
+        }
+      }
+      ptx::cp_async_commit();
+      if (prev_sa >= 0) {
+        ptx::cp_async_wait<1>();
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[prev_sa]));
+      }
+      prev_sa = sa;
+      ++it;
+    }
+    ptx::cp_async_wait<0>();
+    ptx::fence_proxy_async_smem();
+    if (ok && prev_sa >= 0) ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[prev_sa]));
+    if (!ok) {
+      *abort = 1;
+      // let TMA loads already issued land before the CTA can exit
+      if (lane == 0)
+        for (int k = bcount > 2 ? bcount - 2 : 0; k < bcount; ++k)
+          ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k & 1]), (k >> 1) & 1, &sm.zero, kWaitLimitNs);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int it = 0, bcount = 0, last_bucket = -1, sb = 0;
+      bool ok = true;
+      for (TileIter ti(T); ti.valid(); ti.next()) {
+        const int4 info = tile_info[ti.i];
+        const int sa = it & 1, use = it >> 1, acc = it & 1;
+        if (info.x != last_bucket) {
+          sb = bcount & 1;
+          ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[sb]), (bcount >> 1) & 1, abort, kWaitLimitNs);
+          if (!ok) break;
+          ++bcount;
+          last_bucket = info.x;
+        }
+        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_a[sa]), use & 1, abort, kWaitLimitNs) &&
+             ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tempty[acc]), (use & 1) ^ 1, abort, kWaitLimitNs);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t d = tmem + acc * kTileKeys;
+        const uint32_t a0 = ptx::smem_u32(sm.a[sa]), b0 = ptx::smem_u32(sm.b[sb]);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+          ptx::mma_bf16(d, ptx::desc_sw128(a0 + off), ptx::desc_sw128(b0 + off), kIdesc, k > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(ptx::smem_u32(&sm.empty_a[sa]));
+        ptx::mma_commit(ptx::smem_u32(&sm.tfull[acc]));
+        const int nx = ti.peek();
+        if (nx < 0 || tile_info[nx].x != info.x) ptx::mma_commit(ptx::smem_u32(&sm.empty_b[sb]));
+        ++it;
+      }
+      if (!ok) *abort = 1;
+      // every MMA has finished before TMEM is released
+      ptx::mma_commit(ptx::smem_u32(&sm.done));
+      ptx::mbar_wait_bounded(ptx::smem_u32(&sm.done), 0, &sm.zero, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;  // TMEM lane quadrant this warp may read
+    const int r = q4 * 32 + lane;
+    const float sc = pr.scale2;
+    int it = 0;
+    for (TileIter ti(T); ti.valid(); ti.next()) {
+      const int4 info = tile_info[ti.i];
+      const int acc = it & 1, use = it >> 1;
+      const bool okw = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tfull[acc]), use & 1, abort, kWaitLimitNs);
+      if (!__all_sync(0xffffffffu, okw)) { *abort = 1; break; }
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + acc * kTileKeys;
+      float lse[2];
+#pragma unroll
+      for (int leaf = 0; leaf < 2; ++leaf) {
+        uint32_t v0[32], v1[32];
+        ptx::tmem_ld32(taddr + leaf * 64, v0);
+        ptx::tmem_ld32(taddr + leaf * 64 + 32, v1);
+        ptx::tmem_ld_wait();
+        float x[64];
+        float m = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          x[j] = __uint_as_float(v0[j]) * sc;
+          x[32 + j] = __uint_as_float(v1[j]) * sc;
+        }
+#pragma unroll
+        for (int j = 0; j < 64; ++j) m = fmaxf(m, x[j]);
+        float s0 = 0.0f, s1 = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 64; j += 2) {
+          s0 += ptx::ex2(x[j] - m);
+          s1 += ptx::ex2(x[j + 1] - m);
+        }
+        lse[leaf] = m + ptx::lg2(s0 + s1);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[acc]));
+#pragma unroll
+      for (int o = 1; o < G; o <<= 1) {
+        lse[0] += __shfl_xor_sync(0xffffffffu, lse[0], o);
+        lse[1] += __shfl_xor_sync(0xffffffffu, lse[1], o);
+      }
+      const int qr = r / G;
+      if ((r % G) == 0 && qr < info.z) {
+        const int64_t bh = (info.x / n2) / nchunk;
+        const int32_t pe = pairs[info.y + qr];
+        const int64_t t = pe >> 5, slot = pe & 31;
+        *reinterpret_cast<float2*>(leaf_score + ((bh * pr.N + t) * pr.K + slot) * 2) = make_float2(lse[0], lse[1]);
+      }
+      ++it;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (threadIdx.x == 0 && sm.abort) set_status(status, PISA_DEV_TIMEOUT);
+}
+
+// -------------------------------------------------------------- finalize
+// One warp per query: Top-K of its eligible candidate leaves (group LSE,
+// ties to the lower index) together with the forced blocks, ascending.
+__global__ void __launch_bounds__(256) finalize_kernel(Prob pr, const int32_t* __restrict__ kept2,
+                                                       const float* __restrict__ leaf_score,
+                                                       int32_t* __restrict__ out_idx, float* __restrict__ out_score) {
+  const int lane = threadIdx.x & 31;
+  const int64_t qi = (int64_t)blockIdx.x * 8 + threadIdx.x / 32;
+  if (qi >= pr.B * pr.Hkv * pr.N) return;
+  const int64_t t = qi % pr.N;
+  const int64_t qb = t / pr.C;
+  const int K = pr.K, W = K + 3, nc = 2 * K;
+  float sc[2];
+  int32_t lf[2];
+  bool val[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int c = lane + 32 * j;
+    val[j] = false; sc[j] = -INFINITY; lf[j] = -1;
+    if (c < nc) {
+      const int32_t p = kept2[qi * K + (c >> 1)];
+      if (p >= 0) {
+        lf[j] = 2 * p + (c & 1);
+        val[j] = node_eligible(1, lf[j], qb);
+        if (val[j]) sc[j] = leaf_score[(qi * K + (c >> 1)) * 2 + (c & 1)];
+      }
+    }
+  }
+  int rank[2] = {0, 0};
+  const int rounds = nc > 32 ? 2 : 1;
+  for (int jr = 0; jr < rounds; ++jr) {
+    for (int src = 0; src < 32; ++src) {
+      const float so = __shfl_sync(0xffffffffu, sc[jr], src);
+      const int32_t lo = __shfl_sync(0xffffffffu, lf[jr], src);
+      const bool vo = __shfl_sync(0xffffffffu, val[jr] ? 1 : 0, src) != 0;
+      if (!vo) continue;
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        if (val[j] && beats(so, lo, sc[j], lf[j])) ++rank[j];
+    }
+  }
+  int32_t* oi = out_idx + qi * W;
+  float* os = out_score ? out_score + qi * W : nullptr;
+  int nkept = 0;
+  for (int j = 0; j < rounds; ++j) {
+    const bool keep = val[j] && rank[j] < K;
+    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+    if (keep) {
+      const int pos = 1 + nkept + __popc(bal & ((1u << lane) - 1));
+      oi[pos] = lf[j];
+      if (os) os[pos] = sc[j] * kLn2;
+    }
+    nkept += __popc(bal);
+  }
+  if (lane == 0) {
+    oi[0] = 0;
+    if (os) os[0] = INFINITY;
+    int pos = 1 + nkept;
+    if (qb - 1 > 0) { oi[pos] = (int32_t)(qb - 1); if (os) os[pos] = INFINITY; ++pos; }
+    if (qb > 0) { oi[pos] = (int32_t)qb; if (os) os[pos] = INFINITY; ++pos; }
+    for (; pos < W; ++pos) { oi[pos] = -1; if (os) os[pos] = -INFINITY; }
+  }
+}
+
+// ------------------------------------------------------------------ host
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D view [rows, d] of a bf16 [.., d] tensor; box = 64 columns x box_rows,
+// 128-byte swizzle (the K-major operand layout of the MMA).
+bool make_tmap_rows(CUtensorMap* m, const void* base, int64_t rows, int d, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D, int G>
+static cudaError_t launch_leaf_tc_t(const Prob& pr, const PrefillWs& w, char* ws, const CUtensorMap& kmap,
+                                    const void* q, int grid, cudaStream_t st) {
+  const size_t smem = sizeof(LeafTcSmem<D>) + 1024;
+  auto kern = leaf_tc_kernel<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kLeafTcThreads, smem, st>>>(pr, w.n2, w.nchunk, kmap, (const uint16_t*)q,
+                                           (const int4*)(ws + w.tile_info),
+                                           (const int32_t*)(ws + w.tile_off) + w.nbuckets,
+                                           (const int32_t*)(ws + w.pairs), (float*)(ws + w.leaf_score),
+                                           (int32_t*)(ws + w.status));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, char* ws, const void* q,
+                           const void* k, int32_t* out_idx, float* out_score, int num_sms, cudaStream_t st) {
+  const int64_t nq = pr.B * pr.Hkv * pr.N;
+  const int32_t* kept2 = (const int32_t*)(ws + w.kept2);
+  cudaError_t e;
+  if (w.nbuckets > 0) {
+    const int32_t Q = kTileRows / pr.G;
+    BucketArgs a{nq, pr.N, w.n2, w.nchunk, pr.K};
+    int32_t* counts = (int32_t*)(ws + w.counts);
+    int32_t* offsets = (int32_t*)(ws + w.offsets);
+    int32_t* cursor = (int32_t*)(ws + w.cursor);
+    int32_t* tile_off = (int32_t*)(ws + w.tile_off);
+    // counts, offsets and cursor are contiguous: clear all three at once
+    e = cudaMemsetAsync(counts, 0, w.tile_off - w.counts, st);
+    if (e != cudaSuccess) return e;
+    const int64_t n = nq * pr.K;
+    const unsigned g1 = (unsigned)std::min<int64_t>(ceil_div64(n, 256), (int64_t)num_sms * 16);
+    count_kernel<<<g1, 256, 0, st>>>(a, kept2, counts);
+    scan_kernel<<<1, 1024, 0, st>>>(w.nbuckets, Q, counts, offsets, tile_off);
+    scatter_kernel<<<g1, 256, 0, st>>>(a, kept2, offsets, cursor, (int32_t*)(ws + w.pairs));
+    const unsigned g2 = (unsigned)std::min<int64_t>(ceil_div64(w.nbuckets, 256), (int64_t)num_sms * 8);
+    tiles_kernel<<<g2, 256, 0, st>>>(w.nbuckets, Q, counts, offsets, tile_off, (int4*)(ws + w.tile_info));
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap kmap;
+    if (!make_tmap_rows(&kmap, k, pr.B * pr.Hkv * pr.N, pr.d, kTileKeys)) return cudaErrorInvalidValue;
+    const int grid = num_sms > 0 ? num_sms : 148;
+#define PISA_LEAF_TC_CASE(DD, GG) \
+    if (pr.d == DD && pr.G == GG) e = launch_leaf_tc_t<DD, GG>(pr, w, ws, kmap, q, grid, st); else
+    PISA_LEAF_TC_CASE(128, 1) PISA_LEAF_TC_CASE(128, 2) PISA_LEAF_TC_CASE(128, 4) PISA_LEAF_TC_CASE(128, 8)
+    PISA_LEAF_TC_CASE(64, 1) PISA_LEAF_TC_CASE(64, 2) PISA_LEAF_TC_CASE(64, 4) PISA_LEAF_TC_CASE(64, 8)
+    e = cudaErrorInvalidValue;
+#undef PISA_LEAF_TC_CASE
+    if (e != cudaSuccess) return e;
+  }
+  finalize_kernel<<<(unsigned)ceil_div64(nq, 8), 256, 0, st>>>(pr, kept2, (const float*)(ws + w.leaf_score),
+                                                              out_idx, out_score);
+  return cudaGetLastError();
+}
+
 }  // namespace pisa

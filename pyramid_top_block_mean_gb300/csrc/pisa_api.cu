@@ -39,7 +39,10 @@ PrefillWs prefill_ws_layout(const Prob& pr, const Pyr& s) {
   PrefillWs w{};
   const int64_t nq = pr.B * pr.Hkv * pr.N;
   const int64_t n2 = s.L >= 2 ? s.size[1] : 0;
-  w.nbuckets = pr.B * pr.Hkv * n2;
+  w.n2 = n2;
+  w.nchunk = ceil_div64(pr.N, (int64_t)1 << kChunkShift);
+  w.nbuckets = pr.B * pr.Hkv * w.nchunk * n2;
+  w.max_tiles = w.nbuckets + ceil_div64(nq * pr.K, 128 / 8);
   size_t o = 0;
   w.status = o; o += 256;
   w.kept2 = o; o = align_up(o + (size_t)nq * pr.K * 4, 256);
@@ -49,6 +52,7 @@ PrefillWs prefill_ws_layout(const Prob& pr, const Pyr& s) {
   w.cursor = o; o = align_up(o + (size_t)(w.nbuckets + 1) * 4, 256);
   w.tile_off = o; o = align_up(o + (size_t)(w.nbuckets + 1) * 4, 256);
   w.pairs = o; o = align_up(o + (size_t)nq * pr.K * 4, 256);
+  w.tile_info = o; o = align_up(o + (size_t)w.max_tiles * 16, 256);
   w.total = o;
   return w;
 }
@@ -172,6 +176,8 @@ pisa_status pisa_select_prefill(const pisa_params* p, const void* q, const void*
   if (((uintptr_t)out_idx & 3u) || ((uintptr_t)out_score & 3u) || ((uintptr_t)trace & 3u))
     return PISA_ERR_MISALIGNED;
   if (ws_bytes < w.total) return PISA_ERR_WORKSPACE;
+  // pair counts and TMA row coordinates are 32-bit
+  if (pr.B * pr.Hkv * pr.N * pr.K >= ((int64_t)1 << 31)) return PISA_ERR_UNSUPPORTED;
   cudaStream_t st = (cudaStream_t)stream;
   char* base = (char*)ws;
   int32_t* status = (int32_t*)(base + w.status);

@@ -8,6 +8,11 @@
 
 namespace pisa {
 
+// Pairs (query, kept level-2 node) are bucketed by (sequence, key head,
+// query chunk of 2^kChunkShift positions, level-2 node) so that the leaf
+// stage sweeps one chunk of queries at a time and their rows stay in L2.
+constexpr int kChunkShift = 16;
+
 // Workspace layout of one call (byte offsets from the workspace base).
 struct PrefillWs {
   size_t status;      // int32 status word (first 256 bytes)
@@ -17,9 +22,13 @@ struct PrefillWs {
   size_t offsets;     // int32 [nbuckets + 1] exclusive scan of counts
   size_t cursor;      // int32 [nbuckets]
   size_t tile_off;    // int32 [nbuckets + 1] exclusive scan of tiles per bucket
-  size_t pairs;       // int32 [B * Hkv * N * K] (t * K + slot) grouped by bucket
+  size_t pairs;       // int32 [B * Hkv * N * K] (t << 5 | slot) grouped by bucket
+  size_t tile_info;   // int4  [max_tiles] {bucket, first pair, pairs, 0}
   size_t total;
-  int64_t nbuckets;   // B * Hkv * n_2
+  int64_t nbuckets;   // B * Hkv * nchunk * n_2
+  int64_t nchunk;     // ceil(N / 2^kChunkShift)
+  int64_t n2;         // level-2 nodes
+  int64_t max_tiles;  // nbuckets + B * Hkv * N * K / Q, Q the smallest tile
 };
 
 bool make_pyr(int64_t N, int32_t C, Pyr* s);
