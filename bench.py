@@ -1,0 +1,499 @@
+"""Benchmark of the pyramid Top-K block selector on one GB300 (or N replicas).
+
+Default workload: the long-prefill point of the sweep, 262144 tokens, B = 1,
+16 query / 4 key heads, d = 128, bf16, C = 64, g = 2, K = 8, iid N(0, 1)
+inputs.  One step = pyramid build + routing + leaf LSE + Top-K for every
+query position (the whole prefill selector).  Inputs (1.3 GB) are larger
+than L2, so no flush is needed between steps.
+
+Prints one JSON line.  value = whole-job queries/s (query positions selected
+per second, summed over ranks).  `--impl reference` times the fp64 CPU
+oracle (the only reference this method has) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "PISA selection ms and queries/s at 64K/128K/256K; % of HBM/tensor roofline"
+UNIT = "queries/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["pisa", "reference"], default="pisa")
+    ap.add_argument("--N", type=int, default=262144)
+    ap.add_argument("--no-extras", action="store_true", help="skip the sweep, flat and decode side measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ ranks
+def dist_setup(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("PISA_BENCH_BACKEND", "nccl")
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def reduce_max(x: float, ws: int) -> float:
+    """Max of a float over ranks (identity for one rank)."""
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_rate(units_per_rank: float, ws: int, seconds_max: float) -> float:
+    """Weak scaling: every rank processes its own batch of `units_per_rank`."""
+    return units_per_rank * ws / seconds_max
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads
+def workload(N: int, rank: int):
+    from pyramid_top_block_mean_gb300 import workloads as W
+    s = W.sweep(N)
+    q, k = W.iid(s, 3 + 1000 * rank)
+    return s, q, k
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained"),
+                    sm_max_mhz=d.get("sm_max_mhz", 2070.0), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, sm_max_mhz=2070.0, source="fallback")
+
+
+def eligible_count(level, qb):
+    if qb - 2 < 1:
+        return 0
+    if level == 1:
+        return qb - 2
+    return ((qb - 2) >> (level - 1)) + 1
+
+
+def algorithmic_work(s, kept2):
+    """Exact leaf work from the routing output, plus the routing and byte
+    counts of the method ("algorithmic work")."""
+    import numpy as np
+    K, C, d, G = s.K, s.C, s.d, s.G
+    t = np.arange(s.N)
+    qb = t // C
+    kp = kept2.reshape(-1, s.N, K)  # [B*Hkv, N, K]
+    p = kp.astype(np.int64)
+    valid = p >= 0
+    leaf0, leaf1 = 2 * p, 2 * p + 1
+    e_hi = (qb - 2)[None, :, None]
+    ncand = ((valid & (leaf0 >= 1) & (leaf0 <= e_hi)).sum() + (valid & (leaf1 >= 1) & (leaf1 <= e_hi)).sum())
+    leaf_flops = 2.0 * d * G * C * float(ncand)
+    # routing: child dot products of the walk; every scored level has at most
+    # 2K candidates with at most 2 eligible children each
+    nb = -(-s.N // C)
+    L = 1
+    n = nb
+    while n > 1:
+        n = -(-n // 2)
+        L += 1
+    dots = 0
+    for qbv in range(nb):
+        l0 = 0
+        for level in range(L, 1, -1):
+            if eligible_count(level, qbv) > K:
+                l0 = level
+                break
+        if l0 == 0:
+            continue
+        per = eligible_count(l0 - 1, qbv) + sum(min(4 * K, 2 * eligible_count(lv - 1, qbv)) for lv in range(l0 - 1, 1, -1))
+        nq = min(C, s.N - qbv * C)
+        dots += per * nq
+    route_flops = 2.0 * d * G * dots * s.B * s.Hkv
+    P = 0
+    n = nb
+    while True:
+        P += n
+        if n == 1:
+            break
+        n = -(-n // 2)
+    bytes_ = (s.B * s.Hq * s.N * d * 2 + s.B * s.Hkv * s.N * d * 2 + 2 * s.B * s.Hkv * P * d * 4
+              + s.B * s.Hkv * s.N * (K + 3) * 8)
+    return dict(leaf_candidates=int(ncand), leaf_flops=leaf_flops, route_flops=route_flops, bytes=bytes_,
+                pyramid_bytes=s.B * s.Hkv * s.N * d * 2 + s.B * s.Hkv * P * d * 4)
+
+
+def load_traffic(name):
+    """dram bytes per launch of a kernel, from the committed ncu summary."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        return json.load(open(path)).get(name)
+    except (OSError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------- GPU arm
+def run_pisa(args, ws, rank, local):
+    import numpy as np
+    import torch
+    from pyramid_top_block_mean_gb300 import pisa
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    s, q_h, k_h = workload(args.N, rank)
+    q_h = q_h.pin_memory()
+    k_h = k_h.pin_memory()
+    p = pisa.params_from_shape(s)
+    sel = pisa.Selector(p, device=dev)
+    q = q_h.to(dev, non_blocking=True)
+    k = k_h.to(dev, non_blocking=True)
+    st = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+
+    def step():
+        pisa.build_pyramid(p, k, sel.pyramid, None, st)
+        pisa.prefill_route(p, q, sel.pyramid, sel.ws, None, st)
+        pisa.prefill_leaves(p, q, k, sel.ws, sel.out_idx, sel.out_score, st)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    assert sel.device_status(st) == 0
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    t_all0.record(st)
+    for i in range(args.steps):
+        e = ev[i]
+        e[0].record(st)
+        pisa.build_pyramid(p, k, sel.pyramid, None, st)
+        e[1].record(st)
+        pisa.prefill_route(p, q, sel.pyramid, sel.ws, None, st)
+        e[2].record(st)
+        pisa.prefill_leaves(p, q, k, sel.ws, sel.out_idx, sel.out_score, st)
+        e[3].record(st)
+    t_all1.record(st)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clk = clocks.stop()
+    total_ms = t_all0.elapsed_time(t_all1)
+    ms_step = total_ms / args.steps
+    stage = {nm: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+             for j, nm in enumerate(["build", "route", "leaves"])}
+    ms_max = reduce_max(ms_step, ws)
+    value = whole_job_rate(s.B * s.N, ws, ms_max / 1e3)
+
+    # algorithmic work of this input (outside the timed region)
+    kept2 = sel.ws[256:256 + s.B * s.Hkv * s.N * s.K * 4].view(torch.int32).cpu().numpy()
+    work = algorithmic_work(s, kept2)
+    pk = peaks()
+    t_roof_ms = max(work["bytes"] / (pk["hbm"] * 1e9), (work["leaf_flops"] + work["route_flops"]) /
+                    (pk["bf16_sus"] * 1e12)) * 1e3
+    # dominant stage and its roofline
+    dom = max(stage, key=stage.get)
+    if dom == "leaves":
+        achieved = work["leaf_flops"] / (stage["leaves"] * 1e-3) / 1e12
+        roof = {"kernel": "leaf stage (bucketing + leaf_tc_kernel + finalize)", "bound": "tensor",
+                "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
+                "frac": achieved / pk["bf16_sus"], "traffic": load_traffic("leaf_tc_kernel"),
+                "peak_source": f"{pk['source']} bf16 sustained"}
+    elif dom == "route":
+        fp32_peak = 152 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12
+        achieved = work["route_flops"] / (stage["route"] * 1e-3) / 1e12
+        roof = {"kernel": "route_kernel", "bound": "alu", "achieved": achieved, "peak": fp32_peak,
+                "unit": "TFLOP/s", "frac": achieved / fp32_peak, "traffic": load_traffic("route_kernel"),
+                "peak_source": "fp32 FMA: 152 SMs x 128 lanes x 2 flops x max SM clock"}
+    else:
+        achieved = work["pyramid_bytes"] / (stage["build"] * 1e-3) / 1e9
+        roof = {"kernel": "build_lower_kernel + build_upper_kernel", "bound": "hbm", "achieved": achieved,
+                "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
+                "traffic": load_traffic("build_lower_kernel"), "peak_source": f"{pk['source']} copy"}
+
+    # end to end through the public API with host buffers
+    out_h = torch.empty(sel.out_idx.shape, dtype=torch.int32).pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 5))
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    e0.record(st)
+    for _ in range(e2e_steps):
+        q.copy_(q_h, non_blocking=True)
+        k.copy_(k_h, non_blocking=True)
+        sel.prefill(q, k, stream=st)
+        out_h.copy_(sel.out_idx, non_blocking=True)
+    e1.record(st)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, ws)
+    e2e = {"value": whole_job_rate(s.B * s.N, ws, e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": q_h.numel() * 2 + k_h.numel() * 2,
+           "d2h_bytes_per_step": out_h.numel() * 4}
+
+    extras = {}
+    if not args.no_extras:
+        extras = side_measurements(args, dev, st, rank)
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded iid N(0,1) q and k)",
+            "config": {"workload": f"prefill selection, B={s.B} N={s.N} Hq={s.Hq} Hkv={s.Hkv} d={s.d} C={s.C} "
+                                   f"g=2 K={s.K} bf16 (build + route + leaf LSE + Top-K)",
+                       "B": s.B, "N": s.N, "H_q": s.Hq, "H_kv": s.Hkv, "d": s.d, "C": s.C, "K": s.K,
+                       "l2": "inputs (1.3 GB) larger than L2; no flush", "parallelism": f"replicas x{ws}"},
+            "stage_ms": stage, "selector_roofline": {
+                "t_roof_ms": t_roof_ms, "frac": t_roof_ms / ms_max, "bytes": work["bytes"],
+                "flops": work["leaf_flops"] + work["route_flops"], "leaf_candidates": work["leaf_candidates"],
+                "rule": "max(bytes / HBM, flops / bf16 tensor peak), measured peaks"},
+            "roofline": roof, "e2e": e2e, "gpu_launches": 9 * args.steps, "clocks": clk}
+    line.update(extras)
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(s, q_h, k_h, budget_s=12.0)
+    return line
+
+
+def side_measurements(args, dev, st, rank):
+    """Sweep points, the flat comparator and the decode step (not the
+    headline; each timed with CUDA events after warm-up)."""
+    import torch
+    from pyramid_top_block_mean_gb300 import pisa
+    from pyramid_top_block_mean_gb300 import workloads as W
+
+    def tm(fn, reps):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(dev)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(reps):
+            fn()
+        b.record(st)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    sweep = {}
+    for N in (65536, 131072, 262144):
+        s = W.sweep(N)
+        g = torch.Generator(device=dev)
+        g.manual_seed(3 + N)
+        q = torch.randn(s.B, s.Hq, s.N, s.d, device=dev, generator=g).to(torch.bfloat16)
+        k = torch.randn(s.B, s.Hkv, s.N, s.d, device=dev, generator=g).to(torch.bfloat16)
+        p = pisa.params_from_shape(s)
+        sel = pisa.Selector(p, device=dev)
+        fs = pisa.Selector(p, device=dev, mode="flat")
+        t_pisa = tm(lambda: sel.prefill(q, k, stream=st), 5)
+        t_flat = tm(lambda: fs.flat(q, k, stream=st), 3)
+        sweep[str(N)] = {"pisa_ms": t_pisa, "pisa_queries_per_s": N / t_pisa * 1e3, "flat_ms": t_flat,
+                         "pisa_over_flat_speedup": t_flat / t_pisa}
+        del q, k, sel, fs
+    torch.cuda.empty_cache()
+    # decode: 64 sequences x 131072 cached keys, 32/8 heads, K = 32
+    s = W.DECODE
+    g = torch.Generator(device=dev)
+    g.manual_seed(4)
+    kc = torch.randn(s.B, s.Hkv, s.N, s.d, device=dev, generator=g, dtype=torch.bfloat16)
+    qd = torch.randn(W.DECODE_STEPS, s.B, s.Hq, s.d, device=dev, generator=g, dtype=torch.bfloat16)
+    p = pisa.params_from_shape(s)
+    ds = pisa.Selector(p, device=dev, mode="decode")
+    ds.build(kc, torch.full((s.B,), W.DECODE_CACHED, dtype=torch.int32, device=dev))
+    lens = [torch.full((s.B,), W.DECODE_CACHED + 1 + i, dtype=torch.int32, device=dev)
+            for i in range(W.DECODE_STEPS)]
+    torch.cuda.synchronize(dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for i in range(W.DECODE_STEPS):
+        ds.decode(qd[i], kc, lens[i], stream=st)
+    b.record(st)
+    torch.cuda.synchronize(dev)
+    us = a.elapsed_time(b) / W.DECODE_STEPS * 1e3
+    leaf_bytes = s.B * s.Hkv * 2 * s.K * s.C * s.d * 2
+    del kc
+    torch.cuda.empty_cache()
+    return {"sweep": sweep, "decode": {"us_per_step": us, "steps": W.DECODE_STEPS,
+                                       "workload": "B=64, 131072 cached keys, Hq=32 Hkv=8 d=128 bf16 K=32",
+                                       "leaf_key_bytes_per_step": leaf_bytes,
+                                       "leaf_key_GBps": leaf_bytes / (us * 1e-6) / 1e9}}
+
+
+# ----------------------------------------------------------- CPU oracle
+def cpu_baseline(s, q_h, k_h, budget_s=12.0):
+    """The fp64 oracle as it stands, on the host cores: the full fp64
+    pyramid plus the selection of a sample of query positions (every
+    query of a stratified set of leaf blocks), extrapolated to all N."""
+    import numpy as np
+    import oracle
+
+    o = oracle.Oracle.from_shape(s)
+    kn = k_h.double().numpy()
+    t0 = time.perf_counter()
+    pyr = o.pyramid(kn)
+    t_pyr = time.perf_counter() - t0
+    nb = -(-s.N // s.C)
+    # probe the per-query cost on the last block, then size the sample
+    blocks = list(range(nb - 1, -1, -max(1, nb // 64)))
+    sel, rows = [], []
+    for blk in blocks:
+        for h in range(s.Hkv):
+            for t in range(blk * s.C, min((blk + 1) * s.C, s.N), 8):
+                sel.append((0, h, t))
+    qn = np.stack([q_h[b, h * s.G:(h + 1) * s.G, t].double().numpy() for (b, h, t) in sel])
+    t0 = time.perf_counter()
+    o.select(qn, kn, pyr, sel=sel, qrows=True)
+    t_sel = time.perf_counter() - t0
+    per_query = t_sel / len(sel)  # per (query position, key head)
+    total = t_pyr + per_query * s.N * s.Hkv * s.B
+    return {"value": s.B * s.N / total, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"fp64 pyramid of all {s.N} keys ({t_pyr:.1f} s) + {len(sel)} sampled (query, key head) "
+                      f"selections from {len(blocks)} evenly spaced leaf blocks ({t_sel:.1f} s), extrapolated "
+                      f"to all {s.N * s.Hkv} (query, key head) pairs",
+            "seconds_measured": t_pyr + t_sel}
+
+
+def run_reference(args, ws, rank):
+    """--impl reference: the CPU oracle on this config, rank 0 only."""
+    if rank != 0:
+        return None
+    s, q_h, k_h = workload(args.N, 0)
+    import numpy as np
+    import oracle
+    o = oracle.Oracle.from_shape(s)
+    kn = k_h.double().numpy()
+    nb = -(-s.N // s.C)
+    blocks = list(range(nb - 1, -1, -max(1, nb // 16)))
+    sel = [(0, h, t) for blk in blocks for h in range(s.Hkv) for t in range(blk * s.C, min((blk + 1) * s.C, s.N), 32)]
+    qn = np.stack([q_h[0, h * s.G:(h + 1) * s.G, t].double().numpy() for (_, h, t) in sel])
+
+    def step():
+        t0 = time.perf_counter()
+        pyr = o.pyramid(kn)
+        t1 = time.perf_counter()
+        o.select(qn, kn, pyr, sel=sel, qrows=True)
+        t2 = time.perf_counter()
+        return (t1 - t0) + (t2 - t1) / len(sel) * s.N * s.Hkv * s.B
+
+    for _ in range(args.warmup):
+        step()
+    times = [step() for _ in range(args.steps)]
+    sec = statistics.mean(times)
+    val = s.B * s.N / sec
+    return {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded iid N(0,1) q and k)",
+            "config": {"workload": f"prefill selection, B={s.B} N={s.N} Hq={s.Hq} Hkv={s.Hkv} d={s.d} C={s.C} "
+                                   f"g=2 K={s.K} (fp64 CPU oracle)", "N": s.N, "K": s.K},
+            "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "value": val, "unit": UNIT,
+                             "sample": f"per step: full fp64 pyramid + {len(sel)} sampled (query, key head) "
+                                       f"selections extrapolated to all {s.N * s.Hkv}"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        line = run_reference(args, ws, rank)
+    else:
+        line = run_pisa(args, ws, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

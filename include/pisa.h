@@ -152,6 +152,24 @@ pisa_status pisa_select_prefill(const pisa_params* p, const void* q,
                                 size_t ws_bytes, int32_t* out_idx,
                                 float* out_score, int32_t* trace, void* stream);
 
+/* The two stages of pisa_select_prefill, for callers that time or inspect
+ * them separately; run back to back on one stream with one workspace they
+ * are exactly pisa_select_prefill.
+ *   pisa_prefill_route: clears the status word and walks levels L..2 for
+ *     every query (rcap.io, "Selection walks the tree top-down"), leaving the
+ *     kept level-2 nodes of each query in the workspace; writes `trace`.
+ *   pisa_prefill_leaves: scores the leaf candidates (the two children of each
+ *     kept level-2 node) by LSE over their raw keys and writes out_idx and
+ *     out_score.  It must follow pisa_prefill_route on the same workspace
+ *     with the same params, q and pyramid. */
+pisa_status pisa_prefill_route(const pisa_params* p, const void* q,
+                               const float* pyramid, void* ws, size_t ws_bytes,
+                               int32_t* trace, void* stream);
+pisa_status pisa_prefill_leaves(const pisa_params* p, const void* q,
+                                const void* k, void* ws, size_t ws_bytes,
+                                int32_t* out_idx, float* out_score,
+                                void* stream);
+
 /* One decode step (agihunt.info summary: "Decode routing is O(log N) per
  * step"; kernel paragraph: a single-stage decode kernel).  For each sequence
  * b the caller has already written its new key at position seq_lens[b]-1 of

@@ -1,8 +1,473 @@
+// decode.cu -- one decode step in a single launch: incremental pyramid update
+// along the new key's path, then the top-down walk and leaf scoring for that
+// one query.  agihunt.info summary of "Block Sparse Attention with Log-Linear
+// Complexity": "Decode routing is O(log N) per step" (pyramid paragraph) and
+// the single-stage decode kernel that avoids relaunches (kernel paragraph);
+// rcap.io post, kernel paragraph (one fused kernel per step for decode).
+//
+// One CTA (4 warps) per (sequence, key head).  Phases:
+//  1. update: the new key's leaf is re-averaged from its raw keys (staged in
+//     shared memory by cp.async), then each ancestor is recombined from its
+//     two children with the exact fp32 steps of the pyramid build, so the
+//     state equals a fresh build bit for bit; siblings are prefetched at once.
+//  2. walk: per level the needed child rows are fetched with one bulk copy
+//     each into shared memory (one HBM round trip per level), the four warps
+//     form the G-head dot products, and candidate scoring / Top-K / expansion
+//     run on shared-memory lists (at most 2K candidates).
+//  3. leaves: each warp streams its candidate leaf tiles (C keys) with bulk
+//     copies into its own 16 KB stage and keeps an online log2-sum-exp2 per
+//     head; then the Top-K with the forced blocks.
+// The step is bound by HBM: it reads ~2K leaf tiles per (sequence, key head).
 #include "pisa_common.cuh"
 #include "pisa_internal.h"
+#include "tc_ptx.cuh"
+
 namespace pisa {
-cudaError_t launch_decode(const Prob&, const Pyr&, const void*, const void*, const int32_t*, float*, int32_t*,
-                          int32_t*, float*, int32_t*, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+constexpr int kDecWarps = 4;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kStageBytes = 16384;  // per warp
+constexpr uint64_t kDecWaitNs = 4000000000ull;
+
+template <int G>
+struct DecSmem {
+  alignas(128) unsigned char stage[kDecWarps][kStageBytes];  // 64 KB staging
+  float qs[G][128];
+  int32_t cand[kMaxCand], nxt[kMaxCand];
+  float x[kMaxCand][G], xn[kMaxCand][G];
+  int32_t has_x[kMaxCand], has_xn[kMaxCand];
+  int32_t work[2 * kMaxCand];
+  int32_t slot0[kMaxCand], slot1[kMaxCand];
+  float y[2 * kMaxCand][G];
+  float score[kMaxCand];
+  int32_t kept2[kMaxK];
+  int32_t leaf[kMaxCand];
+  float lscore[kMaxCand];
+  int32_t scan[4];
+  int32_t nkept2, nl;
+  uint64_t bar_rows, bar_leaf[kDecWarps];
+  int32_t abort;
+};
+
+// Exclusive scan of one value per thread over threads [0, 64).
+__device__ __forceinline__ int scan64(int v, int32_t* scratch, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31 && warp < 2) scratch[warp] = x;
+  __syncthreads();
+  const int w0 = scratch[0], w1 = scratch[1];
+  __syncthreads();
+  *total = w0 + w1;
+  return (warp == 1 ? w0 : 0) + x - v;
 }
+
+template <int D, int G>
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, const void* __restrict__ q,
+                                                             const void* __restrict__ kc,
+                                                             const int32_t* __restrict__ seq_lens, float* pyr,
+                                                             int32_t* __restrict__ status, int32_t* __restrict__ out_idx,
+                                                             float* __restrict__ out_score, int32_t* __restrict__ trace) {
+  constexpr int DPL = D / 32;
+  constexpr int NB = 32 / G;
+  extern __shared__ unsigned char dsm_raw[];
+  DecSmem<G>& sm = *reinterpret_cast<DecSmem<G>*>((reinterpret_cast<uintptr_t>(dsm_raw) + 127) & ~(uintptr_t)127);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t bh = blockIdx.x, b = bh / pr.Hkv, h = bh % pr.Hkv;
+  const int K = pr.K, W = K + 3;
+  int32_t* oi = out_idx + bh * W;
+  float* os = out_score ? out_score + bh * W : nullptr;
+  int32_t* trow = trace ? trace + bh * (int64_t)s.L * K : nullptr;
+  if (trow)
+    for (int i = tid; i < s.L * K; i += kDecThreads) trow[i] = -1;
+  const int64_t len = seq_lens[b];
+  if (len < 1 || len > s.N) {
+    if (tid == 0) set_status(status, PISA_DEV_BAD_SEQ_LEN);
+    for (int i = tid; i < W; i += kDecThreads) { oi[i] = -1; if (os) os[i] = -INFINITY; }
+    return;
+  }
+  const bool bf16 = pr.dtype == PISA_BF16;
+  const int esz = bf16 ? 2 : 4;
+  const int64_t t = len - 1, qb = t / s.C;
+  float* ph = pyr + bh * s.P * D;
+  volatile int32_t* abort = &sm.abort;
+
+  if (tid == 0) {
+    ptx::mbar_init(ptx::smem_u32(&sm.bar_rows), 1);
+    for (int w = 0; w < kDecWarps; ++w) ptx::mbar_init(ptx::smem_u32(&sm.bar_leaf[w]), 1);
+    sm.abort = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+
+  // ---------------------------------------------------------------- 1. update
+  {
+    unsigned char* keys = &sm.stage[0][0];                 // up to C*D*4 = 32 KB
+    float* sib = reinterpret_cast<float*>(&sm.stage[2][0]);  // one row per level
+    const int64_t n_leaf = len - qb * s.C;
+    const char* src = reinterpret_cast<const char*>(kc) + ((bh * s.N + qb * s.C) * D) * esz;
+    const int chunks = (int)(n_leaf * D * esz / 16);
+    for (int c = tid; c < chunks; c += kDecThreads) ptx::cp_async_16(ptx::smem_u32(keys + 16 * c), src + 16 * c);
+    for (int w = tid; w < s.L * (D / 4); w += kDecThreads) {
+      const int level = 2 + w / (D / 4);
+      const int c4 = w % (D / 4);
+      if (level > s.L) continue;
+      const int64_t cpath = qb >> (level - 2), sibling = cpath ^ 1;
+      if (sibling < s.size[level - 2])
+        ptx::cp_async_16(ptx::smem_u32(sib + (level - 2) * D + 4 * c4), ph + (s.off[level - 2] + sibling) * D + 4 * c4);
+    }
+    ptx::cp_async_commit();
+    ptx::cp_async_wait<0>();
+    __syncthreads();
+    if (tid < D) {
+      // leaf: keys in index order, IEEE fp32 adds, one division (as the build)
+      float acc = 0.0f;
+      for (int64_t i = 0; i < n_leaf; ++i) {
+        const float v = bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(keys)[i * D + tid])
+                             : reinterpret_cast<const float*>(keys)[i * D + tid];
+        acc = __fadd_rn(acc, v);
+      }
+      float m = __fdiv_rn(acc, (float)n_leaf);
+      ph[(s.off[0] + qb) * D + tid] = m;
+      for (int level = 2; level <= s.L; ++level) {
+        const int64_t j = qb >> (level - 1), cpath = qb >> (level - 2), sibling = cpath ^ 1;
+        const int64_t npath = node_count(s, level - 1, cpath, len);
+        const int64_t nsib = sibling < s.size[level - 2] ? node_count(s, level - 1, sibling, len) : 0;
+        const float vs = nsib > 0 ? sib[(level - 2) * D + tid] : 0.0f;
+        m = (cpath & 1) ? combine_children(vs, nsib, m, npath) : combine_children(m, npath, vs, nsib);
+        ph[(s.off[level - 1] + j) * D + tid] = m;
+      }
+      ptx::fence_proxy_async_global();  // the walk below reads these rows by bulk copy
+    }
+  }
+  // query heads, scaled by s * log2(e)
+  for (int i = tid; i < G * D; i += kDecThreads) {
+    const int g = i / D, c = i % D;
+    const int64_t off = (b * pr.Hq + h * G + g) * D + c;
+    const float v = bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(q)[off]) : reinterpret_cast<const float*>(q)[off];
+    sm.qs[g][c] = v * pr.scale2;
+  }
+  __syncthreads();
+
+  // ------------------------------------------------------------------ 2. walk
+  int L_len = 0;
+  {
+    int64_t n = ceil_div64(len, s.C);
+    for (;;) { ++L_len; if (n == 1) break; n = ceil_div64(n, 2); }
+  }
+  float qr[G][DPL];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) qr[g][c] = sm.qs[g][lane * DPL + c];
+
+  if (tid == 0) sm.nkept2 = 0;
+  __syncthreads();
+  if (qb - 2 >= 1) {
+    int l0 = 0;
+    for (int level = L_len; level >= 2; --level)
+      if (eligible_count(level, qb) > K) { l0 = level; break; }
+    if (trow)
+      for (int level = L_len; level >= 2 && level > l0; --level) {
+        const int64_t n = eligible_count(level, qb);
+        for (int i = tid; i < n; i += kDecThreads) trow[(level - 1) * K + i] = i;
+      }
+    if (l0 == 0) {
+      const int n2 = (int)eligible_count(2, qb);
+      for (int i = tid; i < n2; i += kDecThreads) sm.kept2[i] = i;
+      if (tid == 0) sm.nkept2 = n2;
+    } else {
+      int nc = (int)eligible_count(l0, qb);
+      for (int i = tid; i < nc; i += kDecThreads) { sm.cand[i] = i; sm.has_x[i] = 0; }
+      __syncthreads();
+      uint32_t rphase = 0;
+      float* rows = reinterpret_cast<float*>(&sm.stage[0][0]);
+      for (int level = l0; level >= 2; --level) {
+        const int64_t ncap = s.size[level - 2];
+        // work list (threads 0..63 own one candidate each)
+        int nwork = 0, e0 = 0, e1 = 0, der = 0;
+        int64_t c0 = 0;
+        if (tid < nc) {
+          c0 = 2 * (int64_t)sm.cand[tid];
+          e0 = c0 < ncap && node_eligible(level - 1, c0, qb);
+          e1 = c0 + 1 < ncap && node_eligible(level - 1, c0 + 1, qb);
+          der = e0 && e1 && sm.has_x[tid];
+          nwork = e0 + (e1 && !der);
+        }
+        int nwork_all;
+        const int pos = scan64(tid < 64 ? nwork : 0, sm.scan, &nwork_all);
+        if (tid < nc) {
+          int p = pos;
+          sm.slot0[tid] = e0 ? p : -1;
+          if (e0) sm.work[p++] = (int32_t)c0;
+          sm.slot1[tid] = e1 ? (der ? -2 : p) : -1;
+          if (e1 && !der) sm.work[p++] = (int32_t)(c0 + 1);
+        }
+        if (tid == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&sm.bar_rows), (uint32_t)(nwork_all * D * 4));
+        __syncthreads();
+        // one bulk copy per child row into the staging area
+        for (int w = tid; w < nwork_all; w += kDecThreads)
+          ptx::bulk_g2s(ptx::smem_u32(rows + w * D), ph + (s.off[level - 2] + sm.work[w]) * D, D * 4,
+                        ptx::smem_u32(&sm.bar_rows));
+        if (!ptx::mbar_wait_bounded(ptx::smem_u32(&sm.bar_rows), rphase, abort, kDecWaitNs)) *abort = 1;
+        rphase ^= 1;
+        __syncthreads();
+        if (*abort) break;
+        // dot products: warp w takes batches w, w+4, ... of NB child rows
+        for (int w0 = warp * NB; w0 < nwork_all; w0 += kDecWarps * NB) {
+          float v[32];
+#pragma unroll
+          for (int n = 0; n < NB; ++n) {
+            float mu[DPL];
+            const int w = w0 + n;
+            if (w < nwork_all) {
+              if (DPL == 4) {
+                const float4 m4 = *reinterpret_cast<const float4*>(rows + w * D + lane * 4);
+                mu[0] = m4.x; mu[1] = m4.y; mu[2] = m4.z; mu[3] = m4.w;
+              } else {
+                const float2 m2 = *reinterpret_cast<const float2*>(rows + w * D + lane * 2);
+                mu[0] = m2.x; mu[1] = m2.y;
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < DPL; ++c) mu[c] = 0.0f;
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              float acc = 0.0f;
+#pragma unroll
+              for (int c = 0; c < DPL; ++c) acc = fmaf(qr[g][c], mu[c], acc);
+              v[n * G + g] = acc;
+            }
+          }
+          const float r = warp_transpose_sum32(v);
+          const int w = w0 + lane / G;
+          if (w < nwork_all) sm.y[w][lane % G] = r;
+        }
+        __syncthreads();
+        // candidate scores
+        if (tid < nc) {
+          const int s0 = sm.slot0[tid], s1 = sm.slot1[tid];
+          float n0 = 0.0f, n1 = 0.0f;
+          if (s1 == -2) {
+            n0 = (float)node_count(s, level - 1, c0, len);
+            n1 = (float)node_count(s, level - 1, c0 + 1, len);
+          }
+          float sc = 0.0f;
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float a = s0 >= 0 ? sm.y[s0][g] : 0.0f;
+            float bb = 0.0f;
+            if (s1 >= 0) bb = sm.y[s1][g];
+            else if (s1 == -2) bb = ((n0 + n1) * sm.x[tid][g] - n0 * a) / n1;
+            sc += (s0 >= 0 && s1 != -1) ? lse2_pair(a, bb) : (s0 >= 0 ? a : bb);
+          }
+          sm.score[tid] = sc;
+        }
+        __syncthreads();
+        // Top-K and expansion, in index order
+        int keep = 0, nchild = 0;
+        if (tid < nc) {
+          const float si = sm.score[tid];
+          const int32_t ci = sm.cand[tid];
+          int rank = 0;
+          for (int j = 0; j < nc; ++j) rank += beats(sm.score[j], sm.cand[j], si, ci) ? 1 : 0;
+          keep = rank < K;
+          nchild = keep ? (level > 2 ? e0 + e1 : 1) : 0;
+        }
+        int total;
+        const int p2 = scan64(tid < 64 ? nchild : 0, sm.scan, &total);
+        if (keep) {
+          if (level == 2) {
+            sm.kept2[p2] = sm.cand[tid];
+          } else {
+            int p = p2;
+            const int s0 = sm.slot0[tid], s1 = sm.slot1[tid];
+            float n0 = 0.0f, n1 = 0.0f;
+            if (s1 == -2) {
+              n0 = (float)node_count(s, level - 1, c0, len);
+              n1 = (float)node_count(s, level - 1, c0 + 1, len);
+            }
+            if (e0) {
+              sm.nxt[p] = (int32_t)c0;
+#pragma unroll
+              for (int g = 0; g < G; ++g) sm.xn[p][g] = sm.y[s0][g];
+              sm.has_xn[p] = 1;
+              ++p;
+            }
+            if (e1) {
+              sm.nxt[p] = (int32_t)(c0 + 1);
+#pragma unroll
+              for (int g = 0; g < G; ++g) {
+                const float a = e0 ? sm.y[s0][g] : 0.0f;
+                sm.xn[p][g] = s1 >= 0 ? sm.y[s1][g] : ((n0 + n1) * sm.x[tid][g] - n0 * a) / n1;
+              }
+              sm.has_xn[p] = 1;
+            }
+          }
+        }
+        // kept set in index order for the trace
+        int kt;
+        const int kpos = scan64(tid < 64 ? keep : 0, sm.scan, &kt);
+        if (keep && trow) trow[(level - 1) * K + kpos] = sm.cand[tid];
+        if (level == 2) {
+          if (tid == 0) sm.nkept2 = total;
+          break;
+        }
+        __syncthreads();
+        nc = total;
+        if (tid < nc) {
+          sm.cand[tid] = sm.nxt[tid];
+          sm.has_x[tid] = sm.has_xn[tid];
+#pragma unroll
+          for (int g = 0; g < G; ++g) sm.x[tid][g] = sm.xn[tid][g];
+        }
+        __syncthreads();
+      }
+    }
+  }
+  __syncthreads();
+
+  // ----------------------------------------------------------- 3. leaf stage
+  {
+    const int nk2 = sm.nkept2;
+    int e0 = 0, e1 = 0;
+    int32_t p = -1;
+    if (tid < nk2) {
+      p = sm.kept2[tid];
+      e0 = node_eligible(1, 2 * (int64_t)p, qb);
+      e1 = node_eligible(1, 2 * (int64_t)p + 1, qb);
+    }
+    int nl;
+    const int pos = scan64(tid < 64 ? e0 + e1 : 0, sm.scan, &nl);
+    if (tid < nk2) {
+      int pp = pos;
+      if (e0) sm.leaf[pp++] = 2 * p;
+      if (e1) sm.leaf[pp++] = 2 * p + 1;
+    }
+    __syncthreads();
+    const int kpc = kStageBytes / (D * esz) < s.C ? kStageBytes / (D * esz) : s.C;  // keys per chunk
+    unsigned char* st = &sm.stage[warp][0];
+    const uint32_t bar = ptx::smem_u32(&sm.bar_leaf[warp]);
+    uint32_t lphase = 0;
+    for (int li = warp; li < nl && !*abort; li += kDecWarps) {
+      const int64_t leaf = sm.leaf[li];
+      float m = -INFINITY, ssum = 0.0f;  // this lane's head: lane % G
+      for (int k0 = 0; k0 < s.C; k0 += kpc) {
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t bytes = (uint32_t)(kpc * D * esz);
+          ptx::mbar_arrive_expect_tx(bar, bytes);
+          ptx::bulk_g2s(ptx::smem_u32(st),
+                        reinterpret_cast<const char*>(kc) + ((bh * s.N + leaf * s.C + k0) * D) * esz, bytes, bar);
+        }
+        const bool ok = ptx::mbar_wait_bounded(bar, lphase, abort, kDecWaitNs);
+        lphase ^= 1;
+        if (!__all_sync(0xffffffffu, ok)) { *abort = 1; break; }
+        for (int k1 = 0; k1 < kpc; k1 += NB) {
+          float v[32];
+#pragma unroll
+          for (int n = 0; n < NB; ++n) {
+            float kv[DPL];
+            const unsigned char* row = st + (k1 + n) * D * esz + lane * DPL * esz;
+            if (bf16) {
+              if (DPL == 4) {
+                const uint2 u = *reinterpret_cast<const uint2*>(row);
+                kv[0] = __uint_as_float(u.x << 16); kv[1] = __uint_as_float(u.x & 0xffff0000u);
+                kv[2] = __uint_as_float(u.y << 16); kv[3] = __uint_as_float(u.y & 0xffff0000u);
+              } else {
+                const uint32_t u = *reinterpret_cast<const uint32_t*>(row);
+                kv[0] = __uint_as_float(u << 16); kv[1] = __uint_as_float(u & 0xffff0000u);
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < DPL; ++c) kv[c] = reinterpret_cast<const float*>(row)[c];
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              float acc = 0.0f;
+#pragma unroll
+              for (int c = 0; c < DPL; ++c) acc = fmaf(qr[g][c], kv[c], acc);
+              v[n * G + g] = acc;
+            }
+          }
+          const float x = warp_transpose_sum32(v);  // key k1 + lane/G, head lane%G
+          const float mn = fmaxf(m, x);
+          ssum = ssum * ptx::ex2(m - mn) + ptx::ex2(x - mn);
+          m = mn;
+        }
+      }
+      // combine the lanes of each head, then sum the heads
+#pragma unroll
+      for (int o = 16; o >= G; o >>= 1) {
+        const float mo = __shfl_xor_sync(0xffffffffu, m, o), so = __shfl_xor_sync(0xffffffffu, ssum, o);
+        const float mn = fmaxf(m, mo);
+        ssum = ssum * ptx::ex2(m - mn) + so * ptx::ex2(mo - mn);
+        m = mn;
+      }
+      float lse = m + ptx::lg2(ssum);
+#pragma unroll
+      for (int o = G / 2; o >= 1; o >>= 1) lse += __shfl_xor_sync(0xffffffffu, lse, o);
+      if (lane == 0) sm.lscore[li] = lse;
+    }
+    __syncthreads();
+    if (*abort) {
+      if (tid == 0) set_status(status, PISA_DEV_TIMEOUT);
+      for (int i = tid; i < W; i += kDecThreads) { oi[i] = -1; if (os) os[i] = -INFINITY; }
+      return;
+    }
+    // Top-K of the candidate leaves plus the forced blocks, ascending
+    int keep = 0;
+    if (tid < nl) {
+      int rank = 0;
+      for (int j = 0; j < nl; ++j) rank += beats(sm.lscore[j], sm.leaf[j], sm.lscore[tid], sm.leaf[tid]) ? 1 : 0;
+      keep = rank < K;
+    }
+    int nkept;
+    const int kp = scan64(tid < 64 ? keep : 0, sm.scan, &nkept);
+    if (keep) {
+      oi[1 + kp] = sm.leaf[tid];
+      if (os) os[1 + kp] = sm.lscore[tid] * kLn2;
+    }
+    if (tid == 0) {
+      oi[0] = 0;
+      if (os) os[0] = INFINITY;
+      int ps = 1 + nkept;
+      if (qb - 1 > 0) { oi[ps] = (int32_t)(qb - 1); if (os) os[ps] = INFINITY; ++ps; }
+      if (qb > 0) { oi[ps] = (int32_t)qb; if (os) os[ps] = INFINITY; ++ps; }
+      for (; ps < W; ++ps) { oi[ps] = -1; if (os) os[ps] = -INFINITY; }
+    }
+  }
+}
+
+template <int D, int G>
+static cudaError_t launch_decode_t(const Prob& pr, const Pyr& s, const void* q, const void* kc,
+                                   const int32_t* seq_lens, float* pyr, int32_t* status, int32_t* out_idx,
+                                   float* out_score, int32_t* trace, cudaStream_t st) {
+  const size_t smem = sizeof(DecSmem<G>) + 128;
+  auto kern = decode_kernel<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<(unsigned)(pr.B * pr.Hkv), kDecThreads, smem, st>>>(pr, s, q, kc, seq_lens, pyr, status, out_idx,
+                                                              out_score, trace);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const Prob& pr, const Pyr& s, const void* q, const void* kc, const int32_t* seq_lens,
+                          float* pyr, int32_t* status, int32_t* out_idx, float* out_score, int32_t* trace,
+                          cudaStream_t st) {
+  if (s.L > 2 * kDecWarps * 8) return cudaErrorInvalidValue;  // sibling rows must fit their staging slot
+#define PISA_DEC_CASE(DD, GG) \
+  if (pr.d == DD && pr.G == GG)  \
+    return launch_decode_t<DD, GG>(pr, s, q, kc, seq_lens, pyr, status, out_idx, out_score, trace, st);
+  PISA_DEC_CASE(128, 1) PISA_DEC_CASE(128, 2) PISA_DEC_CASE(128, 4) PISA_DEC_CASE(128, 8)
+  PISA_DEC_CASE(64, 1) PISA_DEC_CASE(64, 2) PISA_DEC_CASE(64, 4) PISA_DEC_CASE(64, 8)
+#undef PISA_DEC_CASE
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace pisa

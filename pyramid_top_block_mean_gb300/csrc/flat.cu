@@ -1,8 +1,357 @@
+// flat.cu -- the flat O(N^2/C) BSA-style selector used as the comparator.
+// agihunt.info summary of "Block Sparse Attention with Log-Linear
+// Complexity", model paragraph: BSA is NSA's selected branch with
+// mean-pooled block summaries; rcap.io post: standard block-sparse attention
+// scores every query against every block summary.  Each query head h' takes
+// p_h'(i) = softmax over the complete past blocks i < qb of s q_h'.mu_i, the
+// block score is the sum over the GQA group's heads, and the Top-K of E plus
+// the forced blocks is returned (same output format as the pyramid path).
+//
+// Same GB300 machinery as the pyramid leaf stage: a 128-row tile holds
+// 128/G consecutive queries x G heads (gathered once per tile with cp.async
+// into the 128-byte swizzled K-major layout), the leaf means are rounded to
+// bf16 once and streamed as 128-leaf TMA tiles, tcgen05.mma accumulates
+// 128 x 128 fp32 scores in TMEM.  Pass 1 keeps a per-row online
+// log2-sum-exp2; pass 2 recomputes the scores, forms the probabilities, sums
+// the G head rows with shuffles and keeps a streaming Top-K per query.
+#include <algorithm>
+
 #include "pisa_common.cuh"
 #include "pisa_internal.h"
+#include "tc_ptx.cuh"
+
 namespace pisa {
-cudaError_t launch_flat(const Prob&, const Pyr&, const void*, const float*, char*, int32_t*, float*, int,
-                        cudaStream_t) {
-  return cudaErrorNotSupported;
+
+constexpr int kFRows = 128;
+constexpr int kFCols = 128;
+constexpr int kFStagesB = 3;
+constexpr int kFlatThreads = 192;
+constexpr uint32_t kFTmemCols = 256;
+constexpr uint64_t kFWaitNs = 4000000000ull;
+
+template <int D>
+struct FlatSmem {
+  uint8_t a[2][kFRows * D * 2];
+  uint8_t b[kFStagesB][kFCols * D * 2];
+  float top_s[kFRows][kMaxK];
+  int32_t top_i[kFRows][kMaxK];
+  uint64_t full_a[2], empty_a[2], full_b[kFStagesB], empty_b[kFStagesB];
+  uint64_t tfull[2], tempty[2], done;
+  uint32_t tmem_base;
+  int32_t abort, zero;
+};
+
+__global__ void means_to_bf16_kernel(int64_t nbh, int64_t P, int64_t nb, int d, const float* __restrict__ pyr,
+                                     __nv_bfloat16* __restrict__ mu) {
+  const int64_t n = nbh * nb * d;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t c = i % d, row = i / d, leaf = row % nb, bh = row / nb;
+    mu[i] = __float2bfloat16_rn(pyr[(bh * P + leaf) * d + c]);
+  }
 }
+
+struct FlatTiles {
+  int64_t nqt;  // query tiles per (sequence, key head)
+  int32_t Qt;   // queries per tile
+};
+
+// columns (leaf blocks) needed by a query tile: blocks [0, qb_last)
+__device__ __forceinline__ int flat_nj(const Prob& pr, int64_t t0, int Qt) {
+  int64_t tl = t0 + Qt - 1;
+  if (tl >= pr.N) tl = pr.N - 1;
+  const int64_t qb_last = tl / pr.C;
+  return (int)ceil_div64(qb_last, kFCols);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kFlatThreads, 1)
+    flat_tc_kernel(Prob pr, FlatTiles ft, int64_t nb, const __grid_constant__ CUtensorMap mumap,
+                   const uint16_t* __restrict__ q, int32_t* __restrict__ out_idx, float* __restrict__ out_score,
+                   int32_t* __restrict__ status) {
+  extern __shared__ unsigned char smem_raw[];
+  FlatSmem<D>& sm = *reinterpret_cast<FlatSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                    ~static_cast<uintptr_t>(1023));
+  constexpr int kHalf = kFRows * 128;
+  constexpr uint32_t kBBytes = kFCols * D * 2;
+  constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kFRows, kFCols);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  volatile int32_t* abort = &sm.abort;
+  const int64_t QT = pr.B * pr.Hkv * ft.nqt;
+  const int Qt = ft.Qt;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&sm.full_a[s]), 32);
+      ptx::mbar_init(ptx::smem_u32(&sm.empty_a[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sm.tfull[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sm.tempty[s]), 4);
+    }
+    for (int s = 0; s < kFStagesB; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&sm.full_b[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&sm.empty_b[s]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&sm.done), 1);
+    sm.abort = 0;
+    sm.zero = 0;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(&sm.tmem_base), kFTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    constexpr int CPR = D / 8, RPI = 32 / CPR;
+    const int ch = lane % CPR;
+    int ia = 0, ib = 0;
+    bool ok = true;
+    for (int64_t qt = blockIdx.x; qt < QT && ok; qt += gridDim.x) {
+      const int64_t bh = qt / ft.nqt, t0 = (qt % ft.nqt) * Qt;
+      const int64_t b = bh / pr.Hkv, h = bh % pr.Hkv;
+      const int nj = flat_nj(pr, t0, Qt);
+      if (nj == 0) continue;
+      const int sa = ia & 1;
+      ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_a[sa]), ((ia >> 1) & 1) ^ 1, abort, kFWaitNs);
+      if (!ok) break;
+      const uint32_t abase = ptx::smem_u32(sm.a[sa]);
+      for (int r0 = 0; r0 < kFRows; r0 += RPI) {
+        const int r = r0 + lane / CPR;
+        const int64_t t = t0 + r / G;
+        if (t < pr.N) {
+          const uint16_t* src = q + (((b * pr.Hq + h * G + (r % G)) * pr.N + t) * D + ch * 8);
+          ptx::cp_async_16(abase + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4), src);
+        }
+      }
+      ptx::cp_async_commit();
+      ptx::cp_async_wait<0>();
+      ptx::fence_proxy_async_smem();
+      ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[sa]));
+      ++ia;
+      for (int pass = 0; pass < 2 && ok; ++pass)
+        for (int j = 0; j < nj; ++j) {
+          const int sb = ib % kFStagesB, ub = ib / kFStagesB;
+          int okb = 1;
+          if (lane == 0) {
+            okb = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_b[sb]), (ub & 1) ^ 1, abort, kFWaitNs);
+            if (okb) {
+              const uint32_t fb = ptx::smem_u32(&sm.full_b[sb]);
+              ptx::mbar_arrive_expect_tx(fb, kBBytes);
+              const int32_t y = (int32_t)(bh * nb + (int64_t)j * kFCols);
+#pragma unroll
+              for (int hh = 0; hh < D / 64; ++hh)
+                ptx::tma_load_2d(ptx::smem_u32(sm.b[sb]) + hh * kHalf, &mumap, 64 * hh, y, fb);
+            }
+          }
+          ok = __shfl_sync(0xffffffffu, okb, 0) != 0;
+          if (!ok) break;
+          ++ib;
+        }
+    }
+    if (!ok) {
+      *abort = 1;
+      if (lane == 0)
+        for (int k = ib > kFStagesB ? ib - kFStagesB : 0; k < ib; ++k)
+          ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k % kFStagesB]), (k / kFStagesB) & 1, &sm.zero,
+                                 kFWaitNs);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      int ia = 0, ib = 0, it = 0;
+      bool ok = true;
+      for (int64_t qt = blockIdx.x; qt < QT && ok; qt += gridDim.x) {
+        const int64_t t0 = (qt % ft.nqt) * Qt;
+        const int nj = flat_nj(pr, t0, Qt);
+        if (nj == 0) continue;
+        const int sa = ia & 1;
+        ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_a[sa]), (ia >> 1) & 1, abort, kFWaitNs);
+        if (!ok) break;
+        for (int pass = 0; pass < 2 && ok; ++pass)
+          for (int j = 0; j < nj; ++j) {
+            const int sb = ib % kFStagesB, acc = it & 1;
+            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[sb]), (ib / kFStagesB) & 1, abort, kFWaitNs) &&
+                 ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tempty[acc]), ((it >> 1) & 1) ^ 1, abort, kFWaitNs);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint32_t a0 = ptx::smem_u32(sm.a[sa]), b0 = ptx::smem_u32(sm.b[sb]);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
+              ptx::mma_bf16(tmem + acc * kFCols, ptx::desc_sw128(a0 + off), ptx::desc_sw128(b0 + off), kIdesc,
+                            k > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(ptx::smem_u32(&sm.empty_b[sb]));
+            ptx::mma_commit(ptx::smem_u32(&sm.tfull[acc]));
+            ++ib;
+            ++it;
+          }
+        if (ok) ptx::mma_commit(ptx::smem_u32(&sm.empty_a[sa]));
+        ++ia;
+      }
+      if (!ok) *abort = 1;
+      ptx::mma_commit(ptx::smem_u32(&sm.done));
+      ptx::mbar_wait_bounded(ptx::smem_u32(&sm.done), 0, &sm.zero, kFWaitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int g = r % G, qi = r / G;
+    const float sc = pr.scale2;
+    const int K = pr.K, W = K + 3;
+    float* ts = sm.top_s[qi];
+    int32_t* tix = sm.top_i[qi];
+    int it = 0;
+    bool ok = true;
+    for (int64_t qt = blockIdx.x; qt < QT && ok; qt += gridDim.x) {
+      const int64_t bh = qt / ft.nqt, t0 = (qt % ft.nqt) * Qt;
+      const int nj = flat_nj(pr, t0, Qt);
+      const int64_t t = t0 + qi;
+      const int64_t qb = t < pr.N ? t / pr.C : 0;  // valid columns: [0, qb)
+      float m = -INFINITY, ssum = 0.0f, lse = 0.0f;
+      int cnt = 0, minpos = 0;
+      float theta = -INFINITY;
+      for (int pass = 0; pass < 2 && ok; ++pass) {
+        if (pass == 1) lse = m + ptx::lg2(ssum);
+        for (int j = 0; j < nj; ++j) {
+          const int acc = it & 1;
+          const bool okw = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tfull[acc]), (it >> 1) & 1, abort, kFWaitNs);
+          if (!__all_sync(0xffffffffu, okw)) { ok = false; *abort = 1; break; }
+          ptx::tc_fence_after();
+          const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + acc * kFCols;
+          const int64_t col0 = (int64_t)j * kFCols;
+          if (pass == 0) {
+            float tm = -INFINITY;
+            float x[kFCols];
+#pragma unroll
+            for (int c4 = 0; c4 < kFCols / 32; ++c4) {
+              uint32_t v[32];
+              ptx::tmem_ld32(taddr + c4 * 32, v);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const int col = c4 * 32 + c;
+                x[col] = (col0 + col < qb) ? __uint_as_float(v[c]) * sc : -INFINITY;
+                tm = fmaxf(tm, x[col]);
+              }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[acc]));
+            if (tm > -INFINITY) {
+              const float mn = fmaxf(m, tm);
+              float s = 0.0f;
+#pragma unroll
+              for (int c = 0; c < kFCols; ++c) s += ptx::ex2(x[c] - mn);
+              ssum = ssum * ptx::ex2(m - mn) + s;
+              m = mn;
+            }
+          } else {
+#pragma unroll 1
+            for (int c4 = 0; c4 < kFCols / 32; ++c4) {
+              uint32_t v[32];
+              ptx::tmem_ld32(taddr + c4 * 32, v);
+              ptx::tmem_ld_wait();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const int64_t col = col0 + c4 * 32 + c;
+                float p = (col < qb) ? ptx::ex2(__uint_as_float(v[c]) * sc - lse) : 0.0f;
+#pragma unroll
+                for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                // the group's first lane keeps the streaming Top-K over E
+                if (g == 0 && col >= 1 && col <= qb - 2 && (cnt < K || p > theta)) {
+                  if (cnt < K) {
+                    ts[cnt] = p; tix[cnt] = (int32_t)col; ++cnt;
+                  } else {
+                    ts[minpos] = p; tix[minpos] = (int32_t)col;
+                  }
+                  if (cnt == K) {  // refresh the K-th best (ties: the later index is the weaker)
+                    theta = ts[0]; minpos = 0;
+                    for (int u = 1; u < K; ++u)
+                      if (ts[u] < theta || (ts[u] == theta && tix[u] > tix[minpos])) { theta = ts[u]; minpos = u; }
+                  }
+                }
+              }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[acc]));
+          }
+          ++it;
+        }
+      }
+      if (!ok) break;
+      // output for this query: Top-K (ascending) plus F
+      if (g == 0 && t < pr.N) {
+        // insertion sort of the kept entries by block index
+        for (int u = 1; u < cnt; ++u) {
+          const float sv = ts[u];
+          const int32_t iv = tix[u];
+          int w = u - 1;
+          while (w >= 0 && tix[w] > iv) { ts[w + 1] = ts[w]; tix[w + 1] = tix[w]; --w; }
+          ts[w + 1] = sv; tix[w + 1] = iv;
+        }
+        const int64_t qrow = bh * pr.N + t;
+        int32_t* oi = out_idx + qrow * W;
+        float* os = out_score ? out_score + qrow * W : nullptr;
+        int pos = 0;
+        oi[pos] = 0; if (os) os[pos] = INFINITY; ++pos;
+        for (int u = 0; u < cnt; ++u) { oi[pos] = tix[u]; if (os) os[pos] = ts[u]; ++pos; }
+        if (qb - 1 > 0) { oi[pos] = (int32_t)(qb - 1); if (os) os[pos] = INFINITY; ++pos; }
+        if (qb > 0) { oi[pos] = (int32_t)qb; if (os) os[pos] = INFINITY; ++pos; }
+        for (; pos < W; ++pos) { oi[pos] = -1; if (os) os[pos] = -INFINITY; }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, kFTmemCols);
+  if (threadIdx.x == 0 && sm.abort) set_status(status, PISA_DEV_TIMEOUT);
+}
+
+template <int D, int G>
+static cudaError_t launch_flat_t(const Prob& pr, int64_t nb, const void* q, const CUtensorMap& mumap, int32_t* out_idx,
+                                 float* out_score, int32_t* status, int grid, cudaStream_t st) {
+  const size_t smem = sizeof(FlatSmem<D>) + 1024;
+  auto kern = flat_tc_kernel<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  FlatTiles ft;
+  ft.Qt = kFRows / G;
+  ft.nqt = ceil_div64(pr.N, ft.Qt);
+  kern<<<grid, kFlatThreads, smem, st>>>(pr, ft, nb, mumap, (const uint16_t*)q, out_idx, out_score, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_flat(const Prob& pr, const Pyr& s, const void* q, const float* pyr, char* ws, int32_t* out_idx,
+                        float* out_score, int num_sms, cudaStream_t st) {
+  if (pr.dtype != PISA_BF16) return cudaErrorNotSupported;  // the comparator runs on bf16 inputs
+  int32_t* status = (int32_t*)ws;
+  __nv_bfloat16* mu = (__nv_bfloat16*)(ws + 256);
+  const int64_t nbh = pr.B * pr.Hkv;
+  const int64_t n = nbh * s.nb * pr.d;
+  means_to_bf16_kernel<<<(unsigned)std::min<int64_t>(ceil_div64(n, 256), 4096), 256, 0, st>>>(nbh, s.P, s.nb, pr.d,
+                                                                                               pyr, mu);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap mumap;
+  if (!make_tmap_rows(&mumap, mu, nbh * s.nb, pr.d, kFCols)) return cudaErrorInvalidValue;
+  const int grid = num_sms > 0 ? num_sms : 148;
+#define PISA_FLAT_CASE(DD, GG) \
+  if (pr.d == DD && pr.G == GG) return launch_flat_t<DD, GG>(pr, s.nb, q, mumap, out_idx, out_score, status, grid, st);
+  PISA_FLAT_CASE(128, 1) PISA_FLAT_CASE(128, 2) PISA_FLAT_CASE(128, 4) PISA_FLAT_CASE(128, 8)
+  PISA_FLAT_CASE(64, 1) PISA_FLAT_CASE(64, 2) PISA_FLAT_CASE(64, 4) PISA_FLAT_CASE(64, 8)
+#undef PISA_FLAT_CASE
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace pisa

@@ -163,36 +163,74 @@ pisa_status pisa_build_pyramid(const pisa_params* p, const void* k, const int32_
   return cuda_status(launch_build_pyramid(pr, s, k, seq_lens, pyramid, (cudaStream_t)stream));
 }
 
-pisa_status pisa_select_prefill(const pisa_params* p, const void* q, const void* k, const float* pyramid, void* ws,
-                                size_t ws_bytes, int32_t* out_idx, float* out_score, int32_t* trace,
-                                void* stream) {
-  Prob pr; Pyr s;
-  pisa_status rc = check_params(p, &pr, &s);
+// Checks shared by the prefill entry points.
+static pisa_status prefill_checks(const pisa_params* p, Prob* pr, Pyr* s, PrefillWs* w, const void* q, const void* k,
+                                  const float* pyramid, const void* ws, size_t ws_bytes, bool need_k, bool need_pyr,
+                                  const int32_t* out_idx, bool need_out, const float* out_score,
+                                  const int32_t* trace) {
+  pisa_status rc = check_params(p, pr, s);
   if (rc != PISA_OK) return rc;
-  const PrefillWs w = prefill_ws_layout(pr, s);
-  if (pr.B * pr.Hkv * pr.N == 0) return PISA_OK;
-  if (!q || !k || !pyramid || !ws || !out_idx) return PISA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(pyramid) || !aligned16(ws)) return PISA_ERR_MISALIGNED;
+  *w = prefill_ws_layout(*pr, *s);
+  if (pr->B * pr->Hkv * pr->N == 0) return PISA_OK;
+  if (!q || !ws || (need_k && !k) || (need_pyr && !pyramid) || (need_out && !out_idx)) return PISA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(ws) || (need_k && !aligned16(k)) || (need_pyr && !aligned16(pyramid)))
+    return PISA_ERR_MISALIGNED;
   if (((uintptr_t)out_idx & 3u) || ((uintptr_t)out_score & 3u) || ((uintptr_t)trace & 3u))
     return PISA_ERR_MISALIGNED;
-  if (ws_bytes < w.total) return PISA_ERR_WORKSPACE;
+  if (ws_bytes < w->total) return PISA_ERR_WORKSPACE;
   // pair counts and TMA row coordinates are 32-bit
-  if (pr.B * pr.Hkv * pr.N * pr.K >= ((int64_t)1 << 31)) return PISA_ERR_UNSUPPORTED;
-  cudaStream_t st = (cudaStream_t)stream;
-  char* base = (char*)ws;
+  if (pr->B * pr->Hkv * pr->N * pr->K >= ((int64_t)1 << 31)) return PISA_ERR_UNSUPPORTED;
+  return PISA_OK;
+}
+
+static pisa_status run_route(const Prob& pr, const Pyr& s, const PrefillWs& w, const void* q, const float* pyramid,
+                             char* base, int32_t* trace, cudaStream_t st) {
   int32_t* status = (int32_t*)(base + w.status);
-  int32_t* kept2 = (int32_t*)(base + w.kept2);
-  cudaError_t e = cudaMemsetAsync(status, 0, 256, st);
-  if (e != cudaSuccess) return PISA_ERR_CUDA;
-  e = launch_route(pr, s, q, pyramid, kept2, trace, status, st);
-  if (e != cudaSuccess) return PISA_ERR_CUDA;
+  if (cudaMemsetAsync(status, 0, 256, st) != cudaSuccess) return PISA_ERR_CUDA;
+  return cuda_status(launch_route(pr, s, q, pyramid, (int32_t*)(base + w.kept2), trace, status, st));
+}
+
+static pisa_status run_leaves(const Prob& pr, const Pyr& s, const PrefillWs& w, const void* q, const void* k,
+                              char* base, int32_t* out_idx, float* out_score, cudaStream_t st) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PISA_ERR_CUDA;
+  cudaError_t e;
   if (pr.dtype == PISA_BF16)
     e = launch_leaf_tc(pr, s, w, base, q, k, out_idx, out_score, sm_count(dev), st);
   else
-    e = launch_leaf_simt(pr, s, q, k, kept2, out_idx, out_score, st);
+    e = launch_leaf_simt(pr, s, q, k, (const int32_t*)(base + w.kept2), out_idx, out_score, st);
   return cuda_status(e);
+}
+
+pisa_status pisa_select_prefill(const pisa_params* p, const void* q, const void* k, const float* pyramid, void* ws,
+                                size_t ws_bytes, int32_t* out_idx, float* out_score, int32_t* trace,
+                                void* stream) {
+  Prob pr; Pyr s; PrefillWs w;
+  pisa_status rc = prefill_checks(p, &pr, &s, &w, q, k, pyramid, ws, ws_bytes, true, true, out_idx, true, out_score,
+                                  trace);
+  if (rc != PISA_OK || pr.B * pr.Hkv * pr.N == 0) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  rc = run_route(pr, s, w, q, pyramid, (char*)ws, trace, st);
+  if (rc != PISA_OK) return rc;
+  return run_leaves(pr, s, w, q, k, (char*)ws, out_idx, out_score, st);
+}
+
+pisa_status pisa_prefill_route(const pisa_params* p, const void* q, const float* pyramid, void* ws, size_t ws_bytes,
+                               int32_t* trace, void* stream) {
+  Prob pr; Pyr s; PrefillWs w;
+  pisa_status rc = prefill_checks(p, &pr, &s, &w, q, nullptr, pyramid, ws, ws_bytes, false, true, nullptr, false,
+                                  nullptr, trace);
+  if (rc != PISA_OK || pr.B * pr.Hkv * pr.N == 0) return rc;
+  return run_route(pr, s, w, q, pyramid, (char*)ws, trace, (cudaStream_t)stream);
+}
+
+pisa_status pisa_prefill_leaves(const pisa_params* p, const void* q, const void* k, void* ws, size_t ws_bytes,
+                                int32_t* out_idx, float* out_score, void* stream) {
+  Prob pr; Pyr s; PrefillWs w;
+  pisa_status rc = prefill_checks(p, &pr, &s, &w, q, k, nullptr, ws, ws_bytes, true, false, out_idx, true, out_score,
+                                  nullptr);
+  if (rc != PISA_OK || pr.B * pr.Hkv * pr.N == 0) return rc;
+  return run_leaves(pr, s, w, q, k, (char*)ws, out_idx, out_score, (cudaStream_t)stream);
 }
 
 pisa_status pisa_select_decode(const pisa_params* p, const void* q, const void* k_cache, const int32_t* seq_lens,
@@ -222,10 +260,12 @@ pisa_status pisa_select_flat(const pisa_params* p, const void* q, const float* p
   pisa_status rc = check_params(p, &pr, &s);
   if (rc != PISA_OK) return rc;
   if (pr.B * pr.Hkv * pr.N == 0) return PISA_OK;
+  if (pr.dtype != PISA_BF16) return PISA_ERR_UNSUPPORTED;  // the comparator is built for bf16 inputs
   if (!q || !pyramid || !ws || !out_idx) return PISA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(pyramid) || !aligned16(ws)) return PISA_ERR_MISALIGNED;
   if (((uintptr_t)out_idx & 3u) || ((uintptr_t)out_score & 3u)) return PISA_ERR_MISALIGNED;
   if (ws_bytes < flat_ws_bytes(pr, s)) return PISA_ERR_WORKSPACE;
+  if (pr.B * pr.Hkv * s.nb >= ((int64_t)1 << 31)) return PISA_ERR_UNSUPPORTED;
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = cudaMemsetAsync(ws, 0, 256, st);
   if (e != cudaSuccess) return PISA_ERR_CUDA;

@@ -1,6 +1,7 @@
 // pisa_internal.h -- host-side declarations shared by the library's units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -37,6 +38,10 @@ size_t decode_ws_bytes(const Prob& pr, const Pyr& s);
 size_t flat_ws_bytes(const Prob& pr, const Pyr& s);
 
 int sm_count(int device);
+
+// 2D TMA view [rows, d] of a bf16 tensor: box of 64 columns x box_rows rows,
+// 128-byte swizzle (the K-major operand layout of the tcgen05 MMAs).
+bool make_tmap_rows(CUtensorMap* m, const void* base, int64_t rows, int d, int box_rows);
 
 cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, const int32_t* seq_lens,
                                  float* pyr, cudaStream_t st);

@@ -33,7 +33,8 @@ DEV_OK, DEV_BAD_SEQ_LEN, DEV_TIMEOUT, DEV_BAD_INDEX = 0, 1, 2, 3
 
 EXPORTED = ["pisa_abi_version", "pisa_status_string", "pisa_pyramid_levels", "pisa_pyramid_nodes",
             "pisa_pyramid_bytes", "pisa_workspace_bytes", "pisa_build_pyramid", "pisa_select_prefill",
-            "pisa_select_decode", "pisa_select_flat", "pisa_read_device_status"]
+            "pisa_prefill_route", "pisa_prefill_leaves", "pisa_select_decode", "pisa_select_flat",
+            "pisa_read_device_status"]
 
 
 class Params(ctypes.Structure):
@@ -61,6 +62,10 @@ _lib.pisa_build_pyramid.argtypes = [_P, _vp, _vp, _vp, _vp]
 _lib.pisa_build_pyramid.restype = ctypes.c_int
 _lib.pisa_select_prefill.argtypes = [_P, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]
 _lib.pisa_select_prefill.restype = ctypes.c_int
+_lib.pisa_prefill_route.argtypes = [_P, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
+_lib.pisa_prefill_route.restype = ctypes.c_int
+_lib.pisa_prefill_leaves.argtypes = [_P, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
+_lib.pisa_prefill_leaves.restype = ctypes.c_int
 _lib.pisa_select_decode.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp, _vp]
 _lib.pisa_select_decode.restype = ctypes.c_int
 _lib.pisa_select_flat.argtypes = [_P, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
@@ -143,6 +148,22 @@ def select_prefill(p: Params, q, k, pyramid, ws, out_idx, out_score=None, trace=
                                   _ptr(out_idx), _ptr(out_score), _ptr(trace), _stream(stream))
     if check:
         _check(rc, "pisa_select_prefill")
+    return rc
+
+
+def prefill_route(p: Params, q, pyramid, ws, trace=None, stream=None, check: bool = True) -> int:
+    rc = _lib.pisa_prefill_route(ctypes.byref(p), _ptr(q), _ptr(pyramid), _ptr(ws),
+                                 ws.numel() * ws.element_size(), _ptr(trace), _stream(stream))
+    if check:
+        _check(rc, "pisa_prefill_route")
+    return rc
+
+
+def prefill_leaves(p: Params, q, k, ws, out_idx, out_score=None, stream=None, check: bool = True) -> int:
+    rc = _lib.pisa_prefill_leaves(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(ws), ws.numel() * ws.element_size(),
+                                  _ptr(out_idx), _ptr(out_score), _stream(stream))
+    if check:
+        _check(rc, "pisa_prefill_leaves")
     return rc
 
 
