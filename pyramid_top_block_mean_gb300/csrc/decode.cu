@@ -26,13 +26,14 @@ namespace pisa {
 
 constexpr int kDecWarps = 4;
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kStageBytes = 16384;  // per warp
+constexpr int kStageBytes = 12288;  // per warp: three 4 KB leaf chunks
+constexpr int kChunkBytes = 4096;
+constexpr int kNBuf = kStageBytes / kChunkBytes;
 constexpr uint64_t kDecWaitNs = 4000000000ull;
 
 template <int G>
 struct DecSmem {
-  alignas(128) unsigned char stage[kDecWarps][kStageBytes];  // 64 KB staging
-  float qs[G][128];
+  alignas(128) unsigned char stage[kDecWarps][kStageBytes];  // 48 KB staging
   int32_t cand[kMaxCand], nxt[kMaxCand];
   float x[kMaxCand][G], xn[kMaxCand][G];
   int32_t has_x[kMaxCand], has_xn[kMaxCand];
@@ -45,8 +46,9 @@ struct DecSmem {
   float lscore[kMaxCand];
   int32_t scan[4];
   int32_t nkept2, nl;
-  uint64_t bar_rows, bar_leaf[kDecWarps];
+  uint64_t bar_rows, bar_leaf[kDecWarps][kNBuf];
   int32_t abort;
+  int32_t zero;  // stays 0
 };
 
 // Exclusive scan of one value per thread over threads [0, 64).
@@ -98,16 +100,18 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
 
   if (tid == 0) {
     ptx::mbar_init(ptx::smem_u32(&sm.bar_rows), 1);
-    for (int w = 0; w < kDecWarps; ++w) ptx::mbar_init(ptx::smem_u32(&sm.bar_leaf[w]), 1);
+    for (int w = 0; w < kDecWarps; ++w)
+      for (int u = 0; u < kNBuf; ++u) ptx::mbar_init(ptx::smem_u32(&sm.bar_leaf[w][u]), 1);
     sm.abort = 0;
+    sm.zero = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
 
   // ---------------------------------------------------------------- 1. update
   {
-    unsigned char* keys = &sm.stage[0][0];                 // up to C*D*4 = 32 KB
-    float* sib = reinterpret_cast<float*>(&sm.stage[2][0]);  // one row per level
+    unsigned char* keys = &sm.stage[0][0];  // up to C*D*4 = 32 KB
+    float* sib = reinterpret_cast<float*>(&sm.stage[0][0] + 32768);  // one row per level (16 KB)
     const int64_t n_leaf = len - qb * s.C;
     const char* src = reinterpret_cast<const char*>(kc) + ((bh * s.N + qb * s.C) * D) * esz;
     const int chunks = (int)(n_leaf * D * esz / 16);
@@ -144,12 +148,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
       ptx::fence_proxy_async_global();  // the walk below reads these rows by bulk copy
     }
   }
-  // query heads, scaled by s * log2(e)
+  // query heads, scaled by s * log2(e), staged through the (now idle)
+  // staging area on their way into registers
+  float(*qs)[D] = reinterpret_cast<float(*)[D]>(&sm.stage[0][0]);
+  __syncthreads();  // the update phase is done with the staging area
   for (int i = tid; i < G * D; i += kDecThreads) {
     const int g = i / D, c = i % D;
     const int64_t off = (b * pr.Hq + h * G + g) * D + c;
     const float v = bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(q)[off]) : reinterpret_cast<const float*>(q)[off];
-    sm.qs[g][c] = v * pr.scale2;
+    qs[g][c] = v * pr.scale2;
   }
   __syncthreads();
 
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int c = 0; c < DPL; ++c) qr[g][c] = sm.qs[g][lane * DPL + c];
+    for (int c = 0; c < DPL; ++c) qr[g][c] = qs[g][lane * DPL + c];
 
   if (tid == 0) sm.nkept2 = 0;
   __syncthreads();
@@ -207,48 +214,54 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
           sm.slot1[tid] = e1 ? (der ? -2 : p) : -1;
           if (e1 && !der) sm.work[p++] = (int32_t)(c0 + 1);
         }
-        if (tid == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&sm.bar_rows), (uint32_t)(nwork_all * D * 4));
-        __syncthreads();
-        // one bulk copy per child row into the staging area
-        for (int w = tid; w < nwork_all; w += kDecThreads)
-          ptx::bulk_g2s(ptx::smem_u32(rows + w * D), ph + (s.off[level - 2] + sm.work[w]) * D, D * 4,
-                        ptx::smem_u32(&sm.bar_rows));
-        if (!ptx::mbar_wait_bounded(ptx::smem_u32(&sm.bar_rows), rphase, abort, kDecWaitNs)) *abort = 1;
-        rphase ^= 1;
-        __syncthreads();
-        if (*abort) break;
-        // dot products: warp w takes batches w, w+4, ... of NB child rows
-        for (int w0 = warp * NB; w0 < nwork_all; w0 += kDecWarps * NB) {
-          float v[32];
+        // child rows, fetched in batches that fit the staging area: one bulk
+        // copy per row, then the four warps form the dot products
+        constexpr int kRowsPerBatch = kDecWarps * kStageBytes / (D * 4);
+        for (int b0 = 0; b0 < nwork_all && !*abort; b0 += kRowsPerBatch) {
+          const int nrow = nwork_all - b0 < kRowsPerBatch ? nwork_all - b0 : kRowsPerBatch;
+          if (tid == 0) ptx::mbar_arrive_expect_tx(ptx::smem_u32(&sm.bar_rows), (uint32_t)(nrow * D * 4));
+          __syncthreads();
+          for (int w = tid; w < nrow; w += kDecThreads)
+            ptx::bulk_g2s(ptx::smem_u32(rows + w * D), ph + (s.off[level - 2] + sm.work[b0 + w]) * D, D * 4,
+                          ptx::smem_u32(&sm.bar_rows));
+          if (!ptx::mbar_wait_bounded(ptx::smem_u32(&sm.bar_rows), rphase, abort, kDecWaitNs)) *abort = 1;
+          rphase ^= 1;
+          __syncthreads();
+          if (*abort) break;
+          // dot products: warp w takes batches w, w+4, ... of NB child rows
+          for (int w0 = warp * NB; w0 < nrow; w0 += kDecWarps * NB) {
+            float v[32];
 #pragma unroll
-          for (int n = 0; n < NB; ++n) {
-            float mu[DPL];
-            const int w = w0 + n;
-            if (w < nwork_all) {
-              if (DPL == 4) {
-                const float4 m4 = *reinterpret_cast<const float4*>(rows + w * D + lane * 4);
-                mu[0] = m4.x; mu[1] = m4.y; mu[2] = m4.z; mu[3] = m4.w;
+            for (int n = 0; n < NB; ++n) {
+              float mu[DPL];
+              const int w = w0 + n;
+              if (w < nrow) {
+                if (DPL == 4) {
+                  const float4 m4 = *reinterpret_cast<const float4*>(rows + w * D + lane * 4);
+                  mu[0] = m4.x; mu[1] = m4.y; mu[2] = m4.z; mu[3] = m4.w;
+                } else {
+                  const float2 m2 = *reinterpret_cast<const float2*>(rows + w * D + lane * 2);
+                  mu[0] = m2.x; mu[1] = m2.y;
+                }
               } else {
-                const float2 m2 = *reinterpret_cast<const float2*>(rows + w * D + lane * 2);
-                mu[0] = m2.x; mu[1] = m2.y;
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) mu[c] = 0.0f;
               }
-            } else {
 #pragma unroll
-              for (int c = 0; c < DPL; ++c) mu[c] = 0.0f;
+              for (int g = 0; g < G; ++g) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int c = 0; c < DPL; ++c) acc = fmaf(qr[g][c], mu[c], acc);
+                v[n * G + g] = acc;
+              }
             }
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              float acc = 0.0f;
-#pragma unroll
-              for (int c = 0; c < DPL; ++c) acc = fmaf(qr[g][c], mu[c], acc);
-              v[n * G + g] = acc;
-            }
+            const float r = warp_transpose_sum32(v);
+            const int w = w0 + lane / G;
+            if (w < nrow) sm.y[b0 + w][lane % G] = r;
           }
-          const float r = warp_transpose_sum32(v);
-          const int w = w0 + lane / G;
-          if (w < nwork_all) sm.y[w][lane % G] = r;
+          __syncthreads();  // the next batch overwrites the staging area
         }
-        __syncthreads();
+        if (*abort) break;
         // candidate scores
         if (tid < nc) {
           const int s0 = sm.slot0[tid], s1 = sm.slot1[tid];
@@ -350,69 +363,97 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
       if (e1) sm.leaf[pp++] = 2 * p + 1;
     }
     __syncthreads();
-    const int kpc = kStageBytes / (D * esz) < s.C ? kStageBytes / (D * esz) : s.C;  // keys per chunk
+    // each warp streams its leaves in 4 KB chunks through three buffers: the
+    // copies of chunks c+1 and c+2 are in flight while chunk c is scored
+    const int kpc = kChunkBytes / (D * esz) < s.C ? kChunkBytes / (D * esz) : s.C;  // keys per chunk
+    const int cpl = s.C / kpc;                                                      // chunks per leaf
+    const int nlw = nl > warp ? (nl - warp + kDecWarps - 1) / kDecWarps : 0;        // this warp's leaves
+    const int nch = nlw * cpl;
     unsigned char* st = &sm.stage[warp][0];
-    const uint32_t bar = ptx::smem_u32(&sm.bar_leaf[warp]);
-    uint32_t lphase = 0;
-    for (int li = warp; li < nl && !*abort; li += kDecWarps) {
-      const int64_t leaf = sm.leaf[li];
-      float m = -INFINITY, ssum = 0.0f;  // this lane's head: lane % G
-      for (int k0 = 0; k0 < s.C; k0 += kpc) {
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t bytes = (uint32_t)(kpc * D * esz);
-          ptx::mbar_arrive_expect_tx(bar, bytes);
-          ptx::bulk_g2s(ptx::smem_u32(st),
-                        reinterpret_cast<const char*>(kc) + ((bh * s.N + leaf * s.C + k0) * D) * esz, bytes, bar);
-        }
-        const bool ok = ptx::mbar_wait_bounded(bar, lphase, abort, kDecWaitNs);
-        lphase ^= 1;
-        if (!__all_sync(0xffffffffu, ok)) { *abort = 1; break; }
-        for (int k1 = 0; k1 < kpc; k1 += NB) {
-          float v[32];
+    const uint32_t chunk_bytes = (uint32_t)(kpc * D * esz);
+    uint32_t lphase = 0u;  // bit b: phase parity of buffer b
+    auto issue = [&](int c) {
+      if (lane == 0) {
+        const int64_t leaf = sm.leaf[warp + (c / cpl) * kDecWarps];
+        const int k0 = (c % cpl) * kpc;
+        const uint32_t bar = ptx::smem_u32(&sm.bar_leaf[warp][c % kNBuf]);
+        ptx::mbar_arrive_expect_tx(bar, chunk_bytes);
+        ptx::bulk_g2s(ptx::smem_u32(st + (c % kNBuf) * kChunkBytes),
+                      reinterpret_cast<const char*>(kc) + ((bh * s.N + leaf * s.C + k0) * D) * esz, chunk_bytes, bar);
+      }
+    };
+    int issued = 0, waited = 0;
+    for (; issued < nch && issued < kNBuf - 1; ++issued) issue(issued);
+    float m = -INFINITY, ssum = 0.0f;  // this lane's head: lane % G
+    for (int c = 0; c < nch; ++c) {
+      if (c + kNBuf - 1 < nch) {
+        __syncwarp();  // every lane is done with the buffer this copy overwrites
+        issue(c + kNBuf - 1);
+        issued = c + kNBuf;
+      }
+      const int bf = c % kNBuf;
+      const bool ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.bar_leaf[warp][bf]), (lphase >> bf) & 1u, abort,
+                                             kDecWaitNs);
+      lphase ^= 1u << bf;
+      waited = c + 1;
+      if (!__all_sync(0xffffffffu, ok)) { *abort = 1; break; }
+      if (c % cpl == 0) { m = -INFINITY; ssum = 0.0f; }
+      const unsigned char* buf = st + bf * kChunkBytes;
+      for (int k1 = 0; k1 < kpc; k1 += NB) {
+        float v[32];
 #pragma unroll
-          for (int n = 0; n < NB; ++n) {
-            float kv[DPL];
-            const unsigned char* row = st + (k1 + n) * D * esz + lane * DPL * esz;
-            if (bf16) {
-              if (DPL == 4) {
-                const uint2 u = *reinterpret_cast<const uint2*>(row);
-                kv[0] = __uint_as_float(u.x << 16); kv[1] = __uint_as_float(u.x & 0xffff0000u);
-                kv[2] = __uint_as_float(u.y << 16); kv[3] = __uint_as_float(u.y & 0xffff0000u);
-              } else {
-                const uint32_t u = *reinterpret_cast<const uint32_t*>(row);
-                kv[0] = __uint_as_float(u << 16); kv[1] = __uint_as_float(u & 0xffff0000u);
-              }
+        for (int n = 0; n < NB; ++n) {
+          float kv[DPL];
+          const unsigned char* row = buf + (k1 + n) * D * esz + lane * DPL * esz;
+          if (bf16) {
+            if (DPL == 4) {
+              const uint2 u = *reinterpret_cast<const uint2*>(row);
+              kv[0] = __uint_as_float(u.x << 16); kv[1] = __uint_as_float(u.x & 0xffff0000u);
+              kv[2] = __uint_as_float(u.y << 16); kv[3] = __uint_as_float(u.y & 0xffff0000u);
             } else {
-#pragma unroll
-              for (int c = 0; c < DPL; ++c) kv[c] = reinterpret_cast<const float*>(row)[c];
+              const uint32_t u = *reinterpret_cast<const uint32_t*>(row);
+              kv[0] = __uint_as_float(u << 16); kv[1] = __uint_as_float(u & 0xffff0000u);
             }
+          } else {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              float acc = 0.0f;
-#pragma unroll
-              for (int c = 0; c < DPL; ++c) acc = fmaf(qr[g][c], kv[c], acc);
-              v[n * G + g] = acc;
-            }
+            for (int cc = 0; cc < DPL; ++cc) kv[cc] = reinterpret_cast<const float*>(row)[cc];
           }
-          const float x = warp_transpose_sum32(v);  // key k1 + lane/G, head lane%G
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int cc = 0; cc < DPL; ++cc) acc = fmaf(qr[g][cc], kv[cc], acc);
+            v[n * G + g] = acc;
+          }
+        }
+        const float x = warp_transpose_sum32(v);  // key k1 + lane/G, head lane%G
+        if (k1 + lane / G < kpc) {  // a batch may run past a short chunk
           const float mn = fmaxf(m, x);
           ssum = ssum * ptx::ex2(m - mn) + ptx::ex2(x - mn);
           m = mn;
         }
       }
-      // combine the lanes of each head, then sum the heads
+      if (c % cpl == cpl - 1) {
+        // combine the lanes of each head, then sum the heads
+        float mh = m, sh = ssum;
 #pragma unroll
-      for (int o = 16; o >= G; o >>= 1) {
-        const float mo = __shfl_xor_sync(0xffffffffu, m, o), so = __shfl_xor_sync(0xffffffffu, ssum, o);
-        const float mn = fmaxf(m, mo);
-        ssum = ssum * ptx::ex2(m - mn) + so * ptx::ex2(mo - mn);
-        m = mn;
+        for (int o = 16; o >= G; o >>= 1) {
+          const float mo = __shfl_xor_sync(0xffffffffu, mh, o), so = __shfl_xor_sync(0xffffffffu, sh, o);
+          const float mn = fmaxf(mh, mo);
+          sh = sh * ptx::ex2(mh - mn) + so * ptx::ex2(mo - mn);
+          mh = mn;
+        }
+        float lse = mh + ptx::lg2(sh);
+#pragma unroll
+        for (int o = G / 2; o >= 1; o >>= 1) lse += __shfl_xor_sync(0xffffffffu, lse, o);
+        if (lane == 0) sm.lscore[warp + (c / cpl) * kDecWarps] = lse;
       }
-      float lse = m + ptx::lg2(ssum);
-#pragma unroll
-      for (int o = G / 2; o >= 1; o >>= 1) lse += __shfl_xor_sync(0xffffffffu, lse, o);
-      if (lane == 0) sm.lscore[li] = lse;
+    }
+    // after an early exit, let copies already issued land before the CTA ends
+    for (int c = waited; c < issued; ++c) {
+      const int bf = c % kNBuf;
+      ptx::mbar_wait_bounded(ptx::smem_u32(&sm.bar_leaf[warp][bf]), (lphase >> bf) & 1u, &sm.zero, kDecWaitNs);
+      lphase ^= 1u << bf;
     }
     __syncthreads();
     if (*abort) {
@@ -460,7 +501,7 @@ static cudaError_t launch_decode_t(const Prob& pr, const Pyr& s, const void* q, 
 cudaError_t launch_decode(const Prob& pr, const Pyr& s, const void* q, const void* kc, const int32_t* seq_lens,
                           float* pyr, int32_t* status, int32_t* out_idx, float* out_score, int32_t* trace,
                           cudaStream_t st) {
-  if (s.L > 2 * kDecWarps * 8) return cudaErrorInvalidValue;  // sibling rows must fit their staging slot
+  if (s.L * pr.d * 4 > 16384) return cudaErrorInvalidValue;  // sibling rows must fit their staging slot
 #define PISA_DEC_CASE(DD, GG) \
   if (pr.d == DD && pr.G == GG)  \
     return launch_decode_t<DD, GG>(pr, s, q, kc, seq_lens, pyr, status, out_idx, out_score, trace, st);

@@ -24,17 +24,18 @@ namespace pisa {
 
 constexpr int kFRows = 128;
 constexpr int kFCols = 128;
-constexpr int kFStagesB = 3;
+constexpr int kFStagesB = 2;
+constexpr int kFCap = kMaxK + 32;  // Top-K buffer per query: K kept + one 32-column batch
 constexpr int kFlatThreads = 192;
 constexpr uint32_t kFTmemCols = 256;
 constexpr uint64_t kFWaitNs = 4000000000ull;
 
-template <int D>
+template <int D, int G>
 struct FlatSmem {
   uint8_t a[2][kFRows * D * 2];
   uint8_t b[kFStagesB][kFCols * D * 2];
-  float top_s[kFRows][kMaxK];
-  int32_t top_i[kFRows][kMaxK];
+  float top_s[kFRows / G][kFCap];
+  int32_t top_i[kFRows / G][kFCap];
   uint64_t full_a[2], empty_a[2], full_b[kFStagesB], empty_b[kFStagesB];
   uint64_t tfull[2], tempty[2], done;
   uint32_t tmem_base;
@@ -47,6 +48,18 @@ __global__ void means_to_bf16_kernel(int64_t nbh, int64_t P, int64_t nb, int d, 
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t c = i % d, row = i / d, leaf = row % nb, bh = row / nb;
     mu[i] = __float2bfloat16_rn(pyr[(bh * P + leaf) * d + c]);
+  }
+}
+
+// Moves the best K of the n buffered (score, block) entries to the front,
+// best first (higher score, then lower block index).
+__device__ __noinline__ void flat_select_topk(float* ts, int32_t* tix, int n, int K) {
+  for (int r = 0; r < K; ++r) {
+    int best = r;
+    for (int u = r + 1; u < n; ++u)
+      if (ts[u] > ts[best] || (ts[u] == ts[best] && tix[u] < tix[best])) best = u;
+    const float sv = ts[r]; ts[r] = ts[best]; ts[best] = sv;
+    const int32_t iv = tix[r]; tix[r] = tix[best]; tix[best] = iv;
   }
 }
 
@@ -69,7 +82,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
                    const uint16_t* __restrict__ q, int32_t* __restrict__ out_idx, float* __restrict__ out_score,
                    int32_t* __restrict__ status) {
   extern __shared__ unsigned char smem_raw[];
-  FlatSmem<D>& sm = *reinterpret_cast<FlatSmem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+  FlatSmem<D, G>& sm = *reinterpret_cast<FlatSmem<D, G>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                     ~static_cast<uintptr_t>(1023));
   constexpr int kHalf = kFRows * 128;
   constexpr uint32_t kBBytes = kFCols * D * 2;
@@ -207,7 +220,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
     const float sc = pr.scale2;
     const int K = pr.K, W = K + 3;
     float* ts = sm.top_s[qi];
-    int32_t* tix = sm.top_i[qi];
+    int32_t* tix = sm.top_i[qi];  // used by the g == 0 lane of each query
     int it = 0;
     bool ok = true;
     for (int64_t qt = blockIdx.x; qt < QT && ok; qt += gridDim.x) {
@@ -216,8 +229,8 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       const int64_t t = t0 + qi;
       const int64_t qb = t < pr.N ? t / pr.C : 0;  // valid columns: [0, qb)
       float m = -INFINITY, ssum = 0.0f, lse = 0.0f;
-      int cnt = 0, minpos = 0;
-      float theta = -INFINITY;
+      int cnt = 0;              // entries in this query's buffer (g == 0 lane)
+      float theta = -INFINITY;  // K-th best so far, once cnt has reached K
       for (int pass = 0; pass < 2 && ok; ++pass) {
         if (pass == 1) lse = m + ptx::lg2(ssum);
         for (int j = 0; j < nj; ++j) {
@@ -247,10 +260,10 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[acc]));
             if (tm > -INFINITY) {
               const float mn = fmaxf(m, tm);
-              float s = 0.0f;
+              float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-              for (int c = 0; c < kFCols; ++c) s += ptx::ex2(x[c] - mn);
-              ssum = ssum * ptx::ex2(m - mn) + s;
+              for (int c = 0; c < kFCols; ++c) s4[c & 3] += ptx::ex2(x[c] - mn);
+              ssum = ssum * ptx::ex2(m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
               m = mn;
             }
           } else {
@@ -259,24 +272,33 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
               uint32_t v[32];
               ptx::tmem_ld32(taddr + c4 * 32, v);
               ptx::tmem_ld_wait();
+              float pv[32];
+              float bmax = -INFINITY;
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
                 const int64_t col = col0 + c4 * 32 + c;
                 float p = (col < qb) ? ptx::ex2(__uint_as_float(v[c]) * sc - lse) : 0.0f;
 #pragma unroll
                 for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-                // the group's first lane keeps the streaming Top-K over E
-                if (g == 0 && col >= 1 && col <= qb - 2 && (cnt < K || p > theta)) {
-                  if (cnt < K) {
-                    ts[cnt] = p; tix[cnt] = (int32_t)col; ++cnt;
-                  } else {
-                    ts[minpos] = p; tix[minpos] = (int32_t)col;
+                pv[c] = (col >= 1 && col <= qb - 2) ? p : -INFINITY;  // Top-K runs over E only
+                bmax = fmaxf(bmax, pv[c]);
+              }
+              // the group's first lane appends every column above the current
+              // K-th best to its buffer and compacts it back to K when a batch
+              // added anything (rare once the K-th best has settled)
+              if (g == 0 && bmax > theta) {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                  if (pv[c] > theta) {
+                    ts[cnt] = pv[c];
+                    tix[cnt] = (int32_t)(col0 + c4 * 32 + c);
+                    ++cnt;
                   }
-                  if (cnt == K) {  // refresh the K-th best (ties: the later index is the weaker)
-                    theta = ts[0]; minpos = 0;
-                    for (int u = 1; u < K; ++u)
-                      if (ts[u] < theta || (ts[u] == theta && tix[u] > tix[minpos])) { theta = ts[u]; minpos = u; }
-                  }
+                }
+                if (cnt > K) {
+                  flat_select_topk(ts, tix, cnt, K);
+                  cnt = K;
+                  theta = ts[K - 1];
                 }
               }
             }
@@ -290,6 +312,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       if (!ok) break;
       // output for this query: Top-K (ascending) plus F
       if (g == 0 && t < pr.N) {
+        if (cnt > K) { flat_select_topk(ts, tix, cnt, K); cnt = K; }
         // insertion sort of the kept entries by block index
         for (int u = 1; u < cnt; ++u) {
           const float sv = ts[u];
@@ -321,7 +344,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
 template <int D, int G>
 static cudaError_t launch_flat_t(const Prob& pr, int64_t nb, const void* q, const CUtensorMap& mumap, int32_t* out_idx,
                                  float* out_score, int32_t* status, int grid, cudaStream_t st) {
-  const size_t smem = sizeof(FlatSmem<D>) + 1024;
+  const size_t smem = sizeof(FlatSmem<D, G>) + 1024;
   auto kern = flat_tc_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

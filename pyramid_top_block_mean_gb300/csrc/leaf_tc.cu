@@ -35,18 +35,23 @@ namespace pisa {
 
 constexpr int kTileRows = 128;  // MMA M: queries x heads
 constexpr int kTileKeys = 128;  // MMA N: leaves 2p and 2p+1
-constexpr int kStages = 2;
+constexpr int kStagesA = 4;  // query-row tiles in flight
+constexpr int kStagesB = 2;  // key tiles
+constexpr int kAcc = 4;      // TMEM accumulators (4 x 128 columns)
 constexpr int kGroup = 4;
-constexpr int kLeafTcThreads = 192;  // warp 0 loads, warp 1 MMA, warps 2-5 epilogue
-constexpr uint32_t kTmemCols = 256;
+constexpr int kProdWarps = 4;        // warps 0-3 gather 32 rows each
+constexpr int kMmaWarp = 4;          // issues the MMAs, owns TMEM
+constexpr int kEpiWarps = 8;         // warps 5-12: (TMEM lane quadrant, leaf)
+constexpr int kLeafTcThreads = 32 * (kProdWarps + 1 + kEpiWarps);
+constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
 template <int D>
 struct LeafTcSmem {
-  uint8_t a[kStages][kTileRows * D * 2];
-  uint8_t b[kStages][kTileKeys * D * 2];
-  uint64_t full_a[kStages], empty_a[kStages], full_b[kStages], empty_b[kStages];
-  uint64_t tfull[2], tempty[2], done;
+  uint8_t a[kStagesA][kTileRows * D * 2];
+  uint8_t b[kStagesB][kTileKeys * D * 2];
+  uint64_t full_a[kStagesA], empty_a[kStagesA], full_b[kStagesB], empty_b[kStagesB];
+  uint64_t tfull[kAcc], tempty[kAcc], done;
   uint32_t tmem_base;
   int32_t abort;
   int32_t zero;  // stays 0: a wait that must not give up early on abort
@@ -157,15 +162,17 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
   volatile int32_t* abort = &sm.abort;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&sm.full_a[s]), 32);
+    for (int s = 0; s < kStagesA; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&sm.full_a[s]), 32 * kProdWarps);
       ptx::mbar_init(ptx::smem_u32(&sm.empty_a[s]), 1);
+    }
+    for (int s = 0; s < kStagesB; ++s) {
       ptx::mbar_init(ptx::smem_u32(&sm.full_b[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&sm.empty_b[s]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kAcc; ++s) {
       ptx::mbar_init(ptx::smem_u32(&sm.tfull[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&sm.tempty[s]), 4);
+      ptx::mbar_init(ptx::smem_u32(&sm.tempty[s]), kEpiWarps);
     }
     ptx::mbar_init(ptx::smem_u32(&sm.done), 1);
     sm.abort = 0;
@@ -173,7 +180,7 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     ptx::tmem_alloc(ptx::smem_u32(&sm.tmem_base), kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -183,12 +190,16 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
   const uint32_t tmem = sm.tmem_base;
   const int T = *tile_total;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp < kProdWarps) {
+    // ------------------------------------------------------------ producers
+    // warp w gathers rows [32w, 32w + 32); warp 0 also loads the key tiles
     constexpr int CPR = D / 8;     // 16-byte chunks per row
     constexpr int RPI = 32 / CPR;  // rows per warp instruction
+    constexpr int QPW = 32 / G;    // queries per producer warp
     const int ch = lane % CPR;
-    int it = 0, bcount = 0, last_bucket = -1, prev_sa = -1;
+    const int row0 = warp * 32, qbase = row0 / G;
+    int it = 0, bcount = 0, last_bucket = -1;
+    int pend[kStagesA], npend = 0;  // stages whose copies are not yet signalled
     bool ok = true;
     for (TileIter ti(T); ti.valid() && ok; ti.next()) {
       const int4 info = tile_info[ti.i];
@@ -196,13 +207,21 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
       const int64_t p = bucket % n2;
       const int64_t bh = (bucket / n2) / nchunk;
       const int64_t b = bh / pr.Hkv, h = bh % pr.Hkv;
-      const int sa = it & 1, use = it >> 1;
+      const int sa = it % kStagesA, use = it / kStagesA;
       ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_a[sa]), (use & 1) ^ 1, abort, kWaitLimitNs);
       if (!ok) break;
       if (info.x != last_bucket) {
-        const int sb = bcount & 1, ub = bcount >> 1;
+        const int sb = bcount % kStagesB, ub = bcount / kStagesB;
         int okb = 1;
-        if (lane == 0) {
+        if (warp == 0 && npend > 0) {
+          // The key stage is released only after the MMA finished tiles whose
+          // row signals may still be deferred here: send them before waiting.
+          ptx::cp_async_wait<0>();
+          ptx::fence_proxy_async_smem();
+          for (int u = 0; u < npend; ++u) ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[pend[u]]));
+          npend = 0;
+        }
+        if (warp == 0 && lane == 0) {
           okb = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_b[sb]), (ub & 1) ^ 1, abort, kWaitLimitNs);
           if (okb) {
             const uint32_t fb = ptx::smem_u32(&sm.full_b[sb]);
@@ -218,15 +237,17 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
         ++bcount;
         last_bucket = info.x;
       }
-      // gather the tile's 128 query-head rows
+      // gather this warp's 32 query-head rows; the query positions come first
+      // (one load per query) so the copies issue back to back
       const uint32_t abase = ptx::smem_u32(sm.a[sa]);
       const int cnt = info.z;
-      for (int r0 = 0; r0 < kTileRows; r0 += RPI) {
-        const int r = r0 + lane / CPR;
-        const int qr = r / G;
-        if (qr < cnt) {
-          const int32_t pe = pairs[info.y + qr];
-          const int64_t t = pe >> 5;
+      const int32_t tv = (lane < QPW && qbase + lane < cnt) ? (pairs[info.y + qbase + lane] >> 5) : 0;
+#pragma unroll
+      for (int r0 = 0; r0 < 32; r0 += RPI) {
+        const int rl = r0 + lane / CPR;
+        const int r = row0 + rl;
+        const int64_t t = __shfl_sync(0xffffffffu, tv, rl / G);
+        if (qbase + rl / G < cnt) {
           const int g = r % G;
           const uint16_t* src = q + (((b * pr.Hq + h * G + g) * pr.N + t) * D + ch * 8);
           const uint32_t dst = abase + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
@@ -234,41 +255,47 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
         }
       }
       ptx::cp_async_commit();
-      if (prev_sa >= 0) {
-        ptx::cp_async_wait<1>();
+      pend[npend++] = sa;
+      if (npend > kStagesA - 2) {  // keep two tiles of copies in flight
+        ptx::cp_async_wait<kStagesA - 2>();
         ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[prev_sa]));
+        ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[pend[0]]));
+#pragma unroll
+        for (int u = 0; u < kStagesA - 1; ++u) pend[u] = pend[u + 1];
+        --npend;
       }
-      prev_sa = sa;
       ++it;
     }
     ptx::cp_async_wait<0>();
     ptx::fence_proxy_async_smem();
-    if (ok && prev_sa >= 0) ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[prev_sa]));
+    if (ok)
+      for (int u = 0; u < npend; ++u) ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[pend[u]]));
     if (!ok) {
       *abort = 1;
       // let TMA loads already issued land before the CTA can exit
-      if (lane == 0)
-        for (int k = bcount > 2 ? bcount - 2 : 0; k < bcount; ++k)
-          ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k & 1]), (k >> 1) & 1, &sm.zero, kWaitLimitNs);
+      if (warp == 0 && lane == 0)
+        for (int k = bcount > kStagesB ? bcount - kStagesB : 0; k < bcount; ++k)
+          ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k % kStagesB]), (k / kStagesB) & 1, &sm.zero,
+                                 kWaitLimitNs);
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       int it = 0, bcount = 0, last_bucket = -1, sb = 0;
       bool ok = true;
       for (TileIter ti(T); ti.valid(); ti.next()) {
         const int4 info = tile_info[ti.i];
-        const int sa = it & 1, use = it >> 1, acc = it & 1;
+        const int sa = it % kStagesA, use = it / kStagesA;
+        const int acc = it % kAcc, uacc = it / kAcc;
         if (info.x != last_bucket) {
-          sb = bcount & 1;
-          ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[sb]), (bcount >> 1) & 1, abort, kWaitLimitNs);
+          sb = bcount % kStagesB;
+          ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[sb]), (bcount / kStagesB) & 1, abort, kWaitLimitNs);
           if (!ok) break;
           ++bcount;
           last_bucket = info.x;
         }
         ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_a[sa]), use & 1, abort, kWaitLimitNs) &&
-             ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tempty[acc]), (use & 1) ^ 1, abort, kWaitLimitNs);
+             ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tempty[acc]), (uacc & 1) ^ 1, abort, kWaitLimitNs);
         if (!ok) break;
         ptx::tc_fence_after();
         const uint32_t d = tmem + acc * kTileKeys;
@@ -292,55 +319,51 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q4 = warp & 3;  // TMEM lane quadrant this warp may read
+    // warp -> (TMEM lane quadrant warp % 4, leaf): 32 rows x 64 key columns
+    const int q4 = warp & 3;
+    const int leaf = (warp - (kMmaWarp + 1)) / 4;
     const int r = q4 * 32 + lane;
     const float sc = pr.scale2;
     int it = 0;
     for (TileIter ti(T); ti.valid(); ti.next()) {
       const int4 info = tile_info[ti.i];
-      const int acc = it & 1, use = it >> 1;
+      const int acc = it % kAcc, use = it / kAcc;
+      const int qr = r / G;
+      const int32_t pe = qr < info.z ? pairs[info.y + qr] : 0;  // issued before the wait
       const bool okw = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tfull[acc]), use & 1, abort, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, okw)) { *abort = 1; break; }
       ptx::tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + acc * kTileKeys;
-      float lse[2];
-#pragma unroll
-      for (int leaf = 0; leaf < 2; ++leaf) {
-        uint32_t v0[32], v1[32];
-        ptx::tmem_ld32(taddr + leaf * 64, v0);
-        ptx::tmem_ld32(taddr + leaf * 64 + 32, v1);
-        ptx::tmem_ld_wait();
-        float x[64];
-        float m = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          x[j] = __uint_as_float(v0[j]) * sc;
-          x[32 + j] = __uint_as_float(v1[j]) * sc;
-        }
-#pragma unroll
-        for (int j = 0; j < 64; ++j) m = fmaxf(m, x[j]);
-        float s0 = 0.0f, s1 = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 64; j += 2) {
-          s0 += ptx::ex2(x[j] - m);
-          s1 += ptx::ex2(x[j + 1] - m);
-        }
-        lse[leaf] = m + ptx::lg2(s0 + s1);
-      }
+      const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + acc * kTileKeys + leaf * 64;
+      uint32_t v0[32], v1[32];
+      ptx::tmem_ld32(taddr, v0);
+      ptx::tmem_ld32(taddr + 32, v1);
+      ptx::tmem_ld_wait();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[acc]));
+      float x[64];
 #pragma unroll
-      for (int o = 1; o < G; o <<= 1) {
-        lse[0] += __shfl_xor_sync(0xffffffffu, lse[0], o);
-        lse[1] += __shfl_xor_sync(0xffffffffu, lse[1], o);
+      for (int j = 0; j < 32; ++j) {
+        x[j] = __uint_as_float(v0[j]) * sc;
+        x[32 + j] = __uint_as_float(v1[j]) * sc;
       }
-      const int qr = r / G;
+      float mm[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) mm[u] = x[u];
+#pragma unroll
+      for (int j = 8; j < 64; ++j) mm[j & 7] = fmaxf(mm[j & 7], x[j]);
+      const float m = fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
+                            fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7])));
+      float ss[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int j = 0; j < 64; ++j) ss[j & 3] += ptx::ex2(x[j] - m);
+      float lse = m + ptx::lg2((ss[0] + ss[1]) + (ss[2] + ss[3]));
+#pragma unroll
+      for (int o = 1; o < G; o <<= 1) lse += __shfl_xor_sync(0xffffffffu, lse, o);
       if ((r % G) == 0 && qr < info.z) {
         const int64_t bh = (info.x / n2) / nchunk;
-        const int32_t pe = pairs[info.y + qr];
         const int64_t t = pe >> 5, slot = pe & 31;
-        *reinterpret_cast<float2*>(leaf_score + ((bh * pr.N + t) * pr.K + slot) * 2) = make_float2(lse[0], lse[1]);
+        leaf_score[((bh * pr.N + t) * pr.K + slot) * 2 + leaf] = lse;
       }
       ++it;
     }
@@ -349,7 +372,7 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
   if (threadIdx.x == 0 && sm.abort) set_status(status, PISA_DEV_TIMEOUT);
 }
 
@@ -415,6 +438,49 @@ __global__ void __launch_bounds__(256) finalize_kernel(Prob pr, const int32_t* _
     if (qb > 0) { oi[pos] = (int32_t)qb; if (os) os[pos] = INFINITY; ++pos; }
     for (; pos < W; ++pos) { oi[pos] = -1; if (os) os[pos] = -INFINITY; }
   }
+}
+
+// One thread per query for K <= 8: the <= 16 candidates are ranked in
+// registers (the loads and stores of consecutive threads are contiguous).
+__global__ void __launch_bounds__(256) finalize_small_kernel(Prob pr, const int32_t* __restrict__ kept2,
+                                                             const float* __restrict__ leaf_score,
+                                                             int32_t* __restrict__ out_idx,
+                                                             float* __restrict__ out_score) {
+  constexpr int KM = 8, NCM = 2 * KM;
+  const int64_t qi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (qi >= pr.B * pr.Hkv * pr.N) return;
+  const int64_t qb = (qi % pr.N) / pr.C;
+  const int K = pr.K, W = K + 3;
+  float sc[NCM];
+  int32_t lf[NCM];
+  bool val[NCM];
+#pragma unroll
+  for (int c = 0; c < NCM; ++c) {
+    const int slot = c >> 1;
+    const int32_t p = slot < K ? kept2[qi * K + slot] : -1;
+    lf[c] = p >= 0 ? 2 * p + (c & 1) : -1;
+    val[c] = p >= 0 && lf[c] >= 1 && lf[c] <= qb - 2;
+    sc[c] = val[c] ? leaf_score[(qi * K + slot) * 2 + (c & 1)] : -INFINITY;
+  }
+  int32_t* oi = out_idx + qi * W;
+  float* os = out_score ? out_score + qi * W : nullptr;
+  int pos = 1;
+#pragma unroll
+  for (int c = 0; c < NCM; ++c) {
+    int rank = 0;
+#pragma unroll
+    for (int j = 0; j < NCM; ++j) rank += (val[j] && beats(sc[j], lf[j], sc[c], lf[c])) ? 1 : 0;
+    if (val[c] && rank < K) {  // candidates run in ascending leaf order
+      oi[pos] = lf[c];
+      if (os) os[pos] = sc[c] * kLn2;
+      ++pos;
+    }
+  }
+  oi[0] = 0;
+  if (os) os[0] = INFINITY;
+  if (qb - 1 > 0) { oi[pos] = (int32_t)(qb - 1); if (os) os[pos] = INFINITY; ++pos; }
+  if (qb > 0) { oi[pos] = (int32_t)qb; if (os) os[pos] = INFINITY; ++pos; }
+  for (; pos < W; ++pos) { oi[pos] = -1; if (os) os[pos] = -INFINITY; }
 }
 
 // ------------------------------------------------------------------ host
@@ -496,8 +562,12 @@ cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, cha
 #undef PISA_LEAF_TC_CASE
     if (e != cudaSuccess) return e;
   }
-  finalize_kernel<<<(unsigned)ceil_div64(nq, 8), 256, 0, st>>>(pr, kept2, (const float*)(ws + w.leaf_score),
-                                                              out_idx, out_score);
+  if (pr.K <= 8)
+    finalize_small_kernel<<<(unsigned)ceil_div64(nq, 256), 256, 0, st>>>(pr, kept2, (const float*)(ws + w.leaf_score),
+                                                                         out_idx, out_score);
+  else
+    finalize_kernel<<<(unsigned)ceil_div64(nq, 8), 256, 0, st>>>(pr, kept2, (const float*)(ws + w.leaf_score),
+                                                                out_idx, out_score);
   return cudaGetLastError();
 }
 
