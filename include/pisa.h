@@ -201,6 +201,29 @@ pisa_status pisa_select_flat(const pisa_params* p, const void* q,
                              const float* pyramid, void* ws, size_t ws_bytes,
                              int32_t* out_idx, float* out_score, void* stream);
 
+/* Prefill selection without a caller workspace, for callers that cannot
+ * allocate device memory when they select blocks (code running inside a
+ * runtime that owns every device allocation, such as a plug-in or a host
+ * callback that may not call cudaMalloc or a framework allocator).  The paper
+ * has no counterpart: this is a deployment convenience around
+ * pisa_select_prefill.  Arguments and outputs are those of
+ * pisa_select_prefill without ws, ws_bytes and trace.
+ *  - The workspace is one fixed 64 MiB device array inside the library, held
+ *    on every GPU that loads it until the process exits.  Problems needing
+ *    more (pisa_workspace_bytes(p, PISA_MODE_PREFILL) > 64 MiB) get
+ *    PISA_ERR_WORKSPACE and nothing is launched.
+ *  - The first call on a device looks up the array's device address (with
+ *    that device current) and caches it; make that first call before any
+ *    stream capture on the device.
+ *  - Calls never allocate.  All calls on a device share the array, and each
+ *    call clears what must start at zero; calls that overlap on the GPU
+ *    (other streams, other threads) race on it and must be serialised by the
+ *    caller. */
+pisa_status pisa_select_prefill_static(const pisa_params* p, const void* q,
+                                       const void* k, const float* pyramid,
+                                       int32_t* out_idx, float* out_score,
+                                       void* stream);
+
 /* Synchronises `stream`, then copies the workspace status word into
  * *device_code (PISA_DEV_*).  Returns PISA_ERR_DEVICE when it is non-zero. */
 pisa_status pisa_read_device_status(const void* ws, int32_t* device_code,

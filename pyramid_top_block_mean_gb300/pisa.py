@@ -34,7 +34,7 @@ DEV_OK, DEV_BAD_SEQ_LEN, DEV_TIMEOUT, DEV_BAD_INDEX = 0, 1, 2, 3
 EXPORTED = ["pisa_abi_version", "pisa_status_string", "pisa_pyramid_levels", "pisa_pyramid_nodes",
             "pisa_pyramid_bytes", "pisa_workspace_bytes", "pisa_build_pyramid", "pisa_select_prefill",
             "pisa_prefill_route", "pisa_prefill_leaves", "pisa_select_decode", "pisa_select_flat",
-            "pisa_read_device_status"]
+            "pisa_read_device_status", "pisa_select_prefill_static"]
 
 
 class Params(ctypes.Structure):
