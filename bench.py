@@ -38,6 +38,8 @@ def parse():
     ap.add_argument("--N", type=int, default=262144)
     ap.add_argument("--no-extras", action="store_true", help="skip the sweep, flat and decode side measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--profile-case", choices=["prefill64k", "decode8"], default=None,
+                    help="run one small invocation of every kernel (for ncu captures) and exit")
     return ap.parse_args()
 
 
@@ -481,8 +483,50 @@ def run_reference(args, ws, rank):
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def profile_case(name: str):
+    """One small invocation per kernel, sized for profiler captures: the 64K
+    prefill point (build, route, leaves, flat; inputs 335 MB > L2) or one
+    decode step of 8 sequences x 131073 keys (2.1 GB cache)."""
+    import torch
+    from pyramid_top_block_mean_gb300 import pisa
+    from pyramid_top_block_mean_gb300 import workloads as W
+    g = torch.Generator(device="cuda")
+    if name == "prefill64k":
+        s = W.sweep(65536)
+        g.manual_seed(3)
+        q = torch.randn(s.B, s.Hq, s.N, s.d, device="cuda", generator=g).to(torch.bfloat16)
+        k = torch.randn(s.B, s.Hkv, s.N, s.d, device="cuda", generator=g).to(torch.bfloat16)
+        p = pisa.params_from_shape(s)
+        sel = pisa.Selector(p)
+        sel.build(k)
+        pisa.prefill_route(p, q, sel.pyramid, sel.ws)
+        pisa.prefill_leaves(p, q, k, sel.ws, sel.out_idx, sel.out_score)
+        fs = pisa.Selector(p, mode="flat")
+        fs.build(k)
+        pisa.select_flat(p, q, fs.pyramid, fs.ws, fs.out_idx, fs.out_score)
+        torch.cuda.synchronize()
+        status = max(sel.device_status(), fs.device_status())
+    else:
+        s = W.Shape(B=8, N=W.DECODE_CACHED + 16, Hq=32, Hkv=8, d=128, K=32)
+        g.manual_seed(4)
+        kc = torch.randn(s.B, s.Hkv, s.N, s.d, device="cuda", generator=g, dtype=torch.bfloat16)
+        qd = torch.randn(s.B, s.Hq, s.d, device="cuda", generator=g, dtype=torch.bfloat16)
+        p = pisa.params_from_shape(s)
+        ds = pisa.Selector(p, mode="decode")
+        ds.build(kc, torch.full((s.B,), W.DECODE_CACHED, dtype=torch.int32, device="cuda"))
+        ds.decode(qd, kc, torch.full((s.B,), W.DECODE_CACHED + 1, dtype=torch.int32, device="cuda"))
+        torch.cuda.synchronize()
+        status = ds.device_status()
+    print(json.dumps({"profile_case": name, "device_status": status}))
+    if status != 0:
+        sys.exit(1)
+
+
 def main():
     args = parse()
+    if args.profile_case:
+        profile_case(args.profile_case)
+        return
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":
         line = run_reference(args, ws, rank)

@@ -28,12 +28,21 @@
 namespace pisa {
 
 template <int G, int NC>
-struct RouteQ {
+struct RouteQData {
   int32_t cand[2][NC];    // ping-pong candidate lists (ascending node order)
   float x[2][NC][G];      // s2 * q_g . mu_cand, when known
   int32_t hasx[2][NC];
   int32_t work[2 * NC];   // child rows whose dots are computed this level
   float y[2 * NC][G];     // their dots (s2 units)
+};
+
+// Per-query slice, padded so that the slices of the QPW queries sharing a
+// warp start 32/QPW banks apart: their lanes then never collide on a bank.
+template <int G, int NC, int QPW>
+struct RouteQ : RouteQData<G, NC> {
+  static constexpr int kWords = (int)(sizeof(RouteQData<G, NC>) / 4);
+  static constexpr int kPad = ((32 / QPW) - kWords % 32 + 64) % 32;
+  int32_t pad[kPad > 0 ? kPad : 1];
 };
 
 __device__ __forceinline__ uint32_t orderable(float f) {
@@ -94,7 +103,7 @@ __global__ void __launch_bounds__(WARPS * 32) route_kernel(Prob pr, Pyr s, const
   constexpr int QPW = 32 / LQ;                  // queries per warp
   static_assert(LPN <= LQ && NC % LQ == 0, "lane split");
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  RouteQ<G, NC>& sm = reinterpret_cast<RouteQ<G, NC>*>(smem_raw)[threadIdx.x / LQ];
+  RouteQ<G, NC, QPW>& sm = reinterpret_cast<RouteQ<G, NC, QPW>*>(smem_raw)[threadIdx.x / LQ];
   const int lane = threadIdx.x & 31, ll = lane % LQ;
   const int64_t nq = pr.B * pr.Hkv * pr.N;
   const int64_t qi = ((int64_t)blockIdx.x * WARPS + threadIdx.x / 32) * QPW + lane / LQ;
@@ -335,7 +344,7 @@ static cudaError_t launch_route_t(const Prob& pr, const Pyr& s, const void* q, c
                                   int32_t* trace, cudaStream_t st) {
   constexpr int DQ = (64 / G) < D ? 64 / G : D;
   constexpr int LQ = (D / DQ) > 8 ? 16 : 8;  // lanes per query
-  const size_t smem = sizeof(RouteQ<G, 2 * KM>) * (32 / LQ) * WARPS;
+  const size_t smem = sizeof(RouteQ<G, 2 * KM, 32 / LQ>) * (32 / LQ) * WARPS;
   auto kern = route_kernel<D, G, KM, WARPS, LQ>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
