@@ -27,11 +27,10 @@ namespace pisa {
 
 template <int NC>
 struct RouteMmaQ {
+  float4 x[2][NC];  // own dot per head of each candidate (known below the start level)
+  float4 y[2 * NC];  // child dots per head, by work-list position
   int32_t cand[2][NC];
-  float x[2][NC][4];
-  int32_t hasx[2][NC];
   int32_t work[2 * NC];
-  float y[2 * NC][4];
 };
 
 template <int NC>
@@ -39,7 +38,7 @@ struct RouteMmaQPad : RouteMmaQ<NC> {
   // the two queries of a warp start 16 banks apart
   static constexpr int kWords = (int)(sizeof(RouteMmaQ<NC>) / 4);
   static constexpr int kPad = (16 - kWords % 32 + 64) % 32;
-  int32_t pad[kPad > 0 ? kPad : 1];
+  int32_t pad[kPad > 0 ? kPad : 4];
 };
 
 __device__ __forceinline__ uint32_t orderable_key(float f) {
@@ -47,15 +46,15 @@ __device__ __forceinline__ uint32_t orderable_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ int scan16_seg(int v, int ll, int* tot) {
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 16; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o, 16);
-    if (ll >= o) x += y;
-  }
-  *tot = __shfl_sync(0xffffffffu, x, 15, 16);
-  return x - v;
+// Exclusive prefix sum of v in {0, 1, 2} over the 16 lanes of this lane's half
+// of the warp (two ballots, no shuffles); *tot receives the half's total.
+__device__ __forceinline__ int prefix16(int v, int lane, int* tot) {
+  const unsigned b0 = __ballot_sync(0xffffffffu, v & 1);
+  const unsigned b1 = __ballot_sync(0xffffffffu, v & 2);
+  const unsigned hm = (lane & 16) ? 0xffff0000u : 0x0000ffffu;
+  const unsigned lt = hm & ((1u << lane) - 1u);
+  *tot = __popc(b0 & hm) + 2 * __popc(b1 & hm);
+  return __popc(b0 & lt) + 2 * __popc(b1 & lt);
 }
 
 __device__ __forceinline__ bool elig_node(int level, int j, int e_hi) {
@@ -73,6 +72,10 @@ __device__ __forceinline__ float sib_dot(float x, float a, int n0, int n1) {
   return ((float)(n0 + n1) * x - (float)n0 * a) / (float)n1;
 }
 
+__device__ __forceinline__ float comp(const float4& v, int g) {
+  return g == 0 ? v.x : (g == 1 ? v.y : (g == 2 ? v.z : v.w));
+}
+
 __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                           uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -82,23 +85,33 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// fp32 pyramid -> bf16 hi (rounded) and lo (rounded residual), same layout.
-__global__ void split_pyramid_kernel(int64_t n, const float* __restrict__ pyr, __nv_bfloat16* __restrict__ hi,
-                                     __nv_bfloat16* __restrict__ lo) {
+// fp32 pyramid -> bf16 hi (rounded) and lo (rounded residual).  Within each
+// row of D dims the elements are permuted so that 128-byte line bb holds dims
+// [32 bb, 32 bb + 32) of the first half followed by the same 32 dims of the
+// second half: eight lanes then read one line per node (see the dot phase).
+__global__ void split_pyramid_kernel(int64_t n, int D, const float* __restrict__ pyr,
+                                     __nv_bfloat16* __restrict__ hi, __nv_bfloat16* __restrict__ lo) {
+  const int hd = D / 2;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int c = (int)(i % D);
+    const int64_t pos = (i - c) + ((c % hd) / 32) * 64 + (c / hd) * 32 + (c & 31);
     const float v = pyr[i];
     const __nv_bfloat16 h = __float2bfloat16_rn(v);
-    hi[i] = h;
-    lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+    hi[pos] = h;
+    lo[pos] = __float2bfloat16_rn(v - __bfloat162float(h));
   }
 }
 
-// K-block mapping: MMA k-step s of a lane with thread-in-group t uses the
-// physical dims 32 (s/2) + 8t + 4 (s%2) + {0..3}; for each pair of steps the
-// lane's dims are 8 contiguous elements (one 16-byte load), and the same
-// mapping is applied to A (child rows) and B (query heads).
+// MMA layout.  One m16n8k16 sequence serves one query and 8 child nodes:
+// A row r is (node r/2 of rows 0..7 or 4 + (r-8)/2, half r%2 of the D dims),
+// B column j is (query head j%4, half j/4), so only the blocks where the row
+// half equals the column half are used and a node's dot is the sum of its two
+// halves' results.  K-block mapping: k-step pair bb, thread-in-group t covers
+// dims 32 bb + 8 t + {0..7} of its half (one 16-byte load; words x, y for the
+// first step and z, w for the second).  With the permuted row layout the
+// eight lanes of a node read one contiguous 128-byte line per load.
 template <int D, int KM, int WARPS>
-__global__ void __launch_bounds__(WARPS * 32) route_mma_kernel(Prob pr, Pyr s, const uint16_t* __restrict__ q,
+__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob pr, Pyr s, const uint16_t* __restrict__ q,
                                                                const uint16_t* __restrict__ phi,
                                                                const uint16_t* __restrict__ plo,
                                                                int32_t* __restrict__ kept2,
@@ -106,7 +119,6 @@ __global__ void __launch_bounds__(WARPS * 32) route_mma_kernel(Prob pr, Pyr s, c
   constexpr int G = 4;
   constexpr int NC = 2 * KM;
   constexpr int CPL = NC / 16;
-  constexpr int NBLK = D / 32;  // 16-byte slices per row per lane
   extern __shared__ __align__(16) unsigned char smem_raw[];
   RouteMmaQPad<NC>& sm = reinterpret_cast<RouteMmaQPad<NC>*>(smem_raw)[threadIdx.x / 16];
   RouteMmaQPad<NC>* smw = reinterpret_cast<RouteMmaQPad<NC>*>(smem_raw) + (threadIdx.x / 32) * 2;
@@ -116,8 +128,7 @@ __global__ void __launch_bounds__(WARPS * 32) route_mma_kernel(Prob pr, Pyr s, c
   const int64_t qi = ((int64_t)blockIdx.x * WARPS + threadIdx.x / 32) * 2 + half;
   const bool live = qi < nq;
   const int64_t qc = live ? qi : nq - 1;
-  const int64_t t = qc % pr.N, bh = qc / pr.N;
-  const int64_t b = bh / pr.Hkv, h = bh % pr.Hkv;
+  const int64_t t = qc % pr.N;
   const int K = pr.K;
   const int64_t qb = t / s.C;
   int32_t* kout = kept2 + qc * K;
@@ -144,25 +155,29 @@ __global__ void __launch_bounds__(WARPS * 32) route_mma_kernel(Prob pr, Pyr s, c
   const int l0w = max(l0, __shfl_xor_sync(0xffffffffu, l0, 16));
   if (l0w == 0) return;  // warp-uniform
 
-  // B fragments: column grp = (query half, head grp % 4); unscaled bf16 pairs
-  uint32_t bq[D / 16][2];
-  {
-    const int64_t qrow = ((b * pr.Hq + h * G + (grp & 3)) * pr.N + t) * D;
-#pragma unroll
-    for (int blk = 0; blk < NBLK; ++blk) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(q + qrow + 32 * blk + 8 * tig));
-      bq[2 * blk][0] = v.x; bq[2 * blk][1] = v.y;
-      bq[2 * blk + 1][0] = v.z; bq[2 * blk + 1][1] = v.w;
-    }
-  }
-  // the two queries of a warp may belong to different (b, h) rows of the pyramid
+  // B fragments of both queries: column grp = (head grp % 4, half grp / 4)
+  constexpr int NB = D / 64;  // k-step pairs per half
   const int64_t qw = ((int64_t)blockIdx.x * WARPS + threadIdx.x / 32) * 2;
-  const int64_t pbase0 = (min(qw, nq - 1) / pr.N) * s.P * D;
-  const int64_t pbase1 = (min(qw + 1, nq - 1) / pr.N) * s.P * D;
+  uint32_t bq[2][NB][4];
+  int64_t pbase[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int64_t qu = min(qw + u, nq - 1);
+    const int64_t tu = qu % pr.N, bhu = qu / pr.N;
+    const int64_t qrow = (((bhu / pr.Hkv) * pr.Hq + (bhu % pr.Hkv) * G + (grp & 3)) * pr.N + tu) * D +
+                         (grp >> 2) * (D / 2) + 8 * tig;
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(q + qrow + 32 * bb));
+      bq[u][bb][0] = v.x; bq[u][bb][1] = v.y; bq[u][bb][2] = v.z; bq[u][bb][3] = v.w;
+    }
+    // the two queries of a warp may belong to different (b, h) rows of the pyramid
+    pbase[u] = bhu * s.P * D;
+  }
 
   int cur = 0;
   int nc = l0 > 0 ? (int)eligible_count(l0, qb) : 0;
-  for (int i = ll; i < nc; i += 16) { sm.cand[0][i] = i; sm.hasx[0][i] = 0; }
+  for (int i = ll; i < nc; i += 16) sm.cand[0][i] = i;
   const int e_hi = (int)(qb - 2);
   __syncwarp();
 
@@ -170,8 +185,10 @@ __global__ void __launch_bounds__(WARPS * 32) route_mma_kernel(Prob pr, Pyr s, c
     const bool act = level <= l0;
     const int ncur = act ? nc : 0;
     const int ncap = (int)s.size[level - 2];
+    const bool hx = level < l0;  // candidates made by expansion carry their own dot
 
-    // 1. work list
+    // 1. work list: the first child of every candidate, and the second one
+    //    unless it follows from the candidate's own dot
     int c0v[CPL], e0v[CPL], e1v[CPL], s0v[CPL], s1v[CPL];
     int nwork = 0;
 #pragma unroll
@@ -181,9 +198,9 @@ __global__ void __launch_bounds__(WARPS * 32) route_mma_kernel(Prob pr, Pyr s, c
       const int c0 = valid ? 2 * sm.cand[cur][i] : 0;
       const int e0 = valid && c0 < ncap && elig_node(level - 1, c0, e_hi);
       const int e1 = valid && c0 + 1 < ncap && elig_node(level - 1, c0 + 1, e_hi);
-      const int der = e0 && e1 && sm.hasx[cur][i];
+      const int der = e0 && e1 && hx;
       int tot;
-      int p = nwork + scan16_seg(e0 + (e1 && !der), ll, &tot);
+      int p = nwork + prefix16(e0 + (e1 && !der), lane, &tot);
       s0v[sl] = e0 ? p : -1;
       if (e0) sm.work[p++] = c0;
       s1v[sl] = e1 ? (der ? -2 : p) : -1;
@@ -193,68 +210,92 @@ __global__ void __launch_bounds__(WARPS * 32) route_mma_kernel(Prob pr, Pyr s, c
     }
     __syncwarp();
 
-    // 2. dot products: 8 rows of each query per m16n8k16 tile sequence
+    // 2. dot products: per query, 8 child nodes per m16n8k16 sequence
     {
-      const int nw0 = __shfl_sync(0xffffffffu, nwork, 0), nw1 = __shfl_sync(0xffffffffu, nwork, 16);
-      const int nmax = max(nw0, nw1);
-      const int64_t loff = s.off[level - 2] * D + 8 * tig;
+      const int nw[2] = {__shfl_sync(0xffffffffu, nwork, 0), __shfl_sync(0xffffffffu, nwork, 16)};
+      const int nmax = max(nw[0], nw[1]);
+      const int64_t loff = s.off[level - 2] * D + (grp & 1) * 32 + 8 * tig;
+      // lanes (even group, t < 2) finish node grp/2, lanes (odd group, t >= 2) node 4 + grp/2
+      const bool roleA = !(grp & 1) && tig < 2, roleB = (grp & 1) && tig >= 2;
+      const float sc = pr.scale2;
       for (int r0 = 0; r0 < nmax; r0 += 8) {
-        const int wa = r0 + grp;  // work row of query 0 (MMA row grp) and of query 1 (row grp + 8)
-        const bool oka = wa < nw0, okb = wa < nw1;
-        const int64_t ra = pbase0 + loff + (int64_t)(oka ? smw[0].work[wa] : 0) * D;
-        const int64_t rb = pbase1 + loff + (int64_t)(okb ? smw[1].work[wa] : 0) * D;
-        uint4 ha[NBLK], la[NBLK], hb[NBLK], lb[NBLK];
+        uint4 hv[2][2][NB], lv[2][2][NB];  // [query][row grp / grp + 8][pair]
 #pragma unroll
-        for (int blk = 0; blk < NBLK; ++blk) {
-          ha[blk] = __ldg(reinterpret_cast<const uint4*>(phi + ra + 32 * blk));
-          la[blk] = __ldg(reinterpret_cast<const uint4*>(plo + ra + 32 * blk));
-          hb[blk] = __ldg(reinterpret_cast<const uint4*>(phi + rb + 32 * blk));
-          lb[blk] = __ldg(reinterpret_cast<const uint4*>(plo + rb + 32 * blk));
-        }
-        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int u = 0; u < 2; ++u)
 #pragma unroll
-        for (int blk = 0; blk < NBLK; ++blk) {
-          // step 2*blk: dims 8t + 0..3 (words x, y); step 2*blk+1: dims 8t + 4..7 (z, w)
-          mma_16816(d, ha[blk].x, hb[blk].x, ha[blk].y, hb[blk].y, bq[2 * blk][0], bq[2 * blk][1]);
-          mma_16816(d, la[blk].x, lb[blk].x, la[blk].y, lb[blk].y, bq[2 * blk][0], bq[2 * blk][1]);
-          mma_16816(d, ha[blk].z, hb[blk].z, ha[blk].w, hb[blk].w, bq[2 * blk + 1][0], bq[2 * blk + 1][1]);
-          mma_16816(d, la[blk].z, lb[blk].z, la[blk].w, lb[blk].w, bq[2 * blk + 1][0], bq[2 * blk + 1][1]);
-        }
-        // lanes with tig < 2 hold (query 0 row wa, heads 2tig, 2tig+1);
-        // lanes with tig >= 2 hold (query 1 row wa, heads 2tig-4, 2tig-3)
-        const float sc = pr.scale2;
-        if (tig < 2) {
-          if (oka) { smw[0].y[wa][2 * tig] = d[0] * sc; smw[0].y[wa][2 * tig + 1] = d[1] * sc; }
-        } else {
-          if (okb) { smw[1].y[wa][2 * tig - 4] = d[2] * sc; smw[1].y[wa][2 * tig - 3] = d[3] * sc; }
+          for (int rr = 0; rr < 2; ++rr) {
+            const int w = r0 + 4 * rr + (grp >> 1);
+            const int64_t ro = pbase[u] + loff + (int64_t)(w < nw[u] ? smw[u].work[w] : 0) * D;
+#pragma unroll
+            for (int bb = 0; bb < NB; ++bb) {
+              hv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(phi + ro + 64 * bb));
+              lv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(plo + ro + 64 * bb));
+            }
+          }
+        // four independent accumulator chains: (query) x (hi, lo)
+        float dh[2][4], dl[2][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dh[u][e] = dl[u][e] = 0.0f;
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint4 h0 = hv[u][0][bb], h1 = hv[u][1][bb], l0v = lv[u][0][bb], l1v = lv[u][1][bb];
+            mma_16816(dh[u], h0.x, h1.x, h0.y, h1.y, bq[u][bb][0], bq[u][bb][1]);
+            mma_16816(dl[u], l0v.x, l1v.x, l0v.y, l1v.y, bq[u][bb][0], bq[u][bb][1]);
+            mma_16816(dh[u], h0.z, h1.z, h0.w, h1.w, bq[u][bb][2], bq[u][bb][3]);
+            mma_16816(dl[u], l0v.z, l1v.z, l0v.w, l1v.w, bq[u][bb][2], bq[u][bb][3]);
+          }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          float d[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) d[e] = dh[u][e] + dl[u][e];
+          // add the two halves: partner lane = lane ^ 6 (group ^ 1, t ^ 2)
+          const float x0 = __shfl_xor_sync(0xffffffffu, roleA ? d[2] : d[0], 6);
+          const float x1 = __shfl_xor_sync(0xffffffffu, roleA ? d[3] : d[1], 6);
+          const int w = r0 + (roleA ? 0 : 4) + (grp >> 1);
+          if ((roleA || roleB) && w < nw[u]) {
+            const float2 v = roleA ? make_float2((d[0] + x0) * sc, (d[1] + x1) * sc)
+                                   : make_float2((d[2] + x0) * sc, (d[3] + x1) * sc);
+            *reinterpret_cast<float2*>(reinterpret_cast<float*>(&smw[u].y[w]) + 2 * (tig & 1)) = v;
+          }
         }
       }
     }
     __syncwarp();
 
-    // 3. scores and rank keys
-    uint64_t key[CPL];
+    // 3. scores and rank keys (higher score first, then lower index)
+    uint32_t key[CPL];
+    float4 ya[CPL], yb[CPL];
 #pragma unroll
     for (int sl = 0; sl < CPL; ++sl) {
       const int i = sl * 16 + ll;
       key[sl] = 0;
+      ya[sl] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      yb[sl] = ya[sl];
       if (i < ncur) {
         const int s0 = s0v[sl], s1 = s1v[sl];
-        int n0 = 0, n1 = 0;
-        if (s1 == -2) {
-          n0 = count_node(s.C, level - 1, c0v[sl], s.N);
-          n1 = count_node(s.C, level - 1, c0v[sl] + 1, s.N);
+        if (s0 >= 0) ya[sl] = sm.y[s0];
+        if (s1 >= 0) {
+          yb[sl] = sm.y[s1];
+        } else if (s1 == -2) {
+          const int n0 = count_node(s.C, level - 1, c0v[sl], s.N);
+          const int n1 = count_node(s.C, level - 1, c0v[sl] + 1, s.N);
+          const float4 xv = sm.x[cur][i];
+          yb[sl] = make_float4(sib_dot(xv.x, ya[sl].x, n0, n1), sib_dot(xv.y, ya[sl].y, n0, n1),
+                               sib_dot(xv.z, ya[sl].z, n0, n1), sib_dot(xv.w, ya[sl].w, n0, n1));
         }
         float scv = 0.0f;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float a = s0 >= 0 ? sm.y[s0][g] : 0.0f;
-          float bb = 0.0f;
-          if (s1 >= 0) bb = sm.y[s1][g];
-          else if (s1 == -2) bb = sib_dot(sm.x[cur][i][g], a, n0, n1);
+          const float a = comp(ya[sl], g), bb = comp(yb[sl], g);
           scv += (s0 >= 0 && s1 != -1) ? lse2_pair(a, bb) : (s0 >= 0 ? a : bb);
         }
-        key[sl] = ((uint64_t)orderable_key(scv) << 32) | (uint32_t)(~(uint32_t)sm.cand[cur][i]);
+        if (scv == 0.0f) scv = 0.0f;  // -0 ranks like +0
+        key[sl] = orderable_key(scv);
       }
     }
     int rank[CPL];
@@ -262,17 +303,19 @@ __global__ void __launch_bounds__(WARPS * 32) route_mma_kernel(Prob pr, Pyr s, c
     for (int sl = 0; sl < CPL; ++sl) rank[sl] = 0;
 #pragma unroll
     for (int sj = 0; sj < CPL; ++sj) {
-      const uint32_t khi = (uint32_t)(key[sj] >> 32), klo = (uint32_t)key[sj];
 #pragma unroll
       for (int l = 0; l < 16; ++l) {
-        const uint64_t kj = ((uint64_t)__shfl_sync(0xffffffffu, khi, l, 16) << 32) |
-                            __shfl_sync(0xffffffffu, klo, l, 16);
+        const uint32_t kj = __shfl_sync(0xffffffffu, key[sj], l, 16);
 #pragma unroll
-        for (int sl = 0; sl < CPL; ++sl) rank[sl] += kj > key[sl] ? 1 : 0;
+        for (int sl = 0; sl < CPL; ++sl) {
+          // equal scores: the lower slot (the lower node index) ranks first
+          const bool before = sj < sl || (sj == sl && l < ll);
+          rank[sl] += (kj > key[sl] || (kj == key[sl] && before)) ? 1 : 0;
+        }
       }
     }
 
-    // 4. kept set, expansion
+    // 4. kept set (index order), next candidates (ascending) or the kept level-2 nodes
     const int nxt = cur ^ 1;
     int nkept = 0, nchild = 0;
 #pragma unroll
@@ -281,35 +324,20 @@ __global__ void __launch_bounds__(WARPS * 32) route_mma_kernel(Prob pr, Pyr s, c
       const int keep = (i < ncur && rank[sl] < K) ? 1 : 0;
       const int nch = keep && level > 2 ? e0v[sl] + e1v[sl] : 0;
       int ktot, ctot;
-      const int kp = nkept + scan16_seg(keep, ll, &ktot);
-      int cp = nchild + scan16_seg(nch, ll, &ctot);
+      const int kp = nkept + prefix16(keep, lane, &ktot);
+      int cp = nchild + prefix16(nch, lane, &ctot);
       if (keep) {
         const int32_t ci = sm.cand[cur][i];
         if (trow) trow[(level - 1) * K + kp] = ci;
         if (level == 2) kout[kp] = ci;
-        if (nch) {
-          const int s0 = s0v[sl], s1 = s1v[sl];
-          int n0 = 0, n1 = 0;
-          if (s1 == -2) {
-            n0 = count_node(s.C, level - 1, c0v[sl], s.N);
-            n1 = count_node(s.C, level - 1, c0v[sl] + 1, s.N);
-          }
-          if (e0v[sl]) {
-            sm.cand[nxt][cp] = c0v[sl];
-#pragma unroll
-            for (int g = 0; g < G; ++g) sm.x[nxt][cp][g] = sm.y[s0][g];
-            sm.hasx[nxt][cp] = 1;
-            ++cp;
-          }
-          if (e1v[sl]) {
-            sm.cand[nxt][cp] = c0v[sl] + 1;
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const float a = e0v[sl] ? sm.y[s0][g] : 0.0f;
-              sm.x[nxt][cp][g] = s1 >= 0 ? sm.y[s1][g] : sib_dot(sm.x[cur][i][g], a, n0, n1);
-            }
-            sm.hasx[nxt][cp] = 1;
-          }
+        if (e0v[sl] && nch) {
+          sm.cand[nxt][cp] = c0v[sl];
+          sm.x[nxt][cp] = ya[sl];
+          ++cp;
+        }
+        if (e1v[sl] && nch) {
+          sm.cand[nxt][cp] = c0v[sl] + 1;
+          sm.x[nxt][cp] = yb[sl];
         }
       }
       nkept += ktot;
@@ -347,7 +375,7 @@ cudaError_t launch_route_mma(const Prob& pr, const Pyr& s, const void* q, const 
   const int64_t n = pr.B * pr.Hkv * s.P * pr.d;
   if (n == 0) return cudaSuccess;
   split_pyramid_kernel<<<(unsigned)std::min<int64_t>(ceil_div64(n, 256), 8192), 256, 0, st>>>(
-      n, pyr, (__nv_bfloat16*)phi, (__nv_bfloat16*)plo);
+      n, pr.d, pyr, (__nv_bfloat16*)phi, (__nv_bfloat16*)plo);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 #define PISA_RM_CASE(DD)                                                                                  \
