@@ -50,9 +50,10 @@
  *    device status word that kernels set on faults they detect (a decode
  *    sequence length outside [1, N], an exhausted bounded wait); each call
  *    clears it first.  Calls that share a workspace must not overlap.
- *  - The library holds no global state besides the loaded kernels and a
- *    per-device cache of SM counts; it is safe to call from several threads
- *    on different streams with different workspaces.
+ *  - The library holds no global state besides the loaded kernels, a
+ *    per-device cache of SM counts, a process-wide launch counter and the
+ *    fixed scratch of pisa_select_prefill_static; it is safe to call from
+ *    several threads on different streams with different workspaces.
  */
 #ifndef PISA_H_
 #define PISA_H_
@@ -107,6 +108,11 @@ typedef struct {
 
 /* ABI version of the loaded library (PISA_ABI_VERSION). */
 int pisa_abi_version(void);
+
+/* Number of kernel launches this library has issued in this process, over
+ * all devices and streams (a relaxed atomic counter, for launch accounting in
+ * benchmarks).  Host only; never fails. */
+uint64_t pisa_kernel_launches(void);
 
 /* Human-readable name of a status. */
 const char* pisa_status_string(pisa_status s);

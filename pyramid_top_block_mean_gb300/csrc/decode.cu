@@ -493,6 +493,7 @@ static cudaError_t launch_decode_t(const Prob& pr, const Pyr& s, const void* q, 
   auto kern = decode_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  note_launch();
   kern<<<(unsigned)(pr.B * pr.Hkv), kDecThreads, smem, st>>>(pr, s, q, kc, seq_lens, pyr, status, out_idx,
                                                               out_score, trace);
   return cudaGetLastError();

@@ -351,6 +351,7 @@ static cudaError_t launch_flat_t(const Prob& pr, int64_t nb, const void* q, cons
   FlatTiles ft;
   ft.Qt = kFRows / G;
   ft.nqt = ceil_div64(pr.N, ft.Qt);
+  note_launch();
   kern<<<grid, kFlatThreads, smem, st>>>(pr, ft, nb, mumap, (const uint16_t*)q, out_idx, out_score, status);
   return cudaGetLastError();
 }
@@ -362,6 +363,7 @@ cudaError_t launch_flat(const Prob& pr, const Pyr& s, const void* q, const float
   __nv_bfloat16* mu = (__nv_bfloat16*)(ws + 256);
   const int64_t nbh = pr.B * pr.Hkv;
   const int64_t n = nbh * s.nb * pr.d;
+  note_launch();
   means_to_bf16_kernel<<<(unsigned)std::min<int64_t>(ceil_div64(n, 256), 4096), 256, 0, st>>>(nbh, s.P, s.nb, pr.d,
                                                                                                pyr, mu);
   cudaError_t e = cudaGetLastError();

@@ -159,6 +159,7 @@ cudaError_t launch_leaf_simt(const Prob& pr, const Pyr& s, const void* q, const 
   const unsigned grid = (unsigned)ceil_div64(nq, kLeafWarps);
 #define PISA_LEAF_CASE(DD, GG)                                                                         \
   if (pr.d == DD && pr.G == GG) {                                                                      \
+    note_launch();                                                                                     \
     leaf_simt_kernel<DD, GG><<<grid, kLeafWarps * 32, 0, st>>>(pr, s, q, k, kept2, out_idx, out_score); \
     return cudaGetLastError();                                                                         \
   }

@@ -519,6 +519,7 @@ static cudaError_t launch_leaf_tc_t(const Prob& pr, const PrefillWs& w, char* ws
   auto kern = leaf_tc_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  note_launch();
   kern<<<grid, kLeafTcThreads, smem, st>>>(pr, w.n2, w.nchunk, kmap, (const uint16_t*)q,
                                            (const int4*)(ws + w.tile_info),
                                            (const int32_t*)(ws + w.tile_off) + w.nbuckets,
@@ -544,10 +545,14 @@ cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, cha
     if (e != cudaSuccess) return e;
     const int64_t n = nq * pr.K;
     const unsigned g1 = (unsigned)std::min<int64_t>(ceil_div64(n, 256), (int64_t)num_sms * 16);
+    note_launch();
     count_kernel<<<g1, 256, 0, st>>>(a, kept2, counts);
+    note_launch();
     scan_kernel<<<1, 1024, 0, st>>>(w.nbuckets, Q, counts, offsets, tile_off);
+    note_launch();
     scatter_kernel<<<g1, 256, 0, st>>>(a, kept2, offsets, cursor, (int32_t*)(ws + w.pairs));
     const unsigned g2 = (unsigned)std::min<int64_t>(ceil_div64(w.nbuckets, 256), (int64_t)num_sms * 8);
+    note_launch();
     tiles_kernel<<<g2, 256, 0, st>>>(w.nbuckets, Q, counts, offsets, tile_off, (int4*)(ws + w.tile_info));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -562,6 +567,7 @@ cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, cha
 #undef PISA_LEAF_TC_CASE
     if (e != cudaSuccess) return e;
   }
+  note_launch();
   if (pr.K <= 8)
     finalize_small_kernel<<<(unsigned)ceil_div64(nq, 256), 256, 0, st>>>(pr, kept2, (const float*)(ws + w.leaf_score),
                                                                          out_idx, out_score);

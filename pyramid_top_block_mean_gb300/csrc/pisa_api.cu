@@ -1,6 +1,7 @@
 // pisa_api.cu -- the C ABI of include/pisa.h: argument checks, workspace
 // layout and kernel launches.  Every check runs on the host before the first
 // launch; a failing call launches nothing.
+#include <atomic>
 #include <math.h>
 #include <mutex>
 
@@ -105,6 +106,10 @@ static bool aligned16(const void* x) { return ((uintptr_t)x & 15u) == 0; }
 
 static pisa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PISA_OK : PISA_ERR_CUDA; }
 
+static std::atomic<unsigned long long> g_launches{0};
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 }  // namespace pisa
 
 using namespace pisa;
@@ -112,6 +117,8 @@ using namespace pisa;
 extern "C" {
 
 int pisa_abi_version(void) { return PISA_ABI_VERSION; }
+
+uint64_t pisa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* pisa_status_string(pisa_status s) {
   switch (s) {

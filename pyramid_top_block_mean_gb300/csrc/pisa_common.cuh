@@ -132,8 +132,8 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 // log2(2^a + 2^b) without overflow.
 __device__ __forceinline__ float lse2_pair(float a, float b) {
-  const float m = fmaxf(a, b);
-  return m + __log2f(exp2f(a - m) + exp2f(b - m));
+  const float m = fmaxf(a, b), n = fminf(a, b);
+  return m + __log2f(1.0f + exp2f(n - m));
 }
 
 // Record the first device fault in the workspace status word.

@@ -41,6 +41,9 @@ size_t flat_ws_bytes(const Prob& pr, const Pyr& s);
 
 int sm_count(int device);
 
+// Counts one kernel launch (process-wide, relaxed atomic); called before every launch.
+void note_launch();
+
 // 2D TMA view [rows, d] of a bf16 tensor: box of 64 columns x box_rows rows,
 // 128-byte swizzle (the K-major operand layout of the tcgen05 MMAs).
 bool make_tmap_rows(CUtensorMap* m, const void* base, int64_t rows, int d, int box_rows);

@@ -145,11 +145,13 @@ cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, co
                                  float* pyr, cudaStream_t st) {
   if (pr.B == 0 || pr.Hkv == 0 || s.nb == 0) return cudaSuccess;
   dim3 g1((unsigned)ceil_div64(s.nb, kLeavesPerCta), (unsigned)pr.Hkv, (unsigned)pr.B);
+  note_launch();
   if (pr.d == 128) build_lower_kernel<128><<<g1, 256, 0, st>>>(pr, s, k, seq_lens, pyr);
   else build_lower_kernel<64><<<g1, 256, 0, st>>>(pr, s, k, seq_lens, pyr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || s.L <= kLowerLevels) return e;
   dim3 g2((unsigned)pr.Hkv, (unsigned)pr.B);
+  note_launch();
   if (pr.d == 128) build_upper_kernel<128><<<g2, 256, 0, st>>>(pr, s, seq_lens, pyr);
   else build_upper_kernel<64><<<g2, 256, 0, st>>>(pr, s, seq_lens, pyr);
   return cudaGetLastError();

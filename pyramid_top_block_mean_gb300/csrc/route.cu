@@ -350,6 +350,7 @@ static cudaError_t launch_route_t(const Prob& pr, const Pyr& s, const void* q, c
   if (e != cudaSuccess) return e;
   const int64_t nq = pr.B * pr.Hkv * pr.N;
   const int64_t grid = ceil_div64(nq, (32 / LQ) * WARPS);
+  note_launch();
   kern<<<(unsigned)grid, WARPS * 32, smem, st>>>(pr, s, q, pyr, kept2, trace);
   return cudaGetLastError();
 }

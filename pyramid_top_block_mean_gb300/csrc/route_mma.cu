@@ -308,9 +308,10 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob 
         const uint32_t kj = __shfl_sync(0xffffffffu, key[sj], l, 16);
 #pragma unroll
         for (int sl = 0; sl < CPL; ++sl) {
-          // equal scores: the lower slot (the lower node index) ranks first
-          const bool before = sj < sl || (sj == sl && l < ll);
-          rank[sl] += (kj > key[sl] || (kj == key[sl] && before)) ? 1 : 0;
+          // equal scores: the lower slot (the lower node index) ranks first.
+          // Keys of real scores are at most 0xff800000, so kj + 1 cannot wrap.
+          const uint32_t before = (sj < sl || (sj == sl && l < ll)) ? 1u : 0u;
+          rank[sl] += (kj + before > key[sl]) ? 1 : 0;
         }
       }
     }
@@ -361,6 +362,7 @@ static cudaError_t launch_route_mma_t(const Prob& pr, const Pyr& s, const void* 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t nq = pr.B * pr.Hkv * pr.N;
+  note_launch();
   kern<<<(unsigned)ceil_div64(nq, 2 * WARPS), WARPS * 32, smem, st>>>(pr, s, (const uint16_t*)q, phi, plo, kept2,
                                                                         trace);
   return cudaGetLastError();
@@ -374,6 +376,7 @@ cudaError_t launch_route_mma(const Prob& pr, const Pyr& s, const void* q, const 
                              uint16_t* plo, int32_t* kept2, int32_t* trace, cudaStream_t st) {
   const int64_t n = pr.B * pr.Hkv * s.P * pr.d;
   if (n == 0) return cudaSuccess;
+  note_launch();
   split_pyramid_kernel<<<(unsigned)std::min<int64_t>(ceil_div64(n, 256), 8192), 256, 0, st>>>(
       n, pr.d, pyr, (__nv_bfloat16*)phi, (__nv_bfloat16*)plo);
   cudaError_t e = cudaGetLastError();

@@ -34,7 +34,7 @@ DEV_OK, DEV_BAD_SEQ_LEN, DEV_TIMEOUT, DEV_BAD_INDEX = 0, 1, 2, 3
 EXPORTED = ["pisa_abi_version", "pisa_status_string", "pisa_pyramid_levels", "pisa_pyramid_nodes",
             "pisa_pyramid_bytes", "pisa_workspace_bytes", "pisa_build_pyramid", "pisa_select_prefill",
             "pisa_prefill_route", "pisa_prefill_leaves", "pisa_select_decode", "pisa_select_flat",
-            "pisa_read_device_status", "pisa_select_prefill_static"]
+            "pisa_read_device_status", "pisa_select_prefill_static", "pisa_kernel_launches"]
 
 
 class Params(ctypes.Structure):
@@ -48,6 +48,7 @@ class Params(ctypes.Structure):
 _P = ctypes.POINTER(Params)
 _vp = ctypes.c_void_p
 _lib.pisa_abi_version.restype = ctypes.c_int
+_lib.pisa_kernel_launches.restype = ctypes.c_uint64
 _lib.pisa_status_string.argtypes = [ctypes.c_int]
 _lib.pisa_status_string.restype = ctypes.c_char_p
 _lib.pisa_pyramid_levels.argtypes = [_P]
@@ -90,6 +91,11 @@ def status_string(code: int) -> str:
 
 def abi_version() -> int:
     return _lib.pisa_abi_version()
+
+
+def kernel_launches() -> int:
+    """Kernel launches the library has issued in this process so far."""
+    return _lib.pisa_kernel_launches()
 
 
 def make_params(B: int, N: int, H_q: int, H_kv: int, d: int, C: int = 64, g: int = 2, K: int = 8,
