@@ -40,6 +40,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--profile-case", choices=["prefill64k", "decode8"], default=None,
                     help="run one small invocation of every kernel (for ncu captures) and exit")
+    ap.add_argument("--configs", action="store_true",
+                    help="time every listed workload (GPU and CPU oracle), one JSON line each, and exit")
     return ap.parse_args()
 
 
@@ -163,8 +165,12 @@ def eligible_count(level, qb):
 
 
 def algorithmic_work(s, kept2):
-    """Exact leaf work from the routing output, plus the routing and byte
-    counts of the method ("algorithmic work")."""
+    """Algorithmic work of one prefill step.  Leaf flops are exact, from the
+    routing output: 2 d G C per eligible (query, leaf) candidate.  Routing
+    flops are 2 d G per child summary scored, with at most 2 eligible
+    children for each of at most 2K candidates per level below the start
+    level.  Bytes: q and k read once, the fp32 pyramid written and read
+    once, and the K + 3 outputs written."""
     import numpy as np
     K, C, d, G = s.K, s.C, s.d, s.G
     t = np.arange(s.N)
@@ -309,25 +315,66 @@ def run_pisa(args, ws, rank, local):
                 "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
                 "traffic": load_traffic("build_lower_kernel"), "peak_source": f"{pk['source']} copy"}
 
-    # end to end through the public API with host buffers
-    out_h = torch.empty(sel.out_idx.shape, dtype=torch.int32).pin_memory()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(3, min(args.steps, 5))
-    torch.cuda.synchronize(dev)
+    # end to end through the public API with host buffers: every step copies
+    # its q and k from pinned host memory and reads its indices back.  Steps
+    # are pipelined over two buffer sets: the copy of step i+1's inputs and
+    # the read-back of step i-1's indices overlap the selection of step i.
+    del sel
+    torch.cuda.empty_cache()
+    sels = [pisa.Selector(p, device=dev) for _ in range(2)]
+    qs = [q, torch.empty_like(q)]
+    ks = [k, torch.empty_like(k)]
+    out_h = [torch.empty(sels[0].out_idx.shape, dtype=torch.int32).pin_memory() for _ in range(2)]
+    cs_in = torch.cuda.Stream(dev)
+    cs_out = torch.cuda.Stream(dev)
+    e2e_steps = max(4, min(args.steps, 8))
+
+    def e2e_run(n):
+        ready = [torch.cuda.Event() for _ in range(2)]
+        done = [torch.cuda.Event() for _ in range(2)]
+        read = [torch.cuda.Event() for _ in range(2)]
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_end = torch.cuda.Event(enable_timing=True)
+        e_start.record(st)
+        cs_in.wait_event(e_start)
+        with torch.cuda.stream(cs_in):
+            qs[0].copy_(q_h, non_blocking=True)
+            ks[0].copy_(k_h, non_blocking=True)
+        ready[0].record(cs_in)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                nb_ = (i + 1) % 2
+                if i >= 1:
+                    cs_in.wait_event(done[nb_])  # step i-1 has finished reading buffer nb_
+                with torch.cuda.stream(cs_in):
+                    qs[nb_].copy_(q_h, non_blocking=True)
+                    ks[nb_].copy_(k_h, non_blocking=True)
+                ready[nb_].record(cs_in)
+            st.wait_event(ready[b])
+            if i >= 2:
+                st.wait_event(read[b])  # step i-2's indices have left selector b
+            sels[b].prefill(qs[b], ks[b], stream=st)
+            done[b].record(st)
+            cs_out.wait_event(done[b])
+            with torch.cuda.stream(cs_out):
+                out_h[b].copy_(sels[b].out_idx, non_blocking=True)
+            read[b].record(cs_out)
+        st.wait_stream(cs_out)
+        e_end.record(st)
+        torch.cuda.synchronize(dev)
+        return e_start.elapsed_time(e_end) / n
+
+    e2e_run(2)
     barrier(ws)
-    e0.record(st)
-    for _ in range(e2e_steps):
-        q.copy_(q_h, non_blocking=True)
-        k.copy_(k_h, non_blocking=True)
-        sel.prefill(q, k, stream=st)
-        out_h.copy_(sel.out_idx, non_blocking=True)
-    e1.record(st)
-    torch.cuda.synchronize(dev)
-    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, ws)
+    e2e_ms = reduce_max(e2e_run(e2e_steps), ws)
     e2e = {"value": whole_job_rate(s.B * s.N, ws, e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": q_h.numel() * 2 + k_h.numel() * 2,
-           "d2h_bytes_per_step": out_h.numel() * 4}
+           "d2h_bytes_per_step": out_h[0].numel() * 4, "steps": e2e_steps,
+           "how": "pisa_select_prefill (build + select) per step; H2D of q, k from pinned memory and D2H of "
+                  "the indices on two copy streams, double-buffered so they overlap the neighbouring steps"}
+    del sels, qs, ks
+    torch.cuda.empty_cache()
 
     extras = {}
     if not args.no_extras:
@@ -533,10 +580,121 @@ def profile_case(name: str):
         sys.exit(1)
 
 
+def _cuda_ms(fn, reps, st):
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(reps):
+        fn()
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def configs_table():
+    """Every listed workload: GPU prefill (build + select) and flat-comparator
+    times with CUDA events, the CPU oracle on the host cores (in full where it
+    takes seconds, else the sampled estimate of cpu_baseline), and the decode
+    step.  Side table, not the headline line."""
+    import time as _t
+    import numpy as np
+    import torch
+    import oracle
+    from pyramid_top_block_mean_gb300 import pisa
+    from pyramid_top_block_mean_gb300 import workloads as W
+    st = torch.cuda.current_stream()
+    rows = []
+
+    def prefill_row(name, s, q, k, cpu_full):
+        p = pisa.params_from_shape(s)
+        sel = pisa.Selector(p)
+        qd, kd = q.cuda(), k.cuda()
+        reps = 20 if s.N <= 65536 else 5
+        t_pisa = _cuda_ms(lambda: sel.prefill(qd, kd, stream=st), reps, st)
+        t_flat = None
+        if s.dtype == "bf16":
+            fs = pisa.Selector(p, mode="flat")
+            t_flat = _cuda_ms(lambda: fs.flat(qd, kd, stream=st), max(2, reps // 4), st)
+            del fs
+        del sel, qd, kd
+        torch.cuda.empty_cache()
+        if cpu_full:
+            o = oracle.Oracle.from_shape(s)
+            t0 = _t.perf_counter()
+            pyr = o.pyramid(k.double().numpy())
+            o.select(q.double().numpy(), k.double().numpy(), pyr)
+            cpu_ms, cpu_how = (_t.perf_counter() - t0) * 1e3, "full"
+        else:
+            cb = cpu_baseline(s, q, k, budget_s=5.0)
+            cpu_ms, cpu_how = s.B * s.N / cb["value"] * 1e3, "sampled: " + cb["sample"]
+        rows.append({"config": name, "N": s.N, "K": s.K, "dtype": s.dtype, "pisa_ms": t_pisa,
+                     "pisa_queries_per_s": s.B * s.N / t_pisa * 1e3, "flat_ms": t_flat,
+                     "pisa_over_flat": (t_flat / t_pisa) if t_flat else None,
+                     "cpu_oracle_ms": cpu_ms, "cpu_cores": oracle.num_threads(), "cpu_how": cpu_how})
+        print(json.dumps(rows[-1]), flush=True)
+
+    q, k = W.iid(W.TINY, 0)
+    prefill_row("tiny B=1 N=1024 H=1/1 d=64 fp32 K=4", W.TINY, q, k, True)
+    q, k = W.planted(W.PRETRAIN, 1)
+    prefill_row("pretrain B=2 N=4096 16/4 d=128 bf16 K=8 planted", W.PRETRAIN, q, k, True)
+    q, k, _ = W.needles(W.CPT, 2)
+    prefill_row("CPT B=1 N=16384 16/4 d=128 bf16 K=32 needles", W.CPT, q, k, True)
+    for N in W.SWEEP_NS:
+        s = W.sweep(N)
+        q, k = W.iid(s, 3)
+        prefill_row(f"sweep B=1 N={N} 16/4 d=128 bf16 K=8", s, q, k, N <= 16384)
+        del q, k
+    # decode: GPU step on the full workload; the oracle on one sequence, times 64
+    s = W.DECODE
+    g = torch.Generator(device="cuda")
+    g.manual_seed(4)
+    kc = torch.randn(s.B, s.Hkv, s.N, s.d, device="cuda", generator=g, dtype=torch.bfloat16)
+    qd = torch.randn(W.DECODE_STEPS, s.B, s.Hq, s.d, device="cuda", generator=g, dtype=torch.bfloat16)
+    p = pisa.params_from_shape(s)
+    ds = pisa.Selector(p, mode="decode")
+    ds.build(kc, torch.full((s.B,), W.DECODE_CACHED, dtype=torch.int32, device="cuda"))
+    lens = [torch.full((s.B,), W.DECODE_CACHED + 1 + i, dtype=torch.int32, device="cuda")
+            for i in range(W.DECODE_STEPS)]
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for i in range(W.DECODE_STEPS):
+        ds.decode(qd[i], kc, lens[i], stream=st)
+    b.record(st)
+    torch.cuda.synchronize()
+    us = a.elapsed_time(b) / W.DECODE_STEPS * 1e3
+    del kc, ds
+    torch.cuda.empty_cache()
+    s1 = W.Shape(B=1, N=s.N, Hq=s.Hq, Hkv=s.Hkv, d=s.d, K=s.K)
+    q1, k1 = W.decode_inputs(s1, 4, steps=1)
+    o = oracle.Oracle.from_shape(s1)
+    kn = k1.double().numpy()
+    lens1 = [W.DECODE_CACHED + 1]
+    t0 = _t.perf_counter()
+    pyr = o.pyramid(kn, lens1)
+    t1 = _t.perf_counter()
+    o.select(q1[0].double().numpy(), kn, pyr, seq_lens=lens1, decode=True)
+    t2 = _t.perf_counter()
+    rows.append({"config": "decode B=64 x 131072 cached, 32/8 d=128 bf16 K=32", "pisa_us_per_step": us,
+                 "cpu_oracle_ms_per_step": (t2 - t1) * 64 * 1e3,
+                 "cpu_how": f"oracle select of one sequence (8 key heads) x 64; its fp64 pyramid rebuild "
+                            f"({(t1 - t0) * 1e3:.0f} ms per sequence) not included",
+                 "cpu_cores": oracle.num_threads()})
+    print(json.dumps(rows[-1]), flush=True)
+
+
 def main():
     args = parse()
     if args.profile_case:
         profile_case(args.profile_case)
+        return
+    if args.configs:
+        configs_table()
         return
     ws, rank, local = dist_setup(args)
     if args.impl == "reference":

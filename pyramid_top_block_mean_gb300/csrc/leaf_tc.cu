@@ -114,13 +114,14 @@ __global__ void scatter_kernel(BucketArgs a, const int32_t* __restrict__ kept2, 
   }
 }
 
-__global__ void tiles_kernel(int64_t nb, int32_t Q, const int32_t* __restrict__ counts,
+// Tile descriptor: {sequence x key head bh, first pair, pair count, level-2 node}.
+__global__ void tiles_kernel(int64_t nb, int64_t n2, int64_t nchunk, int32_t Q, const int32_t* __restrict__ counts,
                              const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_off,
                              int4* __restrict__ tile_info) {
   for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < nb; j += (int64_t)gridDim.x * blockDim.x) {
     const int32_t n = counts[j], t0 = tile_off[j], p0 = offsets[j];
-    for (int32_t i = 0; i * Q < n; ++i)
-      tile_info[t0 + i] = make_int4((int32_t)j, p0 + i * Q, min(Q, n - i * Q), 0);
+    const int32_t bh = (int32_t)((j / n2) / nchunk), node = (int32_t)(j % n2);
+    for (int32_t i = 0; i * Q < n; ++i) tile_info[t0 + i] = make_int4(bh, p0 + i * Q, min(Q, n - i * Q), node);
   }
 }
 
@@ -148,7 +149,7 @@ struct TileIter {
 
 template <int D, int G>
 __global__ void __launch_bounds__(kLeafTcThreads, 1)
-    leaf_tc_kernel(Prob pr, int64_t n2, int64_t nchunk, const __grid_constant__ CUtensorMap kmap,
+    leaf_tc_kernel(Prob pr, const __grid_constant__ CUtensorMap kmap,
                    const uint16_t* __restrict__ q, const int4* __restrict__ tile_info,
                    const int32_t* __restrict__ tile_total, const int32_t* __restrict__ pairs,
                    float* __restrict__ leaf_score, int32_t* __restrict__ status) {
@@ -198,35 +199,47 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
     constexpr int QPW = 32 / G;    // queries per producer warp
     const int ch = lane % CPR;
     const int row0 = warp * 32, qbase = row0 / G;
-    int it = 0, bcount = 0, last_bucket = -1;
+    int it = 0, bcount = 0, last_bh = -1, last_p = -1;
     int pend[kStagesA], npend = 0;  // stages whose copies are not yet signalled
     bool ok = true;
-    for (TileIter ti(T); ti.valid() && ok; ti.next()) {
-      const int4 info = tile_info[ti.i];
-      const int64_t bucket = info.x;
-      const int64_t p = bucket % n2;
-      const int64_t bh = (bucket / n2) / nchunk;
-      const int64_t b = bh / pr.Hkv, h = bh % pr.Hkv;
+    // Descriptors run two tiles ahead and query positions one tile ahead, so
+    // neither dependent load sits between a stage becoming free and its copies.
+    TileIter ti(T), ahead(T);
+    if (ahead.valid()) ahead.next();
+    const int4 kNone = make_int4(-1, 0, 0, 0);
+    int4 info = ti.valid() ? tile_info[ti.i] : kNone;
+    int4 info1 = ahead.valid() ? tile_info[ahead.i] : kNone;
+    int32_t tv = (ti.valid() && lane < QPW && qbase + lane < info.z) ? pairs[info.y + qbase + lane] : 0;
+    for (; ti.valid() && ok; ti.next()) {
+      if (ahead.valid()) ahead.next();
+      const int4 info2 = ahead.valid() ? tile_info[ahead.i] : kNone;
+      const int bh = info.x, p = info.w;  // consecutive tiles with the same (bh, p) share the key tile
+      const int b = bh / (int)pr.Hkv, h = bh - b * (int)pr.Hkv;
       const int sa = it % kStagesA, use = it / kStagesA;
       ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_a[sa]), (use & 1) ^ 1, abort, kWaitLimitNs);
       if (!ok) break;
-      if (info.x != last_bucket) {
+      if (bh != last_bh || p != last_p) {
         const int sb = bcount % kStagesB, ub = bcount / kStagesB;
+        const uint32_t eb = ptx::smem_u32(&sm.empty_b[sb]);
         int okb = 1;
         if (warp == 0 && npend > 0) {
           // The key stage is released only after the MMA finished tiles whose
-          // row signals may still be deferred here: send them before waiting.
-          ptx::cp_async_wait<0>();
-          ptx::fence_proxy_async_smem();
-          for (int u = 0; u < npend; ++u) ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[pend[u]]));
-          npend = 0;
+          // row signals may still be deferred here: if it is not free yet,
+          // send them before waiting.
+          const int freed = __shfl_sync(0xffffffffu, lane == 0 ? (int)ptx::mbar_try_wait(eb, (ub & 1) ^ 1) : 0, 0);
+          if (!freed) {
+            ptx::cp_async_wait<0>();
+            ptx::fence_proxy_async_smem();
+            for (int u = 0; u < npend; ++u) ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[pend[u]]));
+            npend = 0;
+          }
         }
         if (warp == 0 && lane == 0) {
-          okb = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_b[sb]), (ub & 1) ^ 1, abort, kWaitLimitNs);
+          okb = ptx::mbar_wait_bounded(eb, (ub & 1) ^ 1, abort, kWaitLimitNs);
           if (okb) {
             const uint32_t fb = ptx::smem_u32(&sm.full_b[sb]);
             ptx::mbar_arrive_expect_tx(fb, kBBytes);
-            const int32_t y = (int32_t)(bh * pr.N + 128 * p);
+            const int32_t y = (int32_t)(bh * pr.N + 128 * (int64_t)p);
 #pragma unroll
             for (int hh = 0; hh < D / 64; ++hh)
               ptx::tma_load_2d(ptx::smem_u32(sm.b[sb]) + hh * kHalf, &kmap, 64 * hh, y, fb);
@@ -235,26 +248,30 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
         ok = __shfl_sync(0xffffffffu, okb, 0) != 0;
         if (!ok) break;
         ++bcount;
-        last_bucket = info.x;
+        last_bh = bh;
+        last_p = p;
       }
-      // gather this warp's 32 query-head rows; the query positions come first
-      // (one load per query) so the copies issue back to back
+      // gather this warp's 32 query-head rows
       const uint32_t abase = ptx::smem_u32(sm.a[sa]);
       const int cnt = info.z;
-      const int32_t tv = (lane < QPW && qbase + lane < cnt) ? (pairs[info.y + qbase + lane] >> 5) : 0;
+      const int32_t tq = tv >> 5;
 #pragma unroll
       for (int r0 = 0; r0 < 32; r0 += RPI) {
         const int rl = r0 + lane / CPR;
         const int r = row0 + rl;
-        const int64_t t = __shfl_sync(0xffffffffu, tv, rl / G);
+        const int64_t t = __shfl_sync(0xffffffffu, tq, rl / G);
         if (qbase + rl / G < cnt) {
           const int g = r % G;
-          const uint16_t* src = q + (((b * pr.Hq + h * G + g) * pr.N + t) * D + ch * 8);
+          const uint16_t* src = q + ((((int64_t)b * pr.Hq + h * G + g) * pr.N + t) * D + ch * 8);
           const uint32_t dst = abase + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
           ptx::cp_async_16(dst, src);
         }
       }
       ptx::cp_async_commit();
+      // the next tile's query positions (its descriptor arrived a tile ago)
+      tv = (info1.x >= 0 && lane < QPW && qbase + lane < info1.z) ? pairs[info1.y + qbase + lane] : 0;
+      info = info1;
+      info1 = info2;
       pend[npend++] = sa;
       if (npend > kStagesA - 2) {  // keep two tiles of copies in flight
         ptx::cp_async_wait<kStagesA - 2>();
@@ -281,18 +298,23 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
-      int it = 0, bcount = 0, last_bucket = -1, sb = 0;
+      int it = 0, bcount = 0, last_bh = -1, last_p = -1, sb = 0;
       bool ok = true;
-      for (TileIter ti(T); ti.valid(); ti.next()) {
-        const int4 info = tile_info[ti.i];
+      int4 info = make_int4(-1, 0, 0, 0);
+      TileIter ti(T);
+      if (ti.valid()) info = tile_info[ti.i];
+      for (; ti.valid(); ti.next()) {
+        const int nx = ti.peek();
+        const int4 ninfo = nx >= 0 ? tile_info[nx] : make_int4(-1, 0, 0, 0);  // consumed after the MMAs
         const int sa = it % kStagesA, use = it / kStagesA;
         const int acc = it % kAcc, uacc = it / kAcc;
-        if (info.x != last_bucket) {
+        if (info.x != last_bh || info.w != last_p) {
           sb = bcount % kStagesB;
           ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[sb]), (bcount / kStagesB) & 1, abort, kWaitLimitNs);
           if (!ok) break;
           ++bcount;
-          last_bucket = info.x;
+          last_bh = info.x;
+          last_p = info.w;
         }
         ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_a[sa]), use & 1, abort, kWaitLimitNs) &&
              ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tempty[acc]), (uacc & 1) ^ 1, abort, kWaitLimitNs);
@@ -307,8 +329,8 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
         }
         ptx::mma_commit(ptx::smem_u32(&sm.empty_a[sa]));
         ptx::mma_commit(ptx::smem_u32(&sm.tfull[acc]));
-        const int nx = ti.peek();
-        if (nx < 0 || tile_info[nx].x != info.x) ptx::mma_commit(ptx::smem_u32(&sm.empty_b[sb]));
+        if (ninfo.x != info.x || ninfo.w != info.w) ptx::mma_commit(ptx::smem_u32(&sm.empty_b[sb]));
+        info = ninfo;
         ++it;
       }
       if (!ok) *abort = 1;
@@ -341,11 +363,12 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[acc]));
+      // raw dots; the scale (> 0) is applied inside the exponent's FMA
       float x[64];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        x[j] = __uint_as_float(v0[j]) * sc;
-        x[32 + j] = __uint_as_float(v1[j]) * sc;
+        x[j] = __uint_as_float(v0[j]);
+        x[32 + j] = __uint_as_float(v1[j]);
       }
       float mm[8];
 #pragma unroll
@@ -353,15 +376,15 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
 #pragma unroll
       for (int j = 8; j < 64; ++j) mm[j & 7] = fmaxf(mm[j & 7], x[j]);
       const float m = fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
-                            fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7])));
+                            fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7]))) * sc;
       float ss[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int j = 0; j < 64; ++j) ss[j & 3] += ptx::ex2(x[j] - m);
+      for (int j = 0; j < 64; ++j) ss[j & 3] += ptx::ex2(fmaf(x[j], sc, -m));
       float lse = m + ptx::lg2((ss[0] + ss[1]) + (ss[2] + ss[3]));
 #pragma unroll
       for (int o = 1; o < G; o <<= 1) lse += __shfl_xor_sync(0xffffffffu, lse, o);
       if ((r % G) == 0 && qr < info.z) {
-        const int64_t bh = (info.x / n2) / nchunk;
+        const int64_t bh = info.x;
         const int64_t t = pe >> 5, slot = pe & 31;
         leaf_score[((bh * pr.N + t) * pr.K + slot) * 2 + leaf] = lse;
       }
@@ -520,7 +543,7 @@ static cudaError_t launch_leaf_tc_t(const Prob& pr, const PrefillWs& w, char* ws
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   note_launch();
-  kern<<<grid, kLeafTcThreads, smem, st>>>(pr, w.n2, w.nchunk, kmap, (const uint16_t*)q,
+  kern<<<grid, kLeafTcThreads, smem, st>>>(pr, kmap, (const uint16_t*)q,
                                            (const int4*)(ws + w.tile_info),
                                            (const int32_t*)(ws + w.tile_off) + w.nbuckets,
                                            (const int32_t*)(ws + w.pairs), (float*)(ws + w.leaf_score),
@@ -553,7 +576,7 @@ cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, cha
     scatter_kernel<<<g1, 256, 0, st>>>(a, kept2, offsets, cursor, (int32_t*)(ws + w.pairs));
     const unsigned g2 = (unsigned)std::min<int64_t>(ceil_div64(w.nbuckets, 256), (int64_t)num_sms * 8);
     note_launch();
-    tiles_kernel<<<g2, 256, 0, st>>>(w.nbuckets, Q, counts, offsets, tile_off, (int4*)(ws + w.tile_info));
+    tiles_kernel<<<g2, 256, 0, st>>>(w.nbuckets, w.n2, w.nchunk, Q, counts, offsets, tile_off, (int4*)(ws + w.tile_info));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     CUtensorMap kmap;

@@ -282,8 +282,10 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob 
         if (s1 >= 0) {
           yb[sl] = sm.y[s1];
         } else if (s1 == -2) {
-          const int n0 = count_node(s.C, level - 1, c0v[sl], s.N);
-          const int n1 = count_node(s.C, level - 1, c0v[sl] + 1, s.N);
+          // only the last node of a level can hold fewer keys than the others
+          const bool full = c0v[sl] + 2 < ncap;
+          const int n0 = full ? 1 : count_node(s.C, level - 1, c0v[sl], s.N);
+          const int n1 = full ? 1 : count_node(s.C, level - 1, c0v[sl] + 1, s.N);
           const float4 xv = sm.x[cur][i];
           yb[sl] = make_float4(sib_dot(xv.x, ya[sl].x, n0, n1), sib_dot(xv.y, ya[sl].y, n0, n1),
                                sib_dot(xv.z, ya[sl].z, n0, n1), sib_dot(xv.w, ya[sl].w, n0, n1));
