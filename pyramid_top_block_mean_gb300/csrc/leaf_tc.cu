@@ -10,16 +10,19 @@
 // are counting-sorted by (sequence, key head, query chunk, p).  One tile is
 // 128 rows = 128/G queries x G heads of one bucket against the 128 keys of
 // leaves 2p and 2p+1:
-//   - TMA brings the 128 x d bf16 key tile into shared memory (128-byte
-//     swizzle) once per bucket and it stays there for all of that bucket's
-//     consecutive tiles;
-//   - the producer warp gathers the 128 query-head rows with cp.async into
-//     the same swizzled K-major layout;
+//   - a loader warp brings the 128 x d bf16 key tile into shared memory by
+//     TMA (128-byte swizzle) once per run of consecutive tiles with the same
+//     key tile, up to three key tiles ahead;
+//   - eight producer warps gather the 128 query-head rows (16 each) with
+//     cp.async into the same swizzled K-major layout (TMA four-row gathers
+//     measured 2.3x slower for these 256-byte rows: one TMA operation per
+//     512 bytes);
 //   - one thread issues tcgen05.mma (M = 128, N = 128, K = d) into a TMEM
-//     accumulator (two accumulators alternate);
-//   - four epilogue warps read their 32 TMEM lanes each, take the per-row
-//     log2-sum-exp2 over each leaf's 64 columns, sum the G head rows of a
-//     query, and write two scores per pair.  No score matrix reaches HBM.
+//     accumulator (four accumulators rotate);
+//   - eight epilogue warps (two per TMEM lane quadrant, one per leaf) read
+//     their 32 lanes x 64 columns, take the per-row log2-sum-exp2 over the
+//     leaf's keys, sum the G head rows of a query, and write one score per
+//     (query, leaf).  No score matrix reaches HBM.
 // Persistent CTAs (one per SM) walk the tile list in interleaved groups of
 // four consecutive tiles, so all SMs sweep the same query chunk together.
 #include <cudaTypedefs.h>
@@ -36,13 +39,15 @@ namespace pisa {
 constexpr int kTileRows = 128;  // MMA M: queries x heads
 constexpr int kTileKeys = 128;  // MMA N: leaves 2p and 2p+1
 constexpr int kStagesA = 4;  // query-row tiles in flight
-constexpr int kStagesB = 2;  // key tiles
+constexpr int kStagesB = 3;  // key tiles
 constexpr int kAcc = 4;      // TMEM accumulators (4 x 128 columns)
 constexpr int kGroup = 4;
-constexpr int kProdWarps = 4;        // warps 0-3 gather 32 rows each
-constexpr int kMmaWarp = 4;          // issues the MMAs, owns TMEM
-constexpr int kEpiWarps = 8;         // warps 5-12: (TMEM lane quadrant, leaf)
-constexpr int kLeafTcThreads = 32 * (kProdWarps + 1 + kEpiWarps);
+constexpr int kProdWarps = 8;          // warps 0-7 gather 16 query-head rows each
+constexpr int kProdRows = kTileRows / kProdWarps;
+constexpr int kLoadWarp = kProdWarps;  // loads the key tiles (TMA)
+constexpr int kMmaWarp = kLoadWarp + 1;  // issues the MMAs, owns TMEM
+constexpr int kEpiWarps = 8;             // the next 8 warps: (TMEM lane quadrant, leaf)
+constexpr int kLeafTcThreads = 32 * (kMmaWarp + 1 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 
@@ -193,14 +198,13 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
 
   if (warp < kProdWarps) {
     // ------------------------------------------------------------ producers
-    // warp w gathers rows [32w, 32w + 32); warp 0 also loads the key tiles
+    // warp w gathers rows [16w, 16w + 16) of every tile with cp.async
     constexpr int CPR = D / 8;     // 16-byte chunks per row
     constexpr int RPI = 32 / CPR;  // rows per warp instruction
-    constexpr int QPW = 32 / G;    // queries per producer warp
+    constexpr int QPW = kProdRows / G;  // queries per producer warp
     const int ch = lane % CPR;
-    const int row0 = warp * 32, qbase = row0 / G;
-    int it = 0, bcount = 0, last_bh = -1, last_p = -1;
-    int pend[kStagesA], npend = 0;  // stages whose copies are not yet signalled
+    const int row0 = warp * kProdRows, qbase = row0 / G;
+    int it = 0;
     bool ok = true;
     // Descriptors run two tiles ahead and query positions one tile ahead, so
     // neither dependent load sits between a stage becoming free and its copies.
@@ -213,50 +217,17 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
     for (; ti.valid() && ok; ti.next()) {
       if (ahead.valid()) ahead.next();
       const int4 info2 = ahead.valid() ? tile_info[ahead.i] : kNone;
-      const int bh = info.x, p = info.w;  // consecutive tiles with the same (bh, p) share the key tile
+      const int bh = info.x;
       const int b = bh / (int)pr.Hkv, h = bh - b * (int)pr.Hkv;
       const int sa = it % kStagesA, use = it / kStagesA;
       ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_a[sa]), (use & 1) ^ 1, abort, kWaitLimitNs);
-      if (!ok) break;
-      if (bh != last_bh || p != last_p) {
-        const int sb = bcount % kStagesB, ub = bcount / kStagesB;
-        const uint32_t eb = ptx::smem_u32(&sm.empty_b[sb]);
-        int okb = 1;
-        if (warp == 0 && npend > 0) {
-          // The key stage is released only after the MMA finished tiles whose
-          // row signals may still be deferred here: if it is not free yet,
-          // send them before waiting.
-          const int freed = __shfl_sync(0xffffffffu, lane == 0 ? (int)ptx::mbar_try_wait(eb, (ub & 1) ^ 1) : 0, 0);
-          if (!freed) {
-            ptx::cp_async_wait<0>();
-            ptx::fence_proxy_async_smem();
-            for (int u = 0; u < npend; ++u) ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[pend[u]]));
-            npend = 0;
-          }
-        }
-        if (warp == 0 && lane == 0) {
-          okb = ptx::mbar_wait_bounded(eb, (ub & 1) ^ 1, abort, kWaitLimitNs);
-          if (okb) {
-            const uint32_t fb = ptx::smem_u32(&sm.full_b[sb]);
-            ptx::mbar_arrive_expect_tx(fb, kBBytes);
-            const int32_t y = (int32_t)(bh * pr.N + 128 * (int64_t)p);
-#pragma unroll
-            for (int hh = 0; hh < D / 64; ++hh)
-              ptx::tma_load_2d(ptx::smem_u32(sm.b[sb]) + hh * kHalf, &kmap, 64 * hh, y, fb);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, okb, 0) != 0;
-        if (!ok) break;
-        ++bcount;
-        last_bh = bh;
-        last_p = p;
-      }
-      // gather this warp's 32 query-head rows
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      // gather this warp's query-head rows
       const uint32_t abase = ptx::smem_u32(sm.a[sa]);
       const int cnt = info.z;
       const int32_t tq = tv >> 5;
 #pragma unroll
-      for (int r0 = 0; r0 < 32; r0 += RPI) {
+      for (int r0 = 0; r0 < kProdRows; r0 += RPI) {
         const int rl = r0 + lane / CPR;
         const int r = row0 + rl;
         const int64_t t = __shfl_sync(0xffffffffu, tq, rl / G);
@@ -267,45 +238,72 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
           ptx::cp_async_16(dst, src);
         }
       }
-      ptx::cp_async_commit();
+      // the stage's barrier counts this thread once its copies have landed
+      ptx::cp_async_arrive_noinc(ptx::smem_u32(&sm.full_a[sa]));
       // the next tile's query positions (its descriptor arrived a tile ago)
       tv = (info1.x >= 0 && lane < QPW && qbase + lane < info1.z) ? pairs[info1.y + qbase + lane] : 0;
       info = info1;
       info1 = info2;
-      pend[npend++] = sa;
-      if (npend > kStagesA - 2) {  // keep two tiles of copies in flight
-        ptx::cp_async_wait<kStagesA - 2>();
-        ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[pend[0]]));
-#pragma unroll
-        for (int u = 0; u < kStagesA - 1; ++u) pend[u] = pend[u + 1];
-        --npend;
-      }
       ++it;
     }
-    ptx::cp_async_wait<0>();
-    ptx::fence_proxy_async_smem();
-    if (ok)
-      for (int u = 0; u < npend; ++u) ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[pend[u]]));
-    if (!ok) {
-      *abort = 1;
-      // let TMA loads already issued land before the CTA can exit
-      if (warp == 0 && lane == 0)
+    ptx::cp_async_wait_all();  // no copy may still target this CTA's memory when it exits
+    if (!ok) *abort = 1;
+  } else if (warp == kLoadWarp) {
+    // ------------------------------------------------------- key-tile loads
+    // one TMA load of the 128 x d keys of leaves 2p, 2p+1 per run of tiles
+    // with the same (bh, p); it runs up to kStagesB key tiles ahead
+    if (lane == 0) {
+      int bcount = 0, last_bh = -1, last_p = -1;
+      bool ok = true;
+      const int4 kNone = make_int4(-1, 0, 0, 0);
+      TileIter ti(T), ahead(T);
+      if (ahead.valid()) ahead.next();
+      int4 info = ti.valid() ? tile_info[ti.i] : kNone;
+      int4 info1 = ahead.valid() ? tile_info[ahead.i] : kNone;
+      for (; ti.valid(); ti.next()) {
+        if (ahead.valid()) ahead.next();
+        const int4 info2 = ahead.valid() ? tile_info[ahead.i] : kNone;
+        const int bh = info.x, p = info.w;
+        if (bh != last_bh || p != last_p) {
+          const int sb = bcount % kStagesB, ub = bcount / kStagesB;
+          ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_b[sb]), (ub & 1) ^ 1, abort, kWaitLimitNs);
+          if (!ok) break;
+          const uint32_t fb = ptx::smem_u32(&sm.full_b[sb]);
+          ptx::mbar_arrive_expect_tx(fb, kBBytes);
+          const int32_t y = (int32_t)(bh * pr.N + 128 * (int64_t)p);
+#pragma unroll
+          for (int hh = 0; hh < D / 64; ++hh)
+            ptx::tma_load_2d(ptx::smem_u32(sm.b[sb]) + hh * kHalf, &kmap, 64 * hh, y, fb);
+          ++bcount;
+          last_bh = bh;
+          last_p = p;
+        }
+        info = info1;
+        info1 = info2;
+      }
+      if (!ok) {
+        *abort = 1;
+        // let TMA loads already issued land before the CTA can exit
         for (int k = bcount > kStagesB ? bcount - kStagesB : 0; k < bcount; ++k)
           ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k % kStagesB]), (k / kStagesB) & 1, &sm.zero,
                                  kWaitLimitNs);
+      }
     }
+    __syncwarp();
   } else if (warp == kMmaWarp) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
       int it = 0, bcount = 0, last_bh = -1, last_p = -1, sb = 0;
       bool ok = true;
-      int4 info = make_int4(-1, 0, 0, 0);
-      TileIter ti(T);
-      if (ti.valid()) info = tile_info[ti.i];
+      // descriptors two tiles ahead: the one compared after the MMAs was loaded a tile ago
+      const int4 kNone = make_int4(-1, 0, 0, 0);
+      TileIter ti(T), ahead(T);
+      if (ahead.valid()) ahead.next();
+      int4 info = ti.valid() ? tile_info[ti.i] : kNone;
+      int4 ninfo = ahead.valid() ? tile_info[ahead.i] : kNone;
       for (; ti.valid(); ti.next()) {
-        const int nx = ti.peek();
-        const int4 ninfo = nx >= 0 ? tile_info[nx] : make_int4(-1, 0, 0, 0);  // consumed after the MMAs
+        if (ahead.valid()) ahead.next();
+        const int4 info2 = ahead.valid() ? tile_info[ahead.i] : kNone;
         const int sa = it % kStagesA, use = it / kStagesA;
         const int acc = it % kAcc, uacc = it / kAcc;
         if (info.x != last_bh || info.w != last_p) {
@@ -319,6 +317,9 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
         ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_a[sa]), use & 1, abort, kWaitLimitNs) &&
              ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tempty[acc]), (uacc & 1) ^ 1, abort, kWaitLimitNs);
         if (!ok) break;
+        // the rows arrived through cp.async (generic proxy); the MMA reads
+        // them through the async proxy
+        ptx::fence_proxy_async_smem();
         ptx::tc_fence_after();
         const uint32_t d = tmem + acc * kTileKeys;
         const uint32_t a0 = ptx::smem_u32(sm.a[sa]), b0 = ptx::smem_u32(sm.b[sb]);
@@ -331,6 +332,7 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
         ptx::mma_commit(ptx::smem_u32(&sm.tfull[acc]));
         if (ninfo.x != info.x || ninfo.w != info.w) ptx::mma_commit(ptx::smem_u32(&sm.empty_b[sb]));
         info = ninfo;
+        ninfo = info2;
         ++it;
       }
       if (!ok) *abort = 1;
@@ -347,11 +349,15 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
     const int r = q4 * 32 + lane;
     const float sc = pr.scale2;
     int it = 0;
-    for (TileIter ti(T); ti.valid(); ti.next()) {
-      const int4 info = tile_info[ti.i];
+    // this tile's descriptor and pair come from the previous iteration
+    const int qr = r / G;
+    TileIter ti(T);
+    int4 info = ti.valid() ? tile_info[ti.i] : make_int4(-1, 0, 0, 0);
+    int32_t pe = (ti.valid() && qr < info.z) ? pairs[info.y + qr] : 0;
+    for (; ti.valid(); ti.next()) {
+      const int nx = ti.peek();
+      const int4 ninfo = nx >= 0 ? tile_info[nx] : make_int4(-1, 0, 0, 0);
       const int acc = it % kAcc, use = it / kAcc;
-      const int qr = r / G;
-      const int32_t pe = qr < info.z ? pairs[info.y + qr] : 0;  // issued before the wait
       const bool okw = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tfull[acc]), use & 1, abort, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, okw)) { *abort = 1; break; }
       ptx::tc_fence_after();
@@ -363,6 +369,7 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[acc]));
+      const int32_t npe = (ninfo.x >= 0 && qr < ninfo.z) ? pairs[ninfo.y + qr] : 0;
       // raw dots; the scale (> 0) is applied inside the exponent's FMA
       float x[64];
 #pragma unroll
@@ -388,6 +395,8 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
         const int64_t t = pe >> 5, slot = pe & 31;
         leaf_score[((bh * pr.N + t) * pr.K + slot) * 2 + leaf] = lse;
       }
+      info = ninfo;
+      pe = npe;
       ++it;
     }
   }
