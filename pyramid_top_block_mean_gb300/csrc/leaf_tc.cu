@@ -202,26 +202,28 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
     constexpr int CPR = D / 8;     // 16-byte chunks per row
     constexpr int RPI = 32 / CPR;  // rows per warp instruction
     constexpr int QPW = kProdRows / G;  // queries per producer warp
+    const int4 kNoTile = make_int4(-1, 0, 0, 0);
     const int ch = lane % CPR;
     const int row0 = warp * kProdRows, qbase = row0 / G;
     int it = 0;
     bool ok = true;
-    // Descriptors run two tiles ahead and query positions one tile ahead, so
-    // neither dependent load sits between a stage becoming free and its copies.
+    // Descriptors run two tiles ahead and query positions one tile ahead.
+    // The loop is unrolled three times over rotating slots, so a prefetched
+    // value is never copied between registers (which would wait for it).
     TileIter ti(T), ahead(T);
     if (ahead.valid()) ahead.next();
-    const int4 kNone = make_int4(-1, 0, 0, 0);
-    int4 info = ti.valid() ? tile_info[ti.i] : kNone;
-    int4 info1 = ahead.valid() ? tile_info[ahead.i] : kNone;
-    int32_t tv = (ti.valid() && lane < QPW && qbase + lane < info.z) ? pairs[info.y + qbase + lane] : 0;
-    for (; ti.valid() && ok; ti.next()) {
+    int4 d0 = ti.valid() ? tile_info[ti.i] : kNoTile;
+    int4 d1 = ahead.valid() ? tile_info[ahead.i] : kNoTile, d2;
+    int32_t v0 = (ti.valid() && lane < QPW && qbase + lane < d0.z) ? pairs[d0.y + qbase + lane] : 0, v1, v2;
+    auto step = [&](const int4& info, const int4& info1, int4& slot2, const int32_t& tv, int32_t& slot1) -> bool {
+      if (!ti.valid()) return false;
       if (ahead.valid()) ahead.next();
-      const int4 info2 = ahead.valid() ? tile_info[ahead.i] : kNone;
+      slot2 = ahead.valid() ? tile_info[ahead.i] : kNoTile;  // tile it + 2
       const int bh = info.x;
       const int b = bh / (int)pr.Hkv, h = bh - b * (int)pr.Hkv;
       const int sa = it % kStagesA, use = it / kStagesA;
       ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_a[sa]), (use & 1) ^ 1, abort, kWaitLimitNs);
-      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; return false; }
       // gather this warp's query-head rows
       const uint32_t abase = ptx::smem_u32(sm.a[sa]);
       const int cnt = info.z;
@@ -240,11 +242,13 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
       }
       // the stage's barrier counts this thread once its copies have landed
       ptx::cp_async_arrive_noinc(ptx::smem_u32(&sm.full_a[sa]));
-      // the next tile's query positions (its descriptor arrived a tile ago)
-      tv = (info1.x >= 0 && lane < QPW && qbase + lane < info1.z) ? pairs[info1.y + qbase + lane] : 0;
-      info = info1;
-      info1 = info2;
+      // query positions of tile it + 1 (its descriptor arrived a tile ago)
+      slot1 = (info1.x >= 0 && lane < QPW && qbase + lane < info1.z) ? pairs[info1.y + qbase + lane] : 0;
       ++it;
+      ti.next();
+      return true;
+    };
+    while (step(d0, d1, d2, v0, v1) && step(d1, d2, d0, v1, v2) && step(d2, d0, d1, v2, v0)) {
     }
     ptx::cp_async_wait_all();  // no copy may still target this CTA's memory when it exits
     if (!ok) *abort = 1;
@@ -295,28 +299,29 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
     if (lane == 0) {
       int it = 0, bcount = 0, last_bh = -1, last_p = -1, sb = 0;
       bool ok = true;
-      // descriptors two tiles ahead: the one compared after the MMAs was loaded a tile ago
-      const int4 kNone = make_int4(-1, 0, 0, 0);
+      // descriptors two tiles ahead (three rotating slots, as in the producers)
+      const int4 kNoTile = make_int4(-1, 0, 0, 0);
       TileIter ti(T), ahead(T);
       if (ahead.valid()) ahead.next();
-      int4 info = ti.valid() ? tile_info[ti.i] : kNone;
-      int4 ninfo = ahead.valid() ? tile_info[ahead.i] : kNone;
-      for (; ti.valid(); ti.next()) {
+      int4 d0 = ti.valid() ? tile_info[ti.i] : kNoTile;
+      int4 d1 = ahead.valid() ? tile_info[ahead.i] : kNoTile, d2;
+      auto step = [&](const int4& info, const int4& ninfo, int4& slot2) -> bool {
+        if (!ti.valid()) return false;
         if (ahead.valid()) ahead.next();
-        const int4 info2 = ahead.valid() ? tile_info[ahead.i] : kNone;
+        slot2 = ahead.valid() ? tile_info[ahead.i] : kNoTile;
         const int sa = it % kStagesA, use = it / kStagesA;
         const int acc = it % kAcc, uacc = it / kAcc;
         if (info.x != last_bh || info.w != last_p) {
           sb = bcount % kStagesB;
           ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[sb]), (bcount / kStagesB) & 1, abort, kWaitLimitNs);
-          if (!ok) break;
+          if (!ok) return false;
           ++bcount;
           last_bh = info.x;
           last_p = info.w;
         }
         ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_a[sa]), use & 1, abort, kWaitLimitNs) &&
              ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tempty[acc]), (uacc & 1) ^ 1, abort, kWaitLimitNs);
-        if (!ok) break;
+        if (!ok) return false;
         // the rows arrived through cp.async (generic proxy); the MMA reads
         // them through the async proxy
         ptx::fence_proxy_async_smem();
@@ -331,9 +336,11 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
         ptx::mma_commit(ptx::smem_u32(&sm.empty_a[sa]));
         ptx::mma_commit(ptx::smem_u32(&sm.tfull[acc]));
         if (ninfo.x != info.x || ninfo.w != info.w) ptx::mma_commit(ptx::smem_u32(&sm.empty_b[sb]));
-        info = ninfo;
-        ninfo = info2;
         ++it;
+        ti.next();
+        return true;
+      };
+      while (step(d0, d1, d2) && step(d1, d2, d0) && step(d2, d0, d1)) {
       }
       if (!ok) *abort = 1;
       // every MMA has finished before TMEM is released
