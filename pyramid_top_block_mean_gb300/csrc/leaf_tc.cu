@@ -81,6 +81,63 @@ __global__ void count_kernel(BucketArgs a, const int32_t* __restrict__ kept2, in
   }
 }
 
+// Shared-memory histogram versions for n2 <= kSmemBins level-2 nodes: one CTA
+// per kQueriesPerCta query positions of one (sequence, key head); the range
+// never crosses a query chunk, so a bucket is (CTA's chunk, node p).
+constexpr int kQueriesPerCta = 2048;
+constexpr int kSmemBins = 16384;
+static_assert(((1 << kChunkShift) % kQueriesPerCta) == 0, "a CTA's queries stay in one chunk");
+
+__global__ void __launch_bounds__(512) count_smem_kernel(BucketArgs a, const int32_t* __restrict__ kept2,
+                                                        int32_t* __restrict__ counts) {
+  extern __shared__ int32_t hist[];
+  const int n2 = (int)a.n2, K = a.K;
+  const int64_t bh = blockIdx.y, t0 = (int64_t)blockIdx.x * kQueriesPerCta;
+  const int ne = (int)(a.N - t0 < kQueriesPerCta ? a.N - t0 : kQueriesPerCta) * K;
+  for (int i = threadIdx.x; i < n2; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int32_t* src = kept2 + (bh * a.N + t0) * K;
+  for (int e = threadIdx.x; e < ne; e += blockDim.x) {
+    const int32_t p = src[e];
+    if (p >= 0) atomicAdd(&hist[p], 1);
+  }
+  __syncthreads();
+  int32_t* dst = counts + (bh * a.nchunk + (t0 >> kChunkShift)) * a.n2;
+  for (int i = threadIdx.x; i < n2; i += blockDim.x)
+    if (hist[i]) atomicAdd(&dst[i], hist[i]);
+}
+
+__global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const int32_t* __restrict__ kept2,
+                                                          const int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ cursor, int32_t* __restrict__ pairs) {
+  extern __shared__ int32_t hist[];
+  const int n2 = (int)a.n2, K = a.K;
+  const int64_t bh = blockIdx.y, t0 = (int64_t)blockIdx.x * kQueriesPerCta;
+  const int ne = (int)(a.N - t0 < kQueriesPerCta ? a.N - t0 : kQueriesPerCta) * K;
+  for (int i = threadIdx.x; i < n2; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int32_t* src = kept2 + (bh * a.N + t0) * K;
+  for (int e = threadIdx.x; e < ne; e += blockDim.x) {
+    const int32_t p = src[e];
+    if (p >= 0) atomicAdd(&hist[p], 1);
+  }
+  __syncthreads();
+  // reserve this CTA's range in every bucket it touches
+  const int64_t b0 = (bh * a.nchunk + (t0 >> kChunkShift)) * a.n2;
+  for (int i = threadIdx.x; i < n2; i += blockDim.x) {
+    const int32_t c = hist[i];
+    if (c) hist[i] = offsets[b0 + i] + atomicAdd(&cursor[b0 + i], c);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < ne; e += blockDim.x) {
+    const int32_t p = src[e];
+    if (p >= 0) {
+      const int qn = e / K;
+      pairs[atomicAdd(&hist[p], 1)] = (int32_t)(((t0 + qn) << 5) | (e - qn * K));
+    }
+  }
+}
+
 // Exclusive scans of the pair counts and of the tiles per bucket (one CTA).
 __global__ void __launch_bounds__(1024) scan_kernel(int64_t nb, int32_t Q, const int32_t* __restrict__ counts,
                                                     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_off) {
@@ -89,7 +146,12 @@ __global__ void __launch_bounds__(1024) scan_kernel(int64_t nb, int32_t Q, const
   const int64_t per = ceil_div64(nb, 1024);
   const int64_t lo = tid * per, hi = lo + per < nb ? lo + per : nb;
   int32_t ps = 0, ts = 0;
-  for (int64_t i = lo; i < hi; ++i) { ps += counts[i]; ts += (counts[i] + Q - 1) / Q; }
+#pragma unroll 8
+  for (int64_t i = lo; i < hi; ++i) {
+    const int32_t c = counts[i];
+    ps += c;
+    ts += (c + Q - 1) / Q;
+  }
   sp[tid] = ps; st[tid] = ts;
   __syncthreads();
   for (int o = 1; o < 1024; o <<= 1) {
@@ -99,9 +161,11 @@ __global__ void __launch_bounds__(1024) scan_kernel(int64_t nb, int32_t Q, const
     __syncthreads();
   }
   int32_t pb = sp[tid] - ps, tb = st[tid] - ts;
+#pragma unroll 8
   for (int64_t i = lo; i < hi; ++i) {
+    const int32_t c = counts[i];
     offsets[i] = pb; tile_off[i] = tb;
-    pb += counts[i]; tb += (counts[i] + Q - 1) / Q;
+    pb += c; tb += (c + Q - 1) / Q;
   }
   if (tid == 1023) { offsets[nb] = sp[1023]; tile_off[nb] = st[1023]; }
 }
@@ -584,12 +648,24 @@ cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, cha
     if (e != cudaSuccess) return e;
     const int64_t n = nq * pr.K;
     const unsigned g1 = (unsigned)std::min<int64_t>(ceil_div64(n, 256), (int64_t)num_sms * 16);
+    const bool smem_bins = w.n2 <= kSmemBins;
+    const dim3 gs((unsigned)ceil_div64(pr.N, kQueriesPerCta), (unsigned)(pr.B * pr.Hkv));
+    const size_t hbytes = (size_t)w.n2 * sizeof(int32_t);
+    if (smem_bins) {
+      e = cudaFuncSetAttribute(count_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kSmemBins * 4));
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(scatter_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)(kSmemBins * 4));
+      if (e != cudaSuccess) return e;
+    }
     note_launch();
-    count_kernel<<<g1, 256, 0, st>>>(a, kept2, counts);
+    if (smem_bins) count_smem_kernel<<<gs, 512, hbytes, st>>>(a, kept2, counts);
+    else count_kernel<<<g1, 256, 0, st>>>(a, kept2, counts);
     note_launch();
     scan_kernel<<<1, 1024, 0, st>>>(w.nbuckets, Q, counts, offsets, tile_off);
     note_launch();
-    scatter_kernel<<<g1, 256, 0, st>>>(a, kept2, offsets, cursor, (int32_t*)(ws + w.pairs));
+    if (smem_bins) scatter_smem_kernel<<<gs, 512, hbytes, st>>>(a, kept2, offsets, cursor, (int32_t*)(ws + w.pairs));
+    else scatter_kernel<<<g1, 256, 0, st>>>(a, kept2, offsets, cursor, (int32_t*)(ws + w.pairs));
     const unsigned g2 = (unsigned)std::min<int64_t>(ceil_div64(w.nbuckets, 256), (int64_t)num_sms * 8);
     note_launch();
     tiles_kernel<<<g2, 256, 0, st>>>(w.nbuckets, w.n2, w.nchunk, Q, counts, offsets, tile_off, (int4*)(ws + w.tile_info));
