@@ -138,36 +138,71 @@ __global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const i
   }
 }
 
-// Exclusive scans of the pair counts and of the tiles per bucket (one CTA).
+// Exclusive scans of the pair counts and of the tiles per bucket (one CTA),
+// in rounds of 4096 buckets: coalesced loads into shared memory, four
+// consecutive buckets per thread, warp-shuffle scans of the thread sums, and
+// a running carry between rounds.  Q (rows per tile / G) is a power of two.
 __global__ void __launch_bounds__(1024) scan_kernel(int64_t nb, int32_t Q, const int32_t* __restrict__ counts,
                                                     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_off) {
-  __shared__ int32_t sp[1024], st[1024];
-  const int tid = threadIdx.x;
-  const int64_t per = ceil_div64(nb, 1024);
-  const int64_t lo = tid * per, hi = lo + per < nb ? lo + per : nb;
-  int32_t ps = 0, ts = 0;
-#pragma unroll 8
-  for (int64_t i = lo; i < hi; ++i) {
-    const int32_t c = counts[i];
-    ps += c;
-    ts += (c + Q - 1) / Q;
-  }
-  sp[tid] = ps; st[tid] = ts;
-  __syncthreads();
-  for (int o = 1; o < 1024; o <<= 1) {
-    const int32_t a = tid >= o ? sp[tid - o] : 0, b = tid >= o ? st[tid - o] : 0;
+  constexpr int kRound = 4096;
+  __shared__ int32_t cs[kRound], ts[kRound];
+  __shared__ int32_t wp[32], wt[32];
+  __shared__ int32_t carry[2];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int qs = __ffs(Q) - 1;
+  if (tid == 0) { carry[0] = 0; carry[1] = 0; }
+  for (int64_t base = 0; base < nb; base += kRound) {
+#pragma unroll
+    for (int j = 0; j < kRound / 1024; ++j) {
+      const int64_t i = base + j * 1024 + tid;
+      const int32_t c = i < nb ? counts[i] : 0;
+      cs[j * 1024 + tid] = c;
+      ts[j * 1024 + tid] = (c + Q - 1) >> qs;
+    }
     __syncthreads();
-    sp[tid] += a; st[tid] += b;
+    int32_t pc[4], pt[4], sp = 0, st = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      pc[j] = sp; pt[j] = st;
+      sp += cs[4 * tid + j];
+      st += ts[4 * tid + j];
+    }
+    // inclusive warp scans of the thread sums
+    int32_t ip = sp, it = st;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t a = __shfl_up_sync(0xffffffffu, ip, o), b = __shfl_up_sync(0xffffffffu, it, o);
+      if (lane >= o) { ip += a; it += b; }
+    }
+    if (lane == 31) { wp[wid] = ip; wt[wid] = it; }
+    __syncthreads();
+    if (wid == 0) {
+      int32_t x = wp[lane], y = wt[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t a = __shfl_up_sync(0xffffffffu, x, o), b = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) { x += a; y += b; }
+      }
+      wp[lane] = x - wp[lane];  // exclusive warp offsets
+      wt[lane] = y - wt[lane];
+    }
+    __syncthreads();
+    const int32_t op = carry[0] + wp[wid] + (ip - sp), ot = carry[1] + wt[wid] + (it - st);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      cs[4 * tid + j] = op + pc[j];
+      ts[4 * tid + j] = ot + pt[j];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kRound / 1024; ++j) {
+      const int64_t i = base + j * 1024 + tid;
+      if (i < nb) { offsets[i] = cs[j * 1024 + tid]; tile_off[i] = ts[j * 1024 + tid]; }
+    }
+    if (tid == 1023) { carry[0] = op + sp; carry[1] = ot + st; }
     __syncthreads();
   }
-  int32_t pb = sp[tid] - ps, tb = st[tid] - ts;
-#pragma unroll 8
-  for (int64_t i = lo; i < hi; ++i) {
-    const int32_t c = counts[i];
-    offsets[i] = pb; tile_off[i] = tb;
-    pb += c; tb += (c + Q - 1) / Q;
-  }
-  if (tid == 1023) { offsets[nb] = sp[1023]; tile_off[nb] = st[1023]; }
+  if (tid == 0) { offsets[nb] = carry[0]; tile_off[nb] = carry[1]; }
 }
 
 __global__ void scatter_kernel(BucketArgs a, const int32_t* __restrict__ kept2, const int32_t* __restrict__ offsets,
