@@ -584,41 +584,59 @@ __global__ void __launch_bounds__(256) finalize_small_kernel(Prob pr, const int3
                                                              const float* __restrict__ leaf_score,
                                                              int32_t* __restrict__ out_idx,
                                                              float* __restrict__ out_score) {
-  constexpr int KM = 8, NCM = 2 * KM;
-  const int64_t qi = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (qi >= pr.B * pr.Hkv * pr.N) return;
-  const int64_t qb = (qi % pr.N) / pr.C;
+  constexpr int KM = 8, NCM = 2 * KM, WM = KM + 3;
+  // each thread builds its row in shared memory; the block then writes its
+  // rows out contiguously
+  __shared__ int32_t si[256 * WM];
+  __shared__ float ss[256 * WM];
+  const int64_t nq = pr.B * pr.Hkv * pr.N;
+  const int64_t q0 = (int64_t)blockIdx.x * blockDim.x;
+  const int64_t qi = q0 + threadIdx.x;
   const int K = pr.K, W = K + 3;
-  float sc[NCM];
-  int32_t lf[NCM];
-  bool val[NCM];
+  if (qi < nq) {
+    // pair counts are below 2^31, so query indices fit 32 bits
+    const uint32_t t = (uint32_t)qi % (uint32_t)pr.N;
+    const int32_t qb = (int32_t)(t / (uint32_t)pr.C);
+    float sc[NCM];
+    int32_t lf[NCM];
+    bool val[NCM];
 #pragma unroll
-  for (int c = 0; c < NCM; ++c) {
-    const int slot = c >> 1;
-    const int32_t p = slot < K ? kept2[qi * K + slot] : -1;
-    lf[c] = p >= 0 ? 2 * p + (c & 1) : -1;
-    val[c] = p >= 0 && lf[c] >= 1 && lf[c] <= qb - 2;
-    sc[c] = val[c] ? leaf_score[(qi * K + slot) * 2 + (c & 1)] : -INFINITY;
-  }
-  int32_t* oi = out_idx + qi * W;
-  float* os = out_score ? out_score + qi * W : nullptr;
-  int pos = 1;
-#pragma unroll
-  for (int c = 0; c < NCM; ++c) {
-    int rank = 0;
-#pragma unroll
-    for (int j = 0; j < NCM; ++j) rank += (val[j] && beats(sc[j], lf[j], sc[c], lf[c])) ? 1 : 0;
-    if (val[c] && rank < K) {  // candidates run in ascending leaf order
-      oi[pos] = lf[c];
-      if (os) os[pos] = sc[c] * kLn2;
-      ++pos;
+    for (int c = 0; c < NCM; ++c) {
+      const int slot = c >> 1;
+      const int32_t p = slot < K ? kept2[qi * K + slot] : -1;
+      lf[c] = p >= 0 ? 2 * p + (c & 1) : -1;
+      val[c] = p >= 0 && lf[c] >= 1 && lf[c] <= qb - 2;
+      sc[c] = val[c] ? leaf_score[(qi * K + slot) * 2 + (c & 1)] : -INFINITY;
     }
+    int32_t* oi = si + threadIdx.x * W;
+    float* os = ss + threadIdx.x * W;
+    int pos = 1;
+#pragma unroll
+    for (int c = 0; c < NCM; ++c) {
+      int rank = 0;
+#pragma unroll
+      for (int j = 0; j < NCM; ++j) rank += (val[j] && beats(sc[j], lf[j], sc[c], lf[c])) ? 1 : 0;
+      if (val[c] && rank < K) {  // candidates run in ascending leaf order
+        oi[pos] = lf[c];
+        os[pos] = sc[c] * kLn2;
+        ++pos;
+      }
+    }
+    oi[0] = 0;
+    os[0] = INFINITY;
+    if (qb - 1 > 0) { oi[pos] = qb - 1; os[pos] = INFINITY; ++pos; }
+    if (qb > 0) { oi[pos] = qb; os[pos] = INFINITY; ++pos; }
+    for (; pos < W; ++pos) { oi[pos] = -1; os[pos] = -INFINITY; }
   }
-  oi[0] = 0;
-  if (os) os[0] = INFINITY;
-  if (qb - 1 > 0) { oi[pos] = (int32_t)(qb - 1); if (os) os[pos] = INFINITY; ++pos; }
-  if (qb > 0) { oi[pos] = (int32_t)qb; if (os) os[pos] = INFINITY; ++pos; }
-  for (; pos < W; ++pos) { oi[pos] = -1; if (os) os[pos] = -INFINITY; }
+  __syncthreads();
+  const int64_t nrow = (nq - q0 < (int64_t)blockDim.x ? nq - q0 : (int64_t)blockDim.x);
+  const int n = (int)nrow * W;
+  int32_t* gi = out_idx + q0 * W;
+  for (int e = threadIdx.x; e < n; e += blockDim.x) gi[e] = si[e];
+  if (out_score) {
+    float* gs = out_score + q0 * W;
+    for (int e = threadIdx.x; e < n; e += blockDim.x) gs[e] = ss[e];
+  }
 }
 
 // ------------------------------------------------------------------ host
