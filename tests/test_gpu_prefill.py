@@ -129,3 +129,59 @@ def test_cpt_needles_sampled(pisa):
     for h in range(s.Hkv):
         last = g["idx"][h * s.N + s.N - 1]
         assert set(blocks[h]) <= set(last.tolist())
+
+
+@pytest.mark.parametrize("N,Hq,Hkv,dtype", [
+    (1, 4, 1, "bf16"),      # one query, only block 0
+    (64, 8, 2, "bf16"),     # one full leaf block
+    (65, 4, 1, "bf16"),     # the first query of block 1 forces blocks 0 and 1
+    (191, 8, 2, "bf16"),    # block 2 is the last with no eligible block (E = [1, qb - 2] empty)
+    (193, 4, 1, "fp32"),    # block 3: one eligible leaf
+    (257, 16, 4, "bf16"),   # tensor-core routing path with a handful of leaves
+])
+def test_prefill_shortest_sequences(pisa, N, Hq, Hkv, dtype):
+    """Sequences too short for any scored level: the output is the forced
+    blocks plus the few eligible leaves, -1 padded."""
+    s = W.Shape(B=2, N=N, Hq=Hq, Hkv=Hkv, d=128, K=4, dtype=dtype)
+    q, k = W.iid(s, 11 + N)
+    g, _, _ = full_parity(pisa, s, q, k)
+    first = g["idx"][0]
+    assert first[0] == 0 and (first[1:] == -1).all()
+
+
+def test_prefill_262144_sampled(pisa):
+    """The 262144-token long-prefill workload in the launch configuration the
+    benchmark times (build, then the route and leaf stages): every query of
+    the last two leaf blocks and 1500 random positions per key head against
+    the oracle, which builds its own fp64 pyramid of all keys."""
+    s = W.sweep(262144)
+    q, k = W.iid(s, 3)
+    p = pisa.params_from_shape(s)
+    sel = pisa.Selector(p)
+    L = pisa.pyramid_levels(p)
+    qd, kd = q.cuda(), k.cuda()
+    tr = torch.full((s.B, s.Hkv, s.N, L, s.K), -7, dtype=torch.int32, device="cuda")
+    pisa.build_pyramid(p, kd, sel.pyramid)
+    pisa.prefill_route(p, qd, sel.pyramid, sel.ws, tr)
+    pisa.prefill_leaves(p, qd, kd, sel.ws, sel.out_idx, sel.out_score)
+    torch.cuda.synchronize()
+    assert sel.device_status() == 0
+    gen = np.random.default_rng(5)
+    keys = []
+    for h in range(s.Hkv):
+        ts = set(range(s.N - 2 * 64, s.N)) | set(gen.integers(0, s.N, 1500).tolist())
+        keys += [(0, h, t) for t in sorted(ts)]
+    rows = torch.tensor([h * s.N + t for (_, h, t) in keys], device="cuda")
+    W_ = s.K + 3
+    idx = sel.out_idx.reshape(-1, W_)[rows].cpu().numpy()
+    score = sel.out_score.reshape(-1, W_)[rows].cpu().double().numpy()
+    trace = tr.reshape(s.B * s.Hkv * s.N, L, s.K)[rows].cpu().numpy()
+    del tr
+    o = oracle.Oracle.from_shape(s)
+    kn = k.double().numpy()
+    pyr = o.pyramid(kn)
+    qsel = np.stack([q[0, h * s.G:(h + 1) * s.G, t].double().numpy() for (_, h, t) in keys])
+    ref = o.select(qsel, kn, pyr, sel=keys, qrows=True)
+    rep = compare(o, qsel, kn, pyr, ref, idx, score, trace, keys, Report(), qmode="rows")
+    print(rep)
+    assert rep.ok(), str(rep)
