@@ -51,6 +51,15 @@ struct DecSmem {
   int32_t zero;  // stays 0
 };
 
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // Exclusive scan of one value per thread over threads [0, 64).
 __device__ __forceinline__ int scan64(int v, int32_t* scratch, int* total) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -365,6 +374,105 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
     __syncthreads();
     // each warp streams its leaves in 4 KB chunks through three buffers: the
     // copies of chunks c+1 and c+2 are in flight while chunk c is scored
+    if (bf16) {
+      // bf16 keys: one bulk copy per chunk (row-major key rows; bulk copies
+      // stream faster here than two-dimensional TMA tiles); warp-level
+      // m16n8k16 MMAs give 16 keys x 8 columns (the G heads) per tile, and
+      // every lane keeps an online max / sum for its two heads (2t, 2t+1)
+      // over its keys (rows g and g+8 of each tile).
+      constexpr int KPC = kChunkBytes / (D * 2);  // keys per chunk: 16 (d = 128) or 32 (d = 64)
+      const int cpl = s.C / KPC;
+      const int nlw = nl > warp ? (nl - warp + kDecWarps - 1) / kDecWarps : 0;
+      const int nch = nlw * cpl;
+      unsigned char* st = &sm.stage[warp][0];
+      const int grp = lane >> 2, tig = lane & 3;
+      uint32_t bq[D / 32][4];  // B fragments: column grp = head grp (zero past G)
+      {
+        const int64_t qoff = (b * pr.Hq + h * G + (grp < G ? grp : 0)) * D;
+#pragma unroll
+        for (int bb = 0; bb < D / 32; ++bb) {
+          uint4 v = grp < G ? *reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(q) + qoff + 32 * bb +
+                                                               8 * tig)
+                            : make_uint4(0u, 0u, 0u, 0u);
+          bq[bb][0] = v.x; bq[bb][1] = v.y; bq[bb][2] = v.z; bq[bb][3] = v.w;
+        }
+      }
+      uint32_t lphase = 0u;
+      auto issue = [&](int c) {
+        if (lane == 0) {
+          const int64_t leaf = sm.leaf[warp + (c / cpl) * kDecWarps];
+          const uint32_t bar = ptx::smem_u32(&sm.bar_leaf[warp][c % kNBuf]);
+          ptx::mbar_arrive_expect_tx(bar, KPC * D * 2);
+          ptx::bulk_g2s(ptx::smem_u32(st + (c % kNBuf) * kChunkBytes),
+                        reinterpret_cast<const uint16_t*>(kc) + (bh * s.N + leaf * s.C + (c % cpl) * KPC) * D,
+                        KPC * D * 2, bar);
+        }
+      };
+      int issued = 0, waited = 0;
+      for (; issued < nch && issued < kNBuf - 1; ++issued) issue(issued);
+      float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;  // heads 2t, 2t+1
+      const float sc = pr.scale2;
+      for (int c = 0; c < nch; ++c) {
+        if (c + kNBuf - 1 < nch) {
+          __syncwarp();  // every lane is done with the buffer this copy overwrites
+          issue(c + kNBuf - 1);
+          issued = c + kNBuf;
+        }
+        const int bf = c % kNBuf;
+        const bool ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.bar_leaf[warp][bf]), (lphase >> bf) & 1u, abort,
+                                               kDecWaitNs);
+        lphase ^= 1u << bf;
+        waited = c + 1;
+        if (!__all_sync(0xffffffffu, ok)) { *abort = 1; break; }
+        if (c % cpl == 0) { m0 = -INFINITY; s0 = 0.0f; m1 = -INFINITY; s1 = 0.0f; }
+        const unsigned char* buf = st + bf * kChunkBytes;
+#pragma unroll
+        for (int mt = 0; mt < KPC / 16; ++mt) {
+          float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          const int r0 = 16 * mt + grp, r1 = r0 + 8;
+#pragma unroll
+          for (int bb = 0; bb < D / 32; ++bb) {
+            // dims 32 bb + 8 t + {0..7} of keys r0 and r1 (the k-step mapping of the B fragments)
+            const uint4 a0 = *reinterpret_cast<const uint4*>(buf + r0 * D * 2 + 64 * bb + 16 * tig);
+            const uint4 a1 = *reinterpret_cast<const uint4*>(buf + r1 * D * 2 + 64 * bb + 16 * tig);
+            mma_bf16_16816(d, a0.x, a1.x, a0.y, a1.y, bq[bb][0], bq[bb][1]);
+            mma_bf16_16816(d, a0.z, a1.z, a0.w, a1.w, bq[bb][2], bq[bb][3]);
+          }
+          // d[0], d[1]: key r0, heads 2t, 2t+1; d[2], d[3]: key r1
+          const float x00 = d[0] * sc, x01 = d[1] * sc, x10 = d[2] * sc, x11 = d[3] * sc;
+          const float n0 = fmaxf(m0, fmaxf(x00, x10)), n1 = fmaxf(m1, fmaxf(x01, x11));
+          s0 = s0 * ptx::ex2(m0 - n0) + ptx::ex2(x00 - n0) + ptx::ex2(x10 - n0);
+          s1 = s1 * ptx::ex2(m1 - n1) + ptx::ex2(x01 - n1) + ptx::ex2(x11 - n1);
+          m0 = n0;
+          m1 = n1;
+        }
+        if (c % cpl == cpl - 1) {
+          // combine the 8 lanes (groups) of each head, then sum the G heads
+#pragma unroll
+          for (int o = 4; o <= 16; o <<= 1) {
+            const float mo0 = __shfl_xor_sync(0xffffffffu, m0, o), so0 = __shfl_xor_sync(0xffffffffu, s0, o);
+            const float mo1 = __shfl_xor_sync(0xffffffffu, m1, o), so1 = __shfl_xor_sync(0xffffffffu, s1, o);
+            const float a0 = fmaxf(m0, mo0), a1 = fmaxf(m1, mo1);
+            s0 = s0 * ptx::ex2(m0 - a0) + so0 * ptx::ex2(mo0 - a0);
+            s1 = s1 * ptx::ex2(m1 - a1) + so1 * ptx::ex2(mo1 - a1);
+            m0 = a0;
+            m1 = a1;
+          }
+          float lse = 0.0f;
+          if (2 * tig < G) lse += m0 + ptx::lg2(s0);
+          if (2 * tig + 1 < G) lse += m1 + ptx::lg2(s1);
+          lse += __shfl_xor_sync(0xffffffffu, lse, 1);
+          lse += __shfl_xor_sync(0xffffffffu, lse, 2);
+          if (lane == 0) sm.lscore[warp + (c / cpl) * kDecWarps] = lse;
+        }
+      }
+      // after an early exit, let copies already issued land before the CTA ends
+      for (int c = waited; c < issued; ++c) {
+        const int bf = c % kNBuf;
+        ptx::mbar_wait_bounded(ptx::smem_u32(&sm.bar_leaf[warp][bf]), (lphase >> bf) & 1u, &sm.zero, kDecWaitNs);
+        lphase ^= 1u << bf;
+      }
+    } else {
     const int kpc = kChunkBytes / (D * esz) < s.C ? kChunkBytes / (D * esz) : s.C;  // keys per chunk
     const int cpl = s.C / kpc;                                                      // chunks per leaf
     const int nlw = nl > warp ? (nl - warp + kDecWarps - 1) / kDecWarps : 0;        // this warp's leaves
@@ -455,6 +563,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
       ptx::mbar_wait_bounded(ptx::smem_u32(&sm.bar_leaf[warp][bf]), (lphase >> bf) & 1u, &sm.zero, kDecWaitNs);
       lphase ^= 1u << bf;
     }
+    }  // fp32 keys
     __syncthreads();
     if (*abort) {
       if (tid == 0) set_status(status, PISA_DEV_TIMEOUT);
