@@ -455,12 +455,32 @@ def side_measurements(args, dev, st, rank):
     torch.cuda.synchronize(dev)
     us = a.elapsed_time(b) / W.DECODE_STEPS * 1e3
     leaf_bytes = s.B * s.Hkv * 2 * s.K * s.C * s.d * 2
+    # child summary rows the walk reads (fp32): all children of the start
+    # level's candidates, then one child per candidate below it
+    qb = (W.DECODE_CACHED + W.DECODE_STEPS // 2) // s.C
+    rows = 0
+    nb = qb + 1
+    L = 1
+    while nb > 1:
+        nb = -(-nb // 2)
+        L += 1
+    l0 = next((lv for lv in range(L, 1, -1) if eligible_count(lv, qb) > s.K), 0)
+    if l0:
+        rows = 2 * eligible_count(l0, qb) + sum(min(2 * s.K, eligible_count(lv, qb)) for lv in range(l0 - 1, 1, -1))
+    walk_bytes = s.B * s.Hkv * rows * s.d * 4
+    step_bytes = leaf_bytes + walk_bytes + s.B * s.Hq * s.d * 2
+    pk = peaks()
     del kc
     torch.cuda.empty_cache()
     return {"sweep": sweep, "decode": {"us_per_step": us, "steps": W.DECODE_STEPS,
                                        "workload": "B=64, 131072 cached keys, Hq=32 Hkv=8 d=128 bf16 K=32",
                                        "leaf_key_bytes_per_step": leaf_bytes,
-                                       "leaf_key_GBps": leaf_bytes / (us * 1e-6) / 1e9}}
+                                       "leaf_key_GBps": leaf_bytes / (us * 1e-6) / 1e9,
+                                       "roofline": {"bound": "hbm", "bytes_per_step": step_bytes,
+                                                    "achieved": step_bytes / (us * 1e-6) / 1e9,
+                                                    "peak": pk["hbm"], "unit": "GB/s",
+                                                    "frac": step_bytes / (us * 1e-6) / 1e9 / pk["hbm"],
+                                                    "bytes": "leaf keys + walked child rows (fp32) + q"}}}
 
 
 # ----------------------------------------------------------- CPU oracle
