@@ -534,7 +534,7 @@ def run_reference(args, ws, rank):
     kn = k_h.double().numpy()
     nb = -(-s.N // s.C)
     blocks = list(range(nb - 1, -1, -max(1, nb // 16)))
-    sel = [(0, h, t) for blk in blocks for h in range(s.Hkv) for t in range(blk * s.C, min((blk + 1) * s.C, s.N), 32)]
+    sel = [(0, h, t) for blk in blocks for h in range(s.Hkv) for t in range(blk * s.C, min((blk + 1) * s.C, s.N), 4)]
     qn = np.stack([q_h[0, h * s.G:(h + 1) * s.G, t].double().numpy() for (_, h, t) in sel])
 
     def step():
