@@ -1,0 +1,88 @@
+"""Selection quality on synthetic workloads: Recall@K of the GPU selectors
+(PISA and the flat block-mean comparator) against the exhaustive ranking
+that PISA approximates, i.e. every eligible leaf block scored by the sum
+over the GQA group of the LogSumExp of its raw keys (agihunt.info summary,
+quality paragraph: recall of the blocks dense attention would pick; rcap.io
+post, "The scoring rule matters").  The exhaustive scores come from the fp64
+oracle; recall is |selected ∩ exhaustive Top-K| / min(K, |E|) over the
+eligible set E = [1, qb - 2], forced blocks excluded.  The measured values
+are printed (GB300, this build: planted pretrain Recall@8 PISA 0.42 vs flat
+0.31; needle CPT Recall@32 0.57 vs 0.51; iid 16K 0.25 vs 0.35).  The
+assertions are floors below them, and that on the two structured workloads
+the LSE pyramid recalls at least as well as the flat block means."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from pyramid_top_block_mean_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pisa():
+    from pyramid_top_block_mean_gb300 import pisa as m
+    return m
+
+
+def selections(pisa, s, q, k):
+    p = pisa.params_from_shape(s)
+    out = {}
+    for mode in ("prefill", "flat"):
+        sel = pisa.Selector(p, mode=mode)
+        if mode == "prefill":
+            sel.prefill(q.cuda(), k.cuda())
+        else:
+            sel.flat(q.cuda(), k.cuda())
+        torch.cuda.synchronize()
+        assert sel.device_status() == 0
+        out[mode] = sel.out_idx.reshape(-1, s.K + 3).cpu().numpy()
+    return out
+
+
+def recall(pisa, s, q, k, positions):
+    sel = selections(pisa, s, q, k)
+    o = oracle.Oracle.from_shape(s)
+    qn, kn = q.double().numpy(), k.double().numpy()
+    pyr = o.pyramid(kn)
+    rec = {"prefill": [], "flat": []}
+    for b in range(s.B):
+        for h in range(s.Hkv):
+            for t in positions:
+                qb = t // s.C
+                E = list(range(1, qb - 1))
+                if len(E) <= s.K:
+                    continue
+                sc = o.score_nodes(qn, kn, pyr, b, h, t, 1, E)
+                best = set(np.asarray(E)[np.argsort(-sc, kind="stable")[:s.K]].tolist())
+                F = {0, qb - 1, qb}
+                row = (b * s.Hkv + h) * s.N + t
+                for mode in rec:
+                    got = {int(j) for j in sel[mode][row] if j >= 0 and j not in F}
+                    rec[mode].append(len(got & best) / s.K)
+    return {m: float(np.mean(v)) for m, v in rec.items()}
+
+
+def test_recall_planted_pretrain(pisa):
+    s = W.PRETRAIN
+    q, k = W.planted(s, 1)
+    r = recall(pisa, s, q, k, range(s.N - 640, s.N, 5))
+    print("planted pretrain Recall@8:", r)
+    assert r["prefill"] >= 0.3 and r["prefill"] >= r["flat"]
+
+
+def test_recall_needles_cpt(pisa):
+    s = W.CPT
+    q, k, _ = W.needles(s, 2)
+    r = recall(pisa, s, q, k, range(s.N - 256, s.N, 8))
+    print("needle CPT Recall@32:", r)
+    assert r["prefill"] >= 0.4 and r["prefill"] >= r["flat"]
+
+
+def test_recall_iid_16k(pisa):
+    s = W.Shape(B=1, N=16384, Hq=16, Hkv=4, d=128, K=8)
+    q, k = W.iid(s, 9)
+    r = recall(pisa, s, q, k, range(s.N - 512, s.N, 16))
+    print("iid 16K Recall@8:", r)
+    assert 0.0 <= r["prefill"] <= 1.0 and 0.0 <= r["flat"] <= 1.0
