@@ -306,6 +306,26 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
     const int row0 = warp * kProdRows, qbase = row0 / G;
     int it = 0;
     bool ok = true;
+    // When G >= RPI, the rows of one copy instruction belong to one query and
+    // lane row hi = lane / CPR is head (r0 % G) + hi: every lane keeps the
+    // warp's QPW query positions in registers and the row address is a few
+    // integer operations (no shuffles).  Otherwise the positions are
+    // broadcast from the lane that loaded them.
+    constexpr bool kFast = G >= RPI && G % RPI == 0;
+    constexpr int NT = kFast ? QPW : 1;  // query positions kept per lane
+    const int hi = lane / CPR;
+    const int64_t ND = pr.N * D;
+    const uint32_t dlane = (ch >> 3) * kHalf + (row0 + hi) * 128;
+    const int xl = (ch & 7) ^ hi;  // swizzle term for row r: (ch & 7) ^ (r & 7), r & 7 = (r0 & 7) + hi
+    auto positions = [&](const int4& inf, int32_t (&tq)[NT]) {
+      if constexpr (kFast) {
+#pragma unroll
+        for (int j = 0; j < QPW; ++j)
+          tq[j] = (inf.x >= 0 && qbase + j < inf.z) ? (pairs[inf.y + qbase + j] >> 5) : 0;
+      } else {
+        tq[0] = (inf.x >= 0 && lane < QPW && qbase + lane < inf.z) ? (pairs[inf.y + qbase + lane] >> 5) : 0;
+      }
+    };
     // Descriptors run two tiles ahead and query positions one tile ahead.
     // The loop is unrolled three times over rotating slots, so a prefetched
     // value is never copied between registers (which would wait for it).
@@ -313,8 +333,10 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
     if (ahead.valid()) ahead.next();
     int4 d0 = ti.valid() ? tile_info[ti.i] : kNoTile;
     int4 d1 = ahead.valid() ? tile_info[ahead.i] : kNoTile, d2;
-    int32_t v0 = (ti.valid() && lane < QPW && qbase + lane < d0.z) ? pairs[d0.y + qbase + lane] : 0, v1, v2;
-    auto step = [&](const int4& info, const int4& info1, int4& slot2, const int32_t& tv, int32_t& slot1) -> bool {
+    int32_t v0[NT], v1[NT], v2[NT];
+    positions(d0, v0);
+    auto step = [&](const int4& info, const int4& info1, int4& slot2, const int32_t (&tq)[NT],
+                    int32_t (&slot1)[NT]) -> bool {
       if (!ti.valid()) return false;
       if (ahead.valid()) ahead.next();
       slot2 = ahead.valid() ? tile_info[ahead.i] : kNoTile;  // tile it + 2
@@ -324,25 +346,34 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
       ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_a[sa]), (use & 1) ^ 1, abort, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; return false; }
       // gather this warp's query-head rows
-      const uint32_t abase = ptx::smem_u32(sm.a[sa]);
+      const uint32_t abase = ptx::smem_u32(sm.a[sa]) + dlane;
       const int cnt = info.z;
-      const int32_t tq = tv >> 5;
+      if constexpr (kFast) {
+        const uint16_t* qh = q + ((int64_t)b * pr.Hq + h * G + hi) * ND + ch * 8;  // head hi of the group
 #pragma unroll
-      for (int r0 = 0; r0 < kProdRows; r0 += RPI) {
-        const int rl = r0 + lane / CPR;
-        const int r = row0 + rl;
-        const int64_t t = __shfl_sync(0xffffffffu, tq, rl / G);
-        if (qbase + rl / G < cnt) {
-          const int g = r % G;
-          const uint16_t* src = q + ((((int64_t)b * pr.Hq + h * G + g) * pr.N + t) * D + ch * 8);
-          const uint32_t dst = abase + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-          ptx::cp_async_16(dst, src);
+        for (int r0 = 0; r0 < kProdRows; r0 += RPI) {
+          if (qbase + r0 / G < cnt) {
+            const uint16_t* src = qh + (r0 % G) * ND + (int64_t)tq[r0 / G] * D;
+            ptx::cp_async_16(abase + r0 * 128 + ((xl ^ (r0 & 7)) << 4), src);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int r0 = 0; r0 < kProdRows; r0 += RPI) {
+          const int rl = r0 + hi;
+          const int r = row0 + rl;
+          const int64_t t = __shfl_sync(0xffffffffu, tq[0], rl / G);
+          if (qbase + rl / G < cnt) {
+            const int g = r % G;
+            const uint16_t* src = q + ((((int64_t)b * pr.Hq + h * G + g) * pr.N + t) * D + ch * 8);
+            ptx::cp_async_16(abase + r0 * 128 + (((ch & 7) ^ (r & 7)) << 4), src);
+          }
         }
       }
       // the stage's barrier counts this thread once its copies have landed
       ptx::cp_async_arrive_noinc(ptx::smem_u32(&sm.full_a[sa]));
       // query positions of tile it + 1 (its descriptor arrived a tile ago)
-      slot1 = (info1.x >= 0 && lane < QPW && qbase + lane < info1.z) ? pairs[info1.y + qbase + lane] : 0;
+      positions(info1, slot1);
       ++it;
       ti.next();
       return true;
