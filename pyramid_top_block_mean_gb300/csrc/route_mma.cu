@@ -214,7 +214,10 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob 
     {
       const int nw[2] = {__shfl_sync(0xffffffffu, nwork, 0), __shfl_sync(0xffffffffu, nwork, 16)};
       const int nmax = max(nw[0], nw[1]);
+      // per-level row bases of both queries (hi and lo pyramids); a row adds node * D
       const int64_t loff = s.off[level - 2] * D + (grp & 1) * 32 + 8 * tig;
+      const uint16_t* hbase[2] = {phi + pbase[0] + loff, phi + pbase[1] + loff};
+      const uint16_t* lbase[2] = {plo + pbase[0] + loff, plo + pbase[1] + loff};
       // lanes (even group, t < 2) finish node grp/2, lanes (odd group, t >= 2) node 4 + grp/2
       const bool roleA = !(grp & 1) && tig < 2, roleB = (grp & 1) && tig >= 2;
       const float sc = pr.scale2;
@@ -225,11 +228,11 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob 
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
             const int w = r0 + 4 * rr + (grp >> 1);
-            const int64_t ro = pbase[u] + loff + (int64_t)(w < nw[u] ? smw[u].work[w] : 0) * D;
+            const uint32_t ro = (uint32_t)(w < nw[u] ? smw[u].work[w] : 0) * (uint32_t)D;  // < 2^27
 #pragma unroll
             for (int bb = 0; bb < NB; ++bb) {
-              hv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(phi + ro + 64 * bb));
-              lv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(plo + ro + 64 * bb));
+              hv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(hbase[u] + ro + 64 * bb));
+              lv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(lbase[u] + ro + 64 * bb));
             }
           }
         // four independent accumulator chains: (query) x (hi, lo)
