@@ -124,22 +124,26 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob 
   RouteMmaQPad<NC>* smw = reinterpret_cast<RouteMmaQPad<NC>*>(smem_raw) + (threadIdx.x / 32) * 2;
   const int lane = threadIdx.x & 31, ll = lane & 15, half = lane >> 4;
   const int grp = lane >> 2, tig = lane & 3;  // MMA group id / thread in group
-  const int64_t nq = pr.B * pr.Hkv * pr.N;
-  const int64_t qi = ((int64_t)blockIdx.x * WARPS + threadIdx.x / 32) * 2 + half;
+  // query counts are below 2^31 (the prefill size limit), so 32-bit index math
+  const uint32_t nq = (uint32_t)(pr.B * pr.Hkv * pr.N), N32 = (uint32_t)pr.N;
+  const uint32_t qi = (blockIdx.x * WARPS + threadIdx.x / 32) * 2 + half;
   const bool live = qi < nq;
-  const int64_t qc = live ? qi : nq - 1;
-  const int64_t t = qc % pr.N;
+  const uint32_t qc = live ? qi : nq - 1;
+  const int64_t t = qc % N32;
   const int K = pr.K;
   const int64_t qb = t / s.C;
-  int32_t* kout = kept2 + qc * K;
-  int32_t* trow = (trace && live) ? trace + qc * (int64_t)s.L * K : nullptr;
+  int32_t* kout = kept2 + (int64_t)qc * K;
+  int32_t* trow = (trace && live) ? trace + (int64_t)qc * s.L * K : nullptr;
   if (trow)
     for (int i = ll; i < s.L * K; i += 16) trow[i] = -1;
 
   int l0 = 0;
   if (live && qb - 2 >= 1) {
-    for (int level = s.L; level >= 2; --level)
-      if (eligible_count(level, qb) > K) { l0 = level; break; }
+    // start level: the highest level with more than K eligible nodes, i.e.
+    // the largest l <= L with (qb - 2) >> (l - 1) >= K
+    const uint32_t xk = (uint32_t)(qb - 2) / (uint32_t)K;
+    if (xk >= 2) l0 = min((int)s.L, 32 - __clz(xk));
+    if (l0 < 2) l0 = 0;
     if (trow)
       for (int level = s.L; level >= 2 && level > l0; --level) {
         const int64_t n = eligible_count(level, qb);
@@ -157,14 +161,15 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob 
 
   // B fragments of both queries: column grp = (head grp % 4, half grp / 4)
   constexpr int NB = D / 64;  // k-step pairs per half
-  const int64_t qw = ((int64_t)blockIdx.x * WARPS + threadIdx.x / 32) * 2;
+  const uint32_t qw = (blockIdx.x * WARPS + threadIdx.x / 32) * 2;
   uint32_t bq[2][NB][4];
   int64_t pbase[2];
 #pragma unroll
   for (int u = 0; u < 2; ++u) {
-    const int64_t qu = min(qw + u, nq - 1);
-    const int64_t tu = qu % pr.N, bhu = qu / pr.N;
-    const int64_t qrow = (((bhu / pr.Hkv) * pr.Hq + (bhu % pr.Hkv) * G + (grp & 3)) * pr.N + tu) * D +
+    const uint32_t qu = min(qw + u, nq - 1);
+    const uint32_t tu = qu % N32, bhu = qu / N32;
+    const uint32_t Hkv = (uint32_t)pr.Hkv;
+    const int64_t qrow = ((int64_t)((bhu / Hkv) * (uint32_t)pr.Hq + (bhu % Hkv) * G + (grp & 3)) * pr.N + tu) * D +
                          (grp >> 2) * (D / 2) + 8 * tig;
 #pragma unroll
     for (int bb = 0; bb < NB; ++bb) {
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob 
       bq[u][bb][0] = v.x; bq[u][bb][1] = v.y; bq[u][bb][2] = v.z; bq[u][bb][3] = v.w;
     }
     // the two queries of a warp may belong to different (b, h) rows of the pyramid
-    pbase[u] = bhu * s.P * D;
+    pbase[u] = (int64_t)bhu * s.P * D;
   }
 
   int cur = 0;
