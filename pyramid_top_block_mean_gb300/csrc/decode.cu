@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
     }
     int nkept;
     const int kp = scan64(tid < 64 ? keep : 0, sm.scan, &nkept);
-    if (keep) {
+    if (keep && kp < K) {  // the ranking order is total: at most K are kept
       oi[1 + kp] = sm.leaf[tid];
       if (os) os[1 + kp] = sm.lscore[tid] * kLn2;
     }

@@ -134,8 +134,8 @@ __global__ void __launch_bounds__(kLeafWarps * 32) leaf_simt_kernel(Prob pr, Pyr
       keep = rank < K;
     }
     const unsigned bal = __ballot_sync(0xffffffffu, keep);
-    if (keep) {
-      const int pos = 1 + nkept + __popc(bal & ((1u << lane) - 1));
+    const int pos = 1 + nkept + __popc(bal & ((1u << lane) - 1));
+    if (keep && pos <= K) {  // the ranking order is total: at most K are kept
       oi[pos] = sm.leaf[i];
       if (os) os[pos] = sm.score[i] * kLn2;
     }

@@ -592,8 +592,8 @@ __global__ void __launch_bounds__(256) finalize_kernel(Prob pr, const int32_t* _
   for (int j = 0; j < rounds; ++j) {
     const bool keep = val[j] && rank[j] < K;
     const unsigned bal = __ballot_sync(0xffffffffu, keep);
-    if (keep) {
-      const int pos = 1 + nkept + __popc(bal & ((1u << lane) - 1));
+    const int pos = 1 + nkept + __popc(bal & ((1u << lane) - 1));
+    if (keep && pos <= K) {  // the ranking order is total: at most K are kept
       oi[pos] = lf[j];
       if (os) os[pos] = sc[j] * kLn2;
     }
@@ -647,7 +647,7 @@ __global__ void __launch_bounds__(256) finalize_small_kernel(Prob pr, const int3
       int rank = 0;
 #pragma unroll
       for (int j = 0; j < NCM; ++j) rank += (val[j] && beats(sc[j], lf[j], sc[c], lf[c])) ? 1 : 0;
-      if (val[c] && rank < K) {  // candidates run in ascending leaf order
+      if (val[c] && rank < K && pos <= K) {  // candidates run in ascending leaf order
         oi[pos] = lf[c];
         os[pos] = sc[c] * kLn2;
         ++pos;

@@ -142,7 +142,11 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
 }
 
 // Higher score first; equal scores go to the lower node index.
+// A NaN score ranks as -inf, so the order is total whatever the inputs hold
+// and a Top-K keeps exactly min(K, n) candidates.
 __device__ __forceinline__ bool beats(float sa, int64_t ia, float sb, int64_t ib) {
+  sa = sa != sa ? -INFINITY : sa;
+  sb = sb != sb ? -INFINITY : sb;
   return sa > sb || (sa == sb && ia < ib);
 }
 

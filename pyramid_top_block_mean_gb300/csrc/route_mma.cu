@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob 
           const float a = comp(ya[sl], g), bb = comp(yb[sl], g);
           scv += (s0 >= 0 && s1 != -1) ? lse2_pair(a, bb) : (s0 >= 0 ? a : bb);
         }
-        if (scv == 0.0f) scv = 0.0f;  // -0 ranks like +0
+        if (scv == 0.0f) scv = 0.0f;        // -0 ranks like +0
+        if (scv != scv) scv = -INFINITY;     // NaN ranks last (keys stay <= 0xff800000)
         key[sl] = orderable_key(scv);
       }
     }

@@ -185,3 +185,27 @@ def test_prefill_262144_sampled(pisa):
     rep = compare(o, qsel, kn, pyr, ref, idx, score, trace, keys, Report(), qmode="rows")
     print(rep)
     assert rep.ok(), str(rep)
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv", [("bf16", 8, 2), ("fp32", 4, 2)])
+def test_prefill_nonfinite_keys_stay_well_formed(pisa, dtype, Hq, Hkv):
+    """Keys holding NaN and +-inf (whole leaf blocks and single entries):
+    every ranking treats a NaN score as -inf, so each query still gets its
+    forced blocks plus exactly min(K, |E|) causal blocks, ascending and -1
+    padded, and the device status stays clear."""
+    from parity import check_structure
+    s = W.Shape(B=1, N=64 * 40 + 9, Hq=Hq, Hkv=Hkv, d=128, K=4, dtype=dtype)
+    q, k = W.iid(s, 21)
+    k = k.float()
+    k[0, 0, 64 * 5:64 * 6] = float("nan")
+    k[0, 0, 64 * 11 + 3, 7] = float("inf")
+    k[0, Hkv - 1, 64 * 17:64 * 18, :4] = -float("inf")
+    k[0, Hkv - 1, 64 * 23 + 1] = float("nan")
+    k = k.to(s.torch_dtype)
+    g = run_prefill(pisa, s, q, k, trace=False)
+    rep = Report()
+    for h in range(s.Hkv):
+        for t in range(s.N):
+            row = h * s.N + t
+            ok = check_structure(g["idx"][row], None, t, s.C, s.K, rep, f"(h={h},t={t})")
+            assert ok, rep.failures
