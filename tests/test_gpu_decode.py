@@ -132,3 +132,25 @@ def test_decode_full_size_sampled(pisa):
     pisa.build_pyramid(p, kcd, fresh, lens_tensor([W.DECODE_CACHED + W.DECODE_STEPS] * s.B))
     torch.cuda.synchronize()
     assert torch.equal(fresh, sel.pyramid)
+
+
+def test_decode_nonfinite_keys_stay_well_formed(pisa):
+    """Cache keys holding NaN and +-inf: the decode walk and its leaf Top-K
+    rank NaN scores as -inf, so each sequence still gets its forced blocks
+    plus exactly min(K, |E|) causal blocks and the status stays clear."""
+    from parity import check_structure
+    s = W.Shape(B=3, N=4096, Hq=8, Hkv=2, d=128, K=8)
+    q_steps, kc = W.decode_inputs(s, 23, steps=2)
+    kc = kc.float()
+    kc[0, 0, 64 * 7:64 * 8] = float("nan")
+    kc[1, 1, 64 * 20 + 5, 3] = float("inf")
+    kc[2, 0, 64 * 30:64 * 31, :8] = -float("inf")
+    kc = kc.to(torch.bfloat16)
+    lens0 = [4000, 3000, 2500]
+    results = run_steps(pisa, s, q_steps, kc, lens0, 2, check_rebuild=False)
+    rep = Report()
+    for lens, idx, _, _ in results:
+        for b in range(s.B):
+            for h in range(s.Hkv):
+                ok = check_structure(idx[b * s.Hkv + h], None, lens[b] - 1, s.C, s.K, rep, f"(b={b},h={h})")
+                assert ok, rep.failures
