@@ -6,18 +6,21 @@
 // GQA group, the heads' scores summed).
 //
 // A warp walks two queries.  Per level, the child summary rows each query
-// needs (at most 2K) are multiplied against its four query-head vectors as a
-// sequence of warp-level m16n8k16 MMAs: A = 16 child rows (8 per query),
-// B = 8 columns (the 2 x 4 query heads), fp32 accumulation.  Only the two
-// diagonal 8 x 4 blocks are used.  Each lane loads two 16-byte slices per row
-// and K block with no shuffles or reductions.  The query rows are bf16, so they
-// are exact in the MMA; each fp32 summary is split into bf16 hi + lo
-// (mu = hi + lo to about 2^-16 relative) and multiplied twice, so the dots
-// match an fp32 computation to ~1e-6.  The two pieces are prepared once per
-// call by split_pyramid_kernel into the workspace.
+// needs (one per candidate whose own dot is known, two at the start level)
+// are multiplied against its four query-head vectors as warp-level m16n8k16
+// MMAs with fp32 accumulation: for one query, A = 16 rows = 8 child nodes x
+// the two halves of the d dims, B = 8 columns = the 4 heads x the two halves;
+// only the blocks where row half = column half are used, and one shuffle
+// pair adds a node's two halves.  With the rows stored half-interleaved,
+// the eight lanes of a node read one whole 128-byte line per load.  The
+// query rows are bf16, so they are exact in the MMA; each fp32 summary is
+// split into bf16 hi + lo (mu = hi + lo to about 2^-16 relative) and
+// multiplied twice, so the dots match an fp32 computation to ~1e-6.  The two
+// pieces are prepared once per call by split_pyramid_kernel.
 //
-// The candidate bookkeeping (work list, scores, Top-K by a 64-bit rank key,
-// expansion into ascending ping-pong lists) runs on 16 lanes per query.
+// The candidate bookkeeping (work list by ballot prefix sums, scores, Top-K
+// by 32-bit orderable keys with the slot order breaking ties, expansion
+// into ascending ping-pong lists) runs on 16 lanes per query.
 #include <algorithm>
 
 #include "pisa_common.cuh"
