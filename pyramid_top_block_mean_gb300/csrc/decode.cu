@@ -14,9 +14,11 @@
 //     each into shared memory (one HBM round trip per level), the four warps
 //     form the G-head dot products, and candidate scoring / Top-K / expansion
 //     run on shared-memory lists (at most 2K candidates).
-//  3. leaves: each warp streams its candidate leaf tiles (C keys) with bulk
-//     copies into its own 16 KB stage and keeps an online log2-sum-exp2 per
-//     head; then the Top-K with the forced blocks.
+//  3. leaves: each warp streams its candidate leaves in 4 KB chunks (one bulk
+//     copy each, three buffers per warp) and keeps an online log2-sum-exp2 per
+//     head; bf16 keys are scored by warp-level m16n8k16 MMAs (16 keys x the G
+//     heads per tile), fp32 keys by CUDA-core FMAs; then the Top-K with the
+//     forced blocks.
 // The step is bound by HBM: it reads ~2K leaf tiles per (sequence, key head).
 #include "pisa_common.cuh"
 #include "pisa_internal.h"
