@@ -99,6 +99,10 @@ def test_pretrain_planted_bf16(pisa):
     (3333, 4, 2, 128, 3, "fp32"),         # G = 2, fp32 leaves on the CUDA cores
     (64 * 3 + 5, 4, 4, 128, 8, "bf16"),   # a few leaves only
     (5000, 2, 2, 64, 32, "bf16"),         # K = 32
+    (3000, 8, 2, 64, 8, "bf16"),          # tensor-core routing with d = 64
+    (2500, 8, 2, 128, 1, "bf16"),         # K = 1
+    (2600, 16, 4, 128, 2, "bf16"),        # K = 2
+    (2700, 16, 4, 128, 16, "bf16"),       # K = 16 on the tensor-core path
 ])
 def test_prefill_shapes(pisa, N, Hq, Hkv, d, K, dtype):
     s = W.Shape(B=2, N=N, Hq=Hq, Hkv=Hkv, d=d, K=K, dtype=dtype)
