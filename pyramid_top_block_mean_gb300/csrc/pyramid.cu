@@ -120,22 +120,33 @@ __global__ void __launch_bounds__(256) build_lower_kernel(Prob pr, Pyr s, const 
 template <int D>
 __global__ void __launch_bounds__(256) build_upper_kernel(Prob pr, Pyr s, const int32_t* __restrict__ seq_lens,
                                                           float* __restrict__ pyr) {
+  // D / 4 threads per node, four consecutive dims each (float4); the node
+  // counts are computed once per node, and the loop over a level's nodes is
+  // unrolled so several child loads are in flight
+  constexpr int TPN = D / 4, NPP = 256 / TPN;  // threads per node, nodes per pass
   const int64_t b = blockIdx.y, h = blockIdx.x;
   const int64_t len = seq_len_of(seq_lens, b, s.N);
   float* ph = pyr + (b * pr.Hkv + h) * s.P * D;
+  const int c4 = (threadIdx.x % TPN) * 4, jl = threadIdx.x / TPN;
   for (int level = kLowerLevels + 1; level <= s.L; ++level) {
-    const int64_t n = s.size[level - 1];
-    const int64_t nc = s.size[level - 2];
+    const int n = (int)s.size[level - 1];
+    const int nc = (int)s.size[level - 2];
     const float* child = ph + s.off[level - 2] * D;
     float* out = ph + s.off[level - 1] * D;
-    for (int64_t w = threadIdx.x; w < n * D; w += blockDim.x) {
-      const int64_t j = w / D;
-      const int c = (int)(w % D);
-      const int64_t n0 = node_count(s, level - 1, 2 * j, len);
-      const int64_t n1 = (2 * j + 1 < nc) ? node_count(s, level - 1, 2 * j + 1, len) : 0;
-      const float m0 = child[(2 * j) * D + c];
-      const float m1 = (2 * j + 1 < nc) ? child[(2 * j + 1) * D + c] : 0.0f;
-      out[j * D + c] = combine_children(m0, n0, m1, n1);
+#pragma unroll 4
+    for (int j = jl; j < n; j += NPP) {
+      const int64_t n0 = node_count(s, level - 1, 2 * (int64_t)j, len);
+      const bool has1 = 2 * j + 1 < nc;
+      const int64_t n1 = has1 ? node_count(s, level - 1, 2 * (int64_t)j + 1, len) : 0;
+      const float4 m0 = *reinterpret_cast<const float4*>(child + (int64_t)(2 * j) * D + c4);
+      const float4 m1 = has1 ? *reinterpret_cast<const float4*>(child + (int64_t)(2 * j + 1) * D + c4)
+                             : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      float4 r;
+      r.x = combine_children(m0.x, n0, m1.x, n1);
+      r.y = combine_children(m0.y, n0, m1.y, n1);
+      r.z = combine_children(m0.z, n0, m1.z, n1);
+      r.w = combine_children(m0.w, n0, m1.w, n1);
+      *reinterpret_cast<float4*>(out + (int64_t)j * D + c4) = r;
     }
     __syncthreads();
   }
