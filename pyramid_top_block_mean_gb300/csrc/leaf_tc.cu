@@ -637,7 +637,8 @@ __global__ void __launch_bounds__(256) finalize_small_kernel(Prob pr, const int3
       const int32_t p = slot < K ? kept2[qi * K + slot] : -1;
       lf[c] = p >= 0 ? 2 * p + (c & 1) : -1;
       val[c] = p >= 0 && lf[c] >= 1 && lf[c] <= qb - 2;
-      sc[c] = val[c] ? leaf_score[(qi * K + slot) * 2 + (c & 1)] : -INFINITY;
+      const float v = val[c] ? leaf_score[(qi * K + slot) * 2 + (c & 1)] : -INFINITY;
+      sc[c] = v != v ? -INFINITY : v;  // NaN ranks as -inf (a total order)
     }
     int32_t* oi = si + threadIdx.x * W;
     float* os = ss + threadIdx.x * W;
@@ -646,7 +647,7 @@ __global__ void __launch_bounds__(256) finalize_small_kernel(Prob pr, const int3
     for (int c = 0; c < NCM; ++c) {
       int rank = 0;
 #pragma unroll
-      for (int j = 0; j < NCM; ++j) rank += (val[j] && beats(sc[j], lf[j], sc[c], lf[c])) ? 1 : 0;
+      for (int j = 0; j < NCM; ++j) rank += (val[j] && beats_clean(sc[j], lf[j], sc[c], lf[c])) ? 1 : 0;
       if (val[c] && rank < K && pos <= K) {  // candidates run in ascending leaf order
         oi[pos] = lf[c];
         os[pos] = sc[c] * kLn2;
