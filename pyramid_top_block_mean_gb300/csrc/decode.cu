@@ -290,7 +290,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
             else if (s1 == -2) bb = ((n0 + n1) * sm.x[tid][g] - n0 * a) / n1;
             sc += (s0 >= 0 && s1 != -1) ? lse2_pair(a, bb) : (s0 >= 0 ? a : bb);
           }
-          sm.score[tid] = sc;
+          sm.score[tid] = sc != sc ? -INFINITY : sc;  // NaN ranks as -inf
         }
         __syncthreads();
         // Top-K and expansion, in index order
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
           if (2 * tig + 1 < G) lse += m1 + ptx::lg2(s1);
           lse += __shfl_xor_sync(0xffffffffu, lse, 1);
           lse += __shfl_xor_sync(0xffffffffu, lse, 2);
-          if (lane == 0) sm.lscore[warp + (c / cpl) * kDecWarps] = lse;
+          if (lane == 0) sm.lscore[warp + (c / cpl) * kDecWarps] = lse != lse ? -INFINITY : lse;
         }
       }
       // after an early exit, let copies already issued land before the CTA ends
@@ -556,7 +556,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
         float lse = mh + ptx::lg2(sh);
 #pragma unroll
         for (int o = G / 2; o >= 1; o >>= 1) lse += __shfl_xor_sync(0xffffffffu, lse, o);
-        if (lane == 0) sm.lscore[warp + (c / cpl) * kDecWarps] = lse;
+        if (lane == 0) sm.lscore[warp + (c / cpl) * kDecWarps] = lse != lse ? -INFINITY : lse;
       }
     }
     // after an early exit, let copies already issued land before the CTA ends

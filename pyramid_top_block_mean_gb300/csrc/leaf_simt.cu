@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kLeafWarps * 32) leaf_simt_kernel(Prob pr, Pyr
     // sum over the G heads (lanes 0..G-1 hold distinct heads)
 #pragma unroll
     for (int o = G / 2; o >= 1; o >>= 1) lse += __shfl_xor_sync(0xffffffffu, lse, o);
-    if (lane == 0) sm.score[li] = lse;
+    if (lane == 0) sm.score[li] = lse != lse ? -INFINITY : lse;  // NaN ranks as -inf
   }
   __syncwarp();
 

@@ -569,7 +569,10 @@ __global__ void __launch_bounds__(256) finalize_kernel(Prob pr, const int32_t* _
       if (p >= 0) {
         lf[j] = 2 * p + (c & 1);
         val[j] = node_eligible(1, lf[j], qb);
-        if (val[j]) sc[j] = leaf_score[(qi * K + (c >> 1)) * 2 + (c & 1)];
+        if (val[j]) {
+          const float v = leaf_score[(qi * K + (c >> 1)) * 2 + (c & 1)];
+          sc[j] = v != v ? -INFINITY : v;  // NaN ranks as -inf
+        }
       }
     }
   }
@@ -647,7 +650,7 @@ __global__ void __launch_bounds__(256) finalize_small_kernel(Prob pr, const int3
     for (int c = 0; c < NCM; ++c) {
       int rank = 0;
 #pragma unroll
-      for (int j = 0; j < NCM; ++j) rank += (val[j] && beats_clean(sc[j], lf[j], sc[c], lf[c])) ? 1 : 0;
+      for (int j = 0; j < NCM; ++j) rank += (val[j] && beats(sc[j], lf[j], sc[c], lf[c])) ? 1 : 0;
       if (val[c] && rank < K && pos <= K) {  // candidates run in ascending leaf order
         oi[pos] = lf[c];
         os[pos] = sc[c] * kLn2;

@@ -142,16 +142,10 @@ __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
 }
 
 // Higher score first; equal scores go to the lower node index.
-// The same order for scores already free of NaN (map NaN to -inf on load).
-__device__ __forceinline__ bool beats_clean(float sa, int32_t ia, float sb, int32_t ib) {
-  return sa > sb || (sa == sb && ia < ib);
-}
-
-// A NaN score ranks as -inf, so the order is total whatever the inputs hold
-// and a Top-K keeps exactly min(K, n) candidates.
-__device__ __forceinline__ bool beats(float sa, int64_t ia, float sb, int64_t ib) {
-  sa = sa != sa ? -INFINITY : sa;
-  sb = sb != sb ? -INFINITY : sb;
+// Ranking order of every Top-K: higher score first, then lower index.  The
+// callers map a NaN score to -inf when they load it, so the order is total
+// whatever the inputs hold and a Top-K keeps exactly min(K, n) candidates.
+__device__ __forceinline__ bool beats(float sa, int32_t ia, float sb, int32_t ib) {
   return sa > sb || (sa == sb && ia < ib);
 }
 
