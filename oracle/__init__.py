@@ -66,6 +66,9 @@ def lib():
         L.po_select_flat.argtypes = [ctypes.POINTER(_Params), _dp, _dp, _i64, _i64p,
                                      _i32p, _dp, _dp]
         L.po_select_flat.restype = ctypes.c_int
+        L.po_sparse_attention.argtypes = [ctypes.POINTER(_Params), _dp, _dp, _dp, _i32p,
+                                          _i64, _i64p, _dp]
+        L.po_sparse_attention.restype = ctypes.c_int
         L.po_num_threads.restype = ctypes.c_int
         L.po_set_num_threads.argtypes = [ctypes.c_int]
         _lib = L
@@ -194,6 +197,30 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle flat: bad arguments")
         return dict(idx=idx, score=score, margin=margin)
+
+
+    def attend(self, q, k, v, idx, sel=None) -> np.ndarray:
+        """Attention of the queries over their selected blocks (causal inside
+        each block); idx is the full [B, Hkv, N, K+3] selection.  Returns
+        [nq, G, d] fp64 for the sel triples (b, h, t), or every query."""
+        q = _f64(q); k = _f64(k); v = _f64(v)
+        idx = np.ascontiguousarray(np.asarray(idx, np.int32).reshape(-1))
+        if idx.size != self.B * self.Hkv * self.N * (self.K + 3):
+            raise ValueError("oracle attend: idx has the wrong size")
+        if sel is None:
+            nq = self.B * self.Hkv * self.N
+            selp = None
+        else:
+            selp = np.ascontiguousarray(np.asarray(sel, np.int64).reshape(-1, 3))
+            nq = selp.shape[0]
+        G = self.Hq // self.Hkv
+        out = np.empty((nq, G, self.d), np.float64)
+        rc = lib().po_sparse_attention(ctypes.byref(self.p), _ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp),
+                                       _ptr(idx, _i32p), nq,
+                                       None if selp is None else _ptr(selp, _i64p), _ptr(out, _dp))
+        if rc != 0:
+            raise ValueError("oracle attend: bad arguments or a query with no key")
+        return out
 
 
 def num_threads() -> int:

@@ -31,7 +31,10 @@
  *  - "LSE" is the literal log-sum-exp, summed over the query heads of a GQA
  *    group; the scale is 1/sqrt(d) unless another is given;
  *  - forced blocks F = {0, qb-1, qb} are added to the Top-K of the rest;
- *  - ties in Top-K go to the lower node index.
+ *  - ties in Top-K go to the lower node index;
+ *  - attention over the selection (po_sparse_attention) reads the keys of the
+ *    union of the selected blocks at positions <= t, with the selection's
+ *    score scale, and plain softmax-weighted values.
  */
 #include <math.h>
 #include <stdint.h>
@@ -510,6 +513,92 @@ int po_select_flat(const po_params* p, const double* q, const double* pyr,
     }
     for (int j = 0; j < n; ++j) { oi[j] = (int32_t)all[j].idx; os[j] = all[j].score; }
     free(all); free(c); free(z); free(score);
+  }
+  return err ? -1 : 0;
+}
+
+/* ------------------------------------------- attention over the selection
+ * Block-sparse attention that reads only the selected blocks [AGI opening
+ * paragraph: each query reads only its Top-K tiles, so the attention pass is
+ * linear in N; RCAP "Selection walks the tree top-down": the leaf indices are
+ * then used for sparse attention over the original keys].  For the query
+ * (b, key head h, position t) and each query head g of its group:
+ *   A(t) = union over the selected blocks j >= 0 of idx[b, h, t, :] of the
+ *          key positions i in [j C, (j+1) C) with i <= t   (causal);
+ *   o_g  = sum_{i in A} exp(s q_g . k_i) v_i / sum_{i in A} exp(s q_g . k_i),
+ * with s the score scale of the selection (1/sqrt(d) unless given).  A block
+ * listed twice counts once.  q [B, Hq, N, d]; k, v [B, Hkv, N, d]; idx
+ * [B, Hkv, N, K+3] int32 (-1 = empty slot); sel: nsel triples (b, h, t), or
+ * NULL for every (b, h, t) in order.  out [nq, G, d] fp64.  Returns -1 on a
+ * bad position or when some query has no attended key.                   */
+int po_sparse_attention(const po_params* p, const double* q, const double* k,
+                        const double* v, const int32_t* idx, int64_t nsel,
+                        const int64_t* sel, double* out) {
+  const int W = p->K + 3;
+  const int d = p->d;
+  if (p->Hkv <= 0 || p->Hq % p->Hkv != 0 || p->K < 1 || p->C < 1 || d < 1)
+    return -1;
+  const int32_t G = p->Hq / p->Hkv;
+  const double s = po_scale(p);
+  const int64_t nq = sel ? nsel : p->B * p->Hkv * p->N;
+  int err = 0;
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int64_t i = 0; i < nq; ++i) {
+    int64_t b, t;
+    int32_t h;
+    if (sel) { b = sel[3 * i]; h = (int32_t)sel[3 * i + 1]; t = sel[3 * i + 2]; }
+    else {
+      b = i / (p->Hkv * p->N); h = (int32_t)((i / p->N) % p->Hkv); t = i % p->N;
+    }
+    if (b < 0 || b >= p->B || h < 0 || h >= p->Hkv || t < 0 || t >= p->N) { err = 1; continue; }
+    const int32_t* row = idx + ((b * p->Hkv + h) * p->N + t) * W;
+    /* the attended key positions, each once, ascending */
+    int64_t* keys = (int64_t*)malloc(sizeof(int64_t) * (size_t)W * (size_t)p->C);
+    int64_t nk = 0;
+    int64_t blocks[64];
+    int nbk = 0;
+    for (int j = 0; j < W && j < 64; ++j) {
+      const int64_t blk = row[j];
+      int seen = 0;
+      if (blk < 0) continue;
+      for (int u = 0; u < nbk; ++u) seen |= blocks[u] == blk;
+      if (seen) continue;
+      blocks[nbk++] = blk;
+    }
+    for (int u = 1; u < nbk; ++u) {  /* ascending block order */
+      int64_t x = blocks[u];
+      int w = u - 1;
+      while (w >= 0 && blocks[w] > x) { blocks[w + 1] = blocks[w]; --w; }
+      blocks[w + 1] = x;
+    }
+    for (int u = 0; u < nbk; ++u)
+      for (int64_t c = 0; c < p->C; ++c) {
+        const int64_t pos = blocks[u] * p->C + c;
+        if (pos <= t && pos < p->N) keys[nk++] = pos;
+      }
+    if (nk == 0) { err = 1; free(keys); continue; }
+    double* z = (double*)malloc(sizeof(double) * (size_t)nk);
+    const double* kh = k + (b * p->Hkv + h) * p->N * d;
+    const double* vh = v + (b * p->Hkv + h) * p->N * d;
+    for (int32_t g = 0; g < G; ++g) {
+      const double* qr = q + ((b * p->Hq + (int64_t)h * G + g) * p->N + t) * d;
+      double* o = out + (i * G + g) * d;
+      double m = -INFINITY, l = 0.0;
+      for (int64_t u = 0; u < nk; ++u) {
+        z[u] = s * po_dot(qr, kh + keys[u] * d, d);
+        if (z[u] > m) m = z[u];
+      }
+      for (int c = 0; c < d; ++c) o[c] = 0.0;
+      for (int64_t u = 0; u < nk; ++u) {
+        const double w = exp(z[u] - m);
+        const double* vr = vh + keys[u] * d;
+        l += w;
+        for (int c = 0; c < d; ++c) o[c] += w * vr[c];
+      }
+      for (int c = 0; c < d; ++c) o[c] /= l;
+    }
+    free(z);
+    free(keys);
   }
   return err ? -1 : 0;
 }

@@ -72,6 +72,15 @@ def iid(shape: Shape, seed: int, device: str = "cpu"):
     return q.to(shape.torch_dtype), k.to(shape.torch_dtype)
 
 
+def values(shape: Shape, seed: int, device: str = "cpu"):
+    """v [B, Hkv, N, d] iid N(0, 1) (the values read by attention over the
+    selected blocks), from a generator of its own: seed + 7919."""
+    g = _gen(seed + 7919, device)
+    v = torch.randn(shape.B, shape.Hkv, shape.N, shape.d, generator=g,
+                    device=device, dtype=torch.float32)
+    return v.to(shape.torch_dtype)
+
+
 def planted(shape: Shape, seed: int, frac: float = 0.01, amp: float = 3.0,
             noise: float = 0.5, device: str = "cpu"):
     """iid N(0,1) keys, with a fraction `frac` of key positions j (uniform,
