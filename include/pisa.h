@@ -82,7 +82,8 @@ typedef enum { PISA_BF16 = 0, PISA_FP32 = 1 } pisa_dtype;
 typedef enum {
   PISA_MODE_PREFILL = 0,
   PISA_MODE_DECODE = 1,
-  PISA_MODE_FLAT = 2
+  PISA_MODE_FLAT = 2,
+  PISA_MODE_ATTEND = 3
 } pisa_mode;
 
 /* Device status codes written into the workspace status word. */
@@ -126,8 +127,8 @@ int64_t pisa_pyramid_nodes(const pisa_params* p);
 size_t pisa_pyramid_bytes(const pisa_params* p);
 
 /* Workspace bytes needed by pisa_select_prefill (PISA_MODE_PREFILL),
- * pisa_select_decode (PISA_MODE_DECODE) or pisa_select_flat
- * (PISA_MODE_FLAT); 0 on bad params. */
+ * pisa_select_decode (PISA_MODE_DECODE), pisa_select_flat (PISA_MODE_FLAT)
+ * or pisa_attend_prefill (PISA_MODE_ATTEND); 0 on bad params. */
 size_t pisa_workspace_bytes(const pisa_params* p, int32_t mode);
 
 /* Key pyramid (agihunt.info summary, pyramid paragraph; rcap.io, "Think of
@@ -229,6 +230,34 @@ pisa_status pisa_select_prefill_static(const pisa_params* p, const void* q,
                                        const void* k, const float* pyramid,
                                        int32_t* out_idx, float* out_score,
                                        void* stream);
+
+/* Block-sparse attention over a selection (agihunt.info summary, opening
+ * paragraph: each query reads only its selected tiles of C keys, so the
+ * attention pass is linear in N; rcap.io, "Selection walks the tree
+ * top-down": the kept leaf indices drive sparse attention over the original
+ * keys).  For query position t of key head h, each query head g of its GQA
+ * group (head h*G + g) gets
+ *   out[b, h*G+g, t] = sum_i softmax_i(s q . k_i) v_i
+ * over the key positions i <= t of the blocks listed in idx[b, h, t, :]
+ * (s: the score scale of the params, 1/sqrt(d) when 0).
+ *   q    bf16 [B, H_q, N, d];  k, v  bf16 [B, H_kv, N, d]  (DEVICE)
+ *   idx  int32 [B, H_kv, N, K+3] (DEVICE): block indices, e.g. the out_idx of
+ *        pisa_select_prefill or pisa_select_flat.  Entries outside [0, nb)
+ *        are empty slots; a block listed twice counts once; blocks after the
+ *        query's own block contribute nothing.
+ *   out  bf16 [B, H_q, N, d] (DEVICE).  A query with no key at or before t
+ *        in its blocks gets a zero row.
+ *   ws   at least pisa_workspace_bytes(p, PISA_MODE_ATTEND) bytes; it holds
+ *        one bf16 partial row per (query head, slot): about
+ *        2 * B * H_q * N * (K+3) * d bytes.
+ * dtype must be PISA_BF16 (PISA_ERR_UNSUPPORTED otherwise); q, k, v, out and
+ * ws 16-byte aligned, idx 4-byte aligned.  Inputs are assumed finite.  A
+ * bounded device wait that runs out sets PISA_DEV_TIMEOUT in the status
+ * word. */
+pisa_status pisa_attend_prefill(const pisa_params* p, const void* q,
+                                const void* k, const void* v,
+                                const int32_t* idx, void* ws, size_t ws_bytes,
+                                void* out, void* stream);
 
 /* Synchronises `stream`, then copies the workspace status word into
  * *device_code (PISA_DEV_*).  Returns PISA_ERR_DEVICE when it is non-zero. */

@@ -67,7 +67,7 @@ def lib():
                                      _i32p, _dp, _dp]
         L.po_select_flat.restype = ctypes.c_int
         L.po_sparse_attention.argtypes = [ctypes.POINTER(_Params), _dp, _dp, _dp, _i32p,
-                                          _i64, _i64p, _dp]
+                                          _i64, _i64p, ctypes.c_int, _dp]
         L.po_sparse_attention.restype = ctypes.c_int
         L.po_num_threads.restype = ctypes.c_int
         L.po_set_num_threads.argtypes = [ctypes.c_int]
@@ -199,10 +199,11 @@ class Oracle:
         return dict(idx=idx, score=score, margin=margin)
 
 
-    def attend(self, q, k, v, idx, sel=None) -> np.ndarray:
+    def attend(self, q, k, v, idx, sel=None, qrows: bool = False) -> np.ndarray:
         """Attention of the queries over their selected blocks (causal inside
         each block); idx is the full [B, Hkv, N, K+3] selection.  Returns
-        [nq, G, d] fp64 for the sel triples (b, h, t), or every query."""
+        [nq, G, d] fp64 for the sel triples (b, h, t), or every query.  With
+        qrows, q holds only the selected queries' head rows [nsel, G, d]."""
         q = _f64(q); k = _f64(k); v = _f64(v)
         idx = np.ascontiguousarray(np.asarray(idx, np.int32).reshape(-1))
         if idx.size != self.B * self.Hkv * self.N * (self.K + 3):
@@ -217,7 +218,8 @@ class Oracle:
         out = np.empty((nq, G, self.d), np.float64)
         rc = lib().po_sparse_attention(ctypes.byref(self.p), _ptr(q, _dp), _ptr(k, _dp), _ptr(v, _dp),
                                        _ptr(idx, _i32p), nq,
-                                       None if selp is None else _ptr(selp, _i64p), _ptr(out, _dp))
+                                       None if selp is None else _ptr(selp, _i64p), int(bool(qrows)),
+                                       _ptr(out, _dp))
         if rc != 0:
             raise ValueError("oracle attend: bad arguments or a query with no key")
         return out

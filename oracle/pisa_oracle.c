@@ -529,11 +529,12 @@ int po_select_flat(const po_params* p, const double* q, const double* pyr,
  * with s the score scale of the selection (1/sqrt(d) unless given).  A block
  * listed twice counts once.  q [B, Hq, N, d]; k, v [B, Hkv, N, d]; idx
  * [B, Hkv, N, K+3] int32 (-1 = empty slot); sel: nsel triples (b, h, t), or
- * NULL for every (b, h, t) in order.  out [nq, G, d] fp64.  Returns -1 on a
- * bad position or when some query has no attended key.                   */
+ * NULL for every (b, h, t) in order; qrows != 0 (with sel): q holds only the
+ * selected queries' head rows, [nsel, G, d].  out [nq, G, d] fp64.  Returns
+ * -1 on a bad position or when some query has no attended key.           */
 int po_sparse_attention(const po_params* p, const double* q, const double* k,
                         const double* v, const int32_t* idx, int64_t nsel,
-                        const int64_t* sel, double* out) {
+                        const int64_t* sel, int qrows, double* out) {
   const int W = p->K + 3;
   const int d = p->d;
   if (p->Hkv <= 0 || p->Hq % p->Hkv != 0 || p->K < 1 || p->C < 1 || d < 1)
@@ -542,6 +543,7 @@ int po_sparse_attention(const po_params* p, const double* q, const double* k,
   const double s = po_scale(p);
   const int64_t nq = sel ? nsel : p->B * p->Hkv * p->N;
   int err = 0;
+  if (qrows && !sel) return -1;
 #pragma omp parallel for schedule(dynamic, 16)
   for (int64_t i = 0; i < nq; ++i) {
     int64_t b, t;
@@ -581,7 +583,8 @@ int po_sparse_attention(const po_params* p, const double* q, const double* k,
     const double* kh = k + (b * p->Hkv + h) * p->N * d;
     const double* vh = v + (b * p->Hkv + h) * p->N * d;
     for (int32_t g = 0; g < G; ++g) {
-      const double* qr = q + ((b * p->Hq + (int64_t)h * G + g) * p->N + t) * d;
+      const double* qr = qrows ? q + (i * G + g) * d
+                               : q + ((b * p->Hq + (int64_t)h * G + g) * p->N + t) * d;
       double* o = out + (i * G + g) * d;
       double m = -INFINITY, l = 0.0;
       for (int64_t u = 0; u < nk; ++u) {

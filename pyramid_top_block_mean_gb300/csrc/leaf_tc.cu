@@ -65,8 +65,13 @@ struct LeafTcSmem {
 // ---------------------------------------------------------------- bucketing
 struct BucketArgs {
   int64_t nq, N, n2, nchunk;
-  int32_t K;
+  int32_t K;      // entries per query
+  int32_t shift;  // a pair is (t << shift) | slot, read as uint32
 };
+
+__device__ __forceinline__ int32_t encode_pair(const BucketArgs& a, int64_t t, int64_t slot) {
+  return (int32_t)(((uint32_t)t << a.shift) | (uint32_t)slot);
+}
 
 __device__ __forceinline__ int64_t bucket_of(const BucketArgs& a, int64_t qi, int32_t p) {
   const int64_t t = qi % a.N, bh = qi / a.N;
@@ -77,7 +82,7 @@ __global__ void count_kernel(BucketArgs a, const int32_t* __restrict__ kept2, in
   const int64_t n = a.nq * a.K;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t p = kept2[i];
-    if (p >= 0) atomicAdd(&counts[bucket_of(a, i / a.K, p)], 1);
+    if (p >= 0 && p < a.n2) atomicAdd(&counts[bucket_of(a, i / a.K, p)], 1);
   }
 }
 
@@ -99,7 +104,7 @@ __global__ void __launch_bounds__(512) count_smem_kernel(BucketArgs a, const int
   const int32_t* src = kept2 + (bh * a.N + t0) * K;
   for (int e = threadIdx.x; e < ne; e += blockDim.x) {
     const int32_t p = src[e];
-    if (p >= 0) atomicAdd(&hist[p], 1);
+    if (p >= 0 && p < n2) atomicAdd(&hist[p], 1);
   }
   __syncthreads();
   int32_t* dst = counts + (bh * a.nchunk + (t0 >> kChunkShift)) * a.n2;
@@ -119,7 +124,7 @@ __global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const i
   const int32_t* src = kept2 + (bh * a.N + t0) * K;
   for (int e = threadIdx.x; e < ne; e += blockDim.x) {
     const int32_t p = src[e];
-    if (p >= 0) atomicAdd(&hist[p], 1);
+    if (p >= 0 && p < n2) atomicAdd(&hist[p], 1);
   }
   __syncthreads();
   // reserve this CTA's range in every bucket it touches
@@ -131,9 +136,9 @@ __global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const i
   __syncthreads();
   for (int e = threadIdx.x; e < ne; e += blockDim.x) {
     const int32_t p = src[e];
-    if (p >= 0) {
+    if (p >= 0 && p < n2) {
       const int qn = e / K;
-      pairs[atomicAdd(&hist[p], 1)] = (int32_t)(((t0 + qn) << 5) | (e - qn * K));
+      pairs[atomicAdd(&hist[p], 1)] = encode_pair(a, t0 + qn, e - qn * K);
     }
   }
 }
@@ -210,11 +215,11 @@ __global__ void scatter_kernel(BucketArgs a, const int32_t* __restrict__ kept2, 
   const int64_t n = a.nq * a.K;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t p = kept2[i];
-    if (p < 0) continue;
+    if (p < 0 || p >= a.n2) continue;
     const int64_t qi = i / a.K;
     const int64_t bk = bucket_of(a, qi, p);
     const int32_t pos = offsets[bk] + atomicAdd(&cursor[bk], 1);
-    pairs[pos] = (int32_t)(((qi % a.N) << 5) | (i % a.K));
+    pairs[pos] = encode_pair(a, qi % a.N, i % a.K);
   }
 }
 
@@ -719,6 +724,37 @@ static cudaError_t launch_leaf_tc_t(const Prob& pr, const PrefillWs& w, char* ws
   return cudaGetLastError();
 }
 
+cudaError_t launch_buckets(const BucketJob& j, int num_sms, cudaStream_t st) {
+  BucketArgs a{j.nq, j.N, j.n2, j.nchunk, j.width, j.shift};
+  // counts, offsets and cursor are contiguous: clear all three at once
+  cudaError_t e = cudaMemsetAsync(j.counts, 0, j.clear_bytes, st);
+  if (e != cudaSuccess) return e;
+  const int64_t n = j.nq * j.width;
+  const unsigned g1 = (unsigned)std::min<int64_t>(ceil_div64(n, 256), (int64_t)num_sms * 16);
+  const bool smem_bins = j.n2 <= kSmemBins;
+  const dim3 gs((unsigned)ceil_div64(j.N, kQueriesPerCta), (unsigned)(j.nq / j.N));
+  const size_t hbytes = (size_t)j.n2 * sizeof(int32_t);
+  if (smem_bins) {
+    e = cudaFuncSetAttribute(count_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kSmemBins * 4));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(scatter_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)(kSmemBins * 4));
+    if (e != cudaSuccess) return e;
+  }
+  note_launch();
+  if (smem_bins) count_smem_kernel<<<gs, 512, hbytes, st>>>(a, j.lists, j.counts);
+  else count_kernel<<<g1, 256, 0, st>>>(a, j.lists, j.counts);
+  note_launch();
+  scan_kernel<<<1, 1024, 0, st>>>(j.nbuckets, j.Q, j.counts, j.offsets, j.tile_off);
+  note_launch();
+  if (smem_bins) scatter_smem_kernel<<<gs, 512, hbytes, st>>>(a, j.lists, j.offsets, j.cursor, j.pairs);
+  else scatter_kernel<<<g1, 256, 0, st>>>(a, j.lists, j.offsets, j.cursor, j.pairs);
+  const unsigned g2 = (unsigned)std::min<int64_t>(ceil_div64(j.nbuckets, 256), (int64_t)num_sms * 8);
+  note_launch();
+  tiles_kernel<<<g2, 256, 0, st>>>(j.nbuckets, j.n2, j.nchunk, j.Q, j.counts, j.offsets, j.tile_off, j.tile_info);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, char* ws, const void* q,
                            const void* k, int32_t* out_idx, float* out_score, int num_sms, cudaStream_t st) {
   const int64_t nq = pr.B * pr.Hkv * pr.N;
@@ -726,38 +762,18 @@ cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, cha
   cudaError_t e;
   if (w.nbuckets > 0) {
     const int32_t Q = kTileRows / pr.G;
-    BucketArgs a{nq, pr.N, w.n2, w.nchunk, pr.K};
-    int32_t* counts = (int32_t*)(ws + w.counts);
-    int32_t* offsets = (int32_t*)(ws + w.offsets);
-    int32_t* cursor = (int32_t*)(ws + w.cursor);
-    int32_t* tile_off = (int32_t*)(ws + w.tile_off);
-    // counts, offsets and cursor are contiguous: clear all three at once
-    e = cudaMemsetAsync(counts, 0, w.tile_off - w.counts, st);
-    if (e != cudaSuccess) return e;
-    const int64_t n = nq * pr.K;
-    const unsigned g1 = (unsigned)std::min<int64_t>(ceil_div64(n, 256), (int64_t)num_sms * 16);
-    const bool smem_bins = w.n2 <= kSmemBins;
-    const dim3 gs((unsigned)ceil_div64(pr.N, kQueriesPerCta), (unsigned)(pr.B * pr.Hkv));
-    const size_t hbytes = (size_t)w.n2 * sizeof(int32_t);
-    if (smem_bins) {
-      e = cudaFuncSetAttribute(count_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kSmemBins * 4));
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(scatter_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)(kSmemBins * 4));
-      if (e != cudaSuccess) return e;
-    }
-    note_launch();
-    if (smem_bins) count_smem_kernel<<<gs, 512, hbytes, st>>>(a, kept2, counts);
-    else count_kernel<<<g1, 256, 0, st>>>(a, kept2, counts);
-    note_launch();
-    scan_kernel<<<1, 1024, 0, st>>>(w.nbuckets, Q, counts, offsets, tile_off);
-    note_launch();
-    if (smem_bins) scatter_smem_kernel<<<gs, 512, hbytes, st>>>(a, kept2, offsets, cursor, (int32_t*)(ws + w.pairs));
-    else scatter_kernel<<<g1, 256, 0, st>>>(a, kept2, offsets, cursor, (int32_t*)(ws + w.pairs));
-    const unsigned g2 = (unsigned)std::min<int64_t>(ceil_div64(w.nbuckets, 256), (int64_t)num_sms * 8);
-    note_launch();
-    tiles_kernel<<<g2, 256, 0, st>>>(w.nbuckets, w.n2, w.nchunk, Q, counts, offsets, tile_off, (int4*)(ws + w.tile_info));
-    e = cudaGetLastError();
+    BucketJob j{};
+    j.lists = kept2;
+    j.nq = nq; j.N = pr.N; j.n2 = w.n2; j.nchunk = w.nchunk; j.nbuckets = w.nbuckets;
+    j.width = pr.K; j.shift = 5; j.Q = Q;
+    j.counts = (int32_t*)(ws + w.counts);
+    j.offsets = (int32_t*)(ws + w.offsets);
+    j.cursor = (int32_t*)(ws + w.cursor);
+    j.tile_off = (int32_t*)(ws + w.tile_off);
+    j.pairs = (int32_t*)(ws + w.pairs);
+    j.tile_info = (int4*)(ws + w.tile_info);
+    j.clear_bytes = w.tile_off - w.counts;
+    e = launch_buckets(j, num_sms, st);
     if (e != cudaSuccess) return e;
     CUtensorMap kmap;
     if (!make_tmap_rows(&kmap, k, pr.B * pr.Hkv * pr.N, pr.d, kTileKeys)) return cudaErrorInvalidValue;

@@ -61,6 +61,27 @@ PrefillWs prefill_ws_layout(const Prob& pr, const Pyr& s) {
   return w;
 }
 
+AttendWs attend_ws_layout(const Prob& pr, const Pyr& s) {
+  AttendWs w{};
+  const int64_t nq = pr.B * pr.Hkv * pr.N;
+  const int64_t W = pr.K + 3;
+  w.nchunk = ceil_div64(pr.N, (int64_t)1 << kChunkShift);
+  w.nbuckets = pr.B * pr.Hkv * w.nchunk * s.nb;
+  w.max_tiles = w.nbuckets + ceil_div64(nq * W, 128 / 8);
+  size_t o = 0;
+  w.status = o; o += 256;
+  w.counts = o; o = align_up(o + (size_t)(w.nbuckets + 1) * 4, 256);
+  w.offsets = o; o = align_up(o + (size_t)(w.nbuckets + 1) * 4, 256);
+  w.cursor = o; o = align_up(o + (size_t)(w.nbuckets + 1) * 4, 256);
+  w.tile_off = o; o = align_up(o + (size_t)(w.nbuckets + 1) * 4, 256);
+  w.pairs = o; o = align_up(o + (size_t)nq * W * 4, 256);
+  w.tile_info = o; o = align_up(o + (size_t)w.max_tiles * 16, 256);
+  w.part_lse = o; o = align_up(o + (size_t)nq * W * pr.G * 4, 256);
+  w.part_o = o; o = align_up(o + (size_t)nq * W * pr.G * pr.d * 2, 256);
+  w.total = o;
+  return w;
+}
+
 size_t decode_ws_bytes(const Prob&, const Pyr&) { return 256; }
 
 size_t flat_ws_bytes(const Prob& pr, const Pyr& s) {
@@ -158,6 +179,7 @@ size_t pisa_workspace_bytes(const pisa_params* p, int32_t mode) {
     case PISA_MODE_PREFILL: return prefill_ws_layout(pr, s).total;
     case PISA_MODE_DECODE: return decode_ws_bytes(pr, s);
     case PISA_MODE_FLAT: return flat_ws_bytes(pr, s);
+    case PISA_MODE_ATTEND: return attend_ws_layout(pr, s).total;
   }
   return 0;
 }
@@ -285,6 +307,28 @@ pisa_status pisa_select_flat(const pisa_params* p, const void* q, const float* p
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PISA_ERR_CUDA;
   return cuda_status(launch_flat(pr, s, q, pyramid, (char*)ws, out_idx, out_score, sm_count(dev), st));
+}
+
+pisa_status pisa_attend_prefill(const pisa_params* p, const void* q, const void* k, const void* v,
+                                const int32_t* idx, void* ws, size_t ws_bytes, void* out, void* stream) {
+  Prob pr; Pyr s;
+  pisa_status rc = check_params(p, &pr, &s);
+  if (rc != PISA_OK) return rc;
+  if (pr.B * pr.Hkv * pr.N == 0) return PISA_OK;
+  if (pr.dtype != PISA_BF16) return PISA_ERR_UNSUPPORTED;  // built for bf16 inputs
+  if (!q || !k || !v || !idx || !ws || !out) return PISA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(ws) || !aligned16(out) ||
+      ((uintptr_t)idx & 3u))
+    return PISA_ERR_MISALIGNED;
+  const AttendWs w = attend_ws_layout(pr, s);
+  if (ws_bytes < w.total) return PISA_ERR_WORKSPACE;
+  // pair counts, tile indices and TMA row coordinates are 32-bit
+  if (pr.B * pr.Hkv * pr.N * (pr.K + 3) >= ((int64_t)1 << 31)) return PISA_ERR_UNSUPPORTED;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return PISA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PISA_ERR_CUDA;
+  return cuda_status(launch_attend(pr, s, w, (char*)ws, q, k, v, idx, out, sm_count(dev), st));
 }
 
 pisa_status pisa_read_device_status(const void* ws, int32_t* device_code, void* stream) {

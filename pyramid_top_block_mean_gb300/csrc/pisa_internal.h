@@ -34,8 +34,40 @@ struct PrefillWs {
   int64_t max_tiles;  // nbuckets + B * Hkv * N * K / Q, Q the smallest tile
 };
 
+// Counting sort of (query, entry) pairs into buckets (sequence, key head,
+// query chunk, node) and the tile list over them (leaf_tc.cu).  lists holds
+// `width` entries per query (negative or >= n2: none); a pair is stored as
+// (t << shift) | slot; tiles hold at most Q pairs.
+struct BucketJob {
+  const int32_t* lists;
+  int64_t nq, N, n2, nchunk, nbuckets;
+  int32_t width, shift, Q;
+  int32_t *counts, *offsets, *cursor, *tile_off, *pairs;
+  int4* tile_info;
+  size_t clear_bytes;  // bytes from counts to the end of cursor
+};
+cudaError_t launch_buckets(const BucketJob& j, int num_sms, cudaStream_t st);
+
+// Workspace layout of pisa_attend_prefill.
+struct AttendWs {
+  size_t status;      // int32 status word (first 256 bytes)
+  size_t counts;      // int32 [nbuckets + 1] pairs per (bucket, block)
+  size_t offsets;     // int32 [nbuckets + 1]
+  size_t cursor;      // int32 [nbuckets + 1]
+  size_t tile_off;    // int32 [nbuckets + 1]
+  size_t pairs;       // int32 [B * Hkv * N * (K+3)] (t << 6 | slot) grouped by bucket
+  size_t tile_info;   // int4  [max_tiles]
+  size_t part_lse;    // fp32 [B, Hkv, N, K+3, G] log2-sum-exp2 of each block's scores
+  size_t part_o;      // bf16 [B, Hkv, N, K+3, G, d] softmax-weighted values of each block
+  size_t total;
+  int64_t nbuckets;   // B * Hkv * nchunk * nb
+  int64_t nchunk;
+  int64_t max_tiles;
+};
+
 bool make_pyr(int64_t N, int32_t C, Pyr* s);
 PrefillWs prefill_ws_layout(const Prob& pr, const Pyr& s);
+AttendWs attend_ws_layout(const Prob& pr, const Pyr& s);
 size_t decode_ws_bytes(const Prob& pr, const Pyr& s);
 size_t flat_ws_bytes(const Prob& pr, const Pyr& s);
 
@@ -62,6 +94,8 @@ cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, cha
 cudaError_t launch_decode(const Prob& pr, const Pyr& s, const void* q, const void* kc, const int32_t* seq_lens,
                           float* pyr, int32_t* status, int32_t* out_idx, float* out_score, int32_t* trace,
                           cudaStream_t st);
+cudaError_t launch_attend(const Prob& pr, const Pyr& s, const AttendWs& w, char* ws, const void* q, const void* k,
+                          const void* v, const int32_t* idx, void* out, int num_sms, cudaStream_t st);
 cudaError_t launch_flat(const Prob& pr, const Pyr& s, const void* q, const float* pyr, char* ws,
                         int32_t* out_idx, float* out_score, int num_sms, cudaStream_t st);
 

@@ -28,13 +28,14 @@ STATUS_NAMES = {0: "PISA_OK", -1: "PISA_ERR_INVALID_ARG", -2: "PISA_ERR_UNSUPPOR
                 -3: "PISA_ERR_MISALIGNED", -4: "PISA_ERR_WORKSPACE", -5: "PISA_ERR_CUDA",
                 -6: "PISA_ERR_DEVICE"}
 BF16, FP32 = 0, 1
-MODE_PREFILL, MODE_DECODE, MODE_FLAT = 0, 1, 2
+MODE_PREFILL, MODE_DECODE, MODE_FLAT, MODE_ATTEND = 0, 1, 2, 3
 DEV_OK, DEV_BAD_SEQ_LEN, DEV_TIMEOUT, DEV_BAD_INDEX = 0, 1, 2, 3
 
 EXPORTED = ["pisa_abi_version", "pisa_status_string", "pisa_pyramid_levels", "pisa_pyramid_nodes",
             "pisa_pyramid_bytes", "pisa_workspace_bytes", "pisa_build_pyramid", "pisa_select_prefill",
             "pisa_prefill_route", "pisa_prefill_leaves", "pisa_select_decode", "pisa_select_flat",
-            "pisa_read_device_status", "pisa_select_prefill_static", "pisa_kernel_launches"]
+            "pisa_read_device_status", "pisa_select_prefill_static", "pisa_kernel_launches",
+            "pisa_attend_prefill"]
 
 
 class Params(ctypes.Structure):
@@ -71,6 +72,8 @@ _lib.pisa_select_decode.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t
 _lib.pisa_select_decode.restype = ctypes.c_int
 _lib.pisa_select_flat.argtypes = [_P, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
 _lib.pisa_select_flat.restype = ctypes.c_int
+_lib.pisa_attend_prefill.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
+_lib.pisa_attend_prefill.restype = ctypes.c_int
 _lib.pisa_read_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32), _vp]
 _lib.pisa_read_device_status.restype = ctypes.c_int
 
@@ -192,6 +195,15 @@ def select_flat(p: Params, q, pyramid, ws, out_idx, out_score=None, stream=None,
     return rc
 
 
+def attend_prefill(p: Params, q, k, v, idx, ws, out, stream=None, check: bool = True) -> int:
+    rc = _lib.pisa_attend_prefill(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(ws),
+                                  0 if ws is None else ws.numel() * ws.element_size(), _ptr(out),
+                                  _stream(stream))
+    if check:
+        _check(rc, "pisa_attend_prefill")
+    return rc
+
+
 def read_device_status(ws: torch.Tensor, stream=None) -> int:
     code = ctypes.c_int32(0)
     rc = _lib.pisa_read_device_status(_ptr(ws), ctypes.byref(code), _stream(stream))
@@ -239,6 +251,24 @@ class Selector:
             build_pyramid(self.p, k, self.pyramid, None, stream)
         select_flat(self.p, q, self.pyramid, self.ws, self.out_idx, self.out_score, stream)
         return self.out_idx, self.out_score
+
+    def device_status(self, stream=None) -> int:
+        return read_device_status(self.ws, stream)
+
+
+class Attention:
+    """Owns the workspace and output of block-sparse attention over a
+    selection (pisa_attend_prefill) for one problem shape."""
+
+    def __init__(self, p: Params, device="cuda"):
+        self.p = p
+        self.device = torch.device(device)
+        self.ws = torch.empty(max(workspace_bytes(p, MODE_ATTEND), 256), dtype=torch.uint8, device=self.device)
+        self.out = torch.empty(p.B, p.H_q, p.N, p.d, dtype=torch.bfloat16, device=self.device)
+
+    def __call__(self, q, k, v, idx, stream=None):
+        attend_prefill(self.p, q, k, v, idx, self.ws, self.out, stream)
+        return self.out
 
     def device_status(self, stream=None) -> int:
         return read_device_status(self.ws, stream)

@@ -170,3 +170,7 @@ def test_selected_queries_match_full_run():
     part = O.attend(q, k, v, idx, sel)
     for i, (b, h, t) in enumerate(sel):
         np.testing.assert_array_equal(part[i], full[(b * Hkv + h) * N + t])
+    # the same queries with only their head rows passed
+    G = Hq // Hkv
+    rows = np.stack([q.numpy()[b, h * G:(h + 1) * G, t] for (b, h, t) in sel])
+    np.testing.assert_array_equal(O.attend(rows, k, v, idx, sel, qrows=True), part)
