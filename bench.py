@@ -398,6 +398,72 @@ def run_pisa(args, ws, rank, local):
     return line
 
 
+def attention_work(s, idx):
+    """Algorithmic work of attention over a selection: 4 d flops per (query
+    head, attended key) (the q.k dot and the p v update); bytes = q, k, v and
+    the output read or written once, plus the index rows.  Attended keys
+    come from the selection: 64 per listed block before the query's own
+    block, t mod 64 + 1 in its own block."""
+    import torch
+    t = torch.arange(s.N, device=idx.device)
+    qb = (t // s.C).view(1, 1, -1, 1)
+    own = (t % s.C + 1).view(1, 1, -1, 1)
+    keys = torch.where((idx < 0) | (idx > qb), torch.zeros_like(idx),
+                       torch.where(idx < qb, torch.full_like(idx, s.C), own))
+    n_keys = int(keys.sum().item())  # per (sequence, key head, position): the G heads share it
+    flops = 4.0 * s.d * n_keys * s.G
+    bytes_ = (s.B * s.Hq * s.N * s.d * 2) * 2 + 2 * (s.B * s.Hkv * s.N * s.d * 2) + idx.numel() * 4
+    return flops, bytes_, n_keys
+
+
+def attention_measurements(dev, st, tm):
+    """Block-sparse attention over the PISA selection at 64K-256K tokens
+    (pisa_attend_prefill), the selection + attention total, and PyTorch's
+    dense causal scaled_dot_product_attention (the full attention it
+    replaces) on the same q, k, v; each timed with CUDA events."""
+    import torch
+    from pyramid_top_block_mean_gb300 import pisa
+    from pyramid_top_block_mean_gb300 import workloads as W
+
+    pk = peaks()
+    res = {}
+    for N in (65536, 131072, 262144):
+        s = W.sweep(N)
+        g = torch.Generator(device=dev)
+        g.manual_seed(11 + N)
+        q = torch.randn(s.B, s.Hq, s.N, s.d, device=dev, generator=g).to(torch.bfloat16)
+        k = torch.randn(s.B, s.Hkv, s.N, s.d, device=dev, generator=g).to(torch.bfloat16)
+        v = torch.randn(s.B, s.Hkv, s.N, s.d, device=dev, generator=g).to(torch.bfloat16)
+        p = pisa.params_from_shape(s)
+        sel = pisa.Selector(p, device=dev, with_scores=False)
+        at = pisa.Attention(p, device=dev)
+        with torch.cuda.stream(st):
+            idx, _ = sel.prefill(q, k, stream=st)
+        torch.cuda.synchronize(dev)
+        t_at = tm(lambda: at(q, k, v, idx, stream=st), 5)
+        t_both = tm(lambda: (sel.prefill(q, k, stream=st), at(q, k, v, idx, stream=st)), 5)
+        flops, bytes_, n_keys = attention_work(s, idx)
+        kk = k.repeat_interleave(s.G, 1)
+        vv = v.repeat_interleave(s.G, 1)
+
+        def dense():
+            with torch.cuda.stream(st):
+                torch.nn.functional.scaled_dot_product_attention(q, kk, vv, is_causal=True)
+        t_dense = tm(dense, 2)
+        t_roof = max(bytes_ / (pk["hbm"] * 1e9), flops / ((pk["bf16_sus"] or pk["bf16"]) * 1e12)) * 1e3
+        res[str(N)] = {"attend_ms": t_at, "select_plus_attend_ms": t_both, "dense_sdpa_ms": t_dense,
+                       "dense_over_sparse": t_dense / t_both, "attended_keys_per_query": n_keys / (s.B * s.Hkv * s.N),
+                       "roofline": {"t_roof_ms": t_roof, "frac": t_roof / t_at, "flops": flops, "bytes": bytes_,
+                                    "bound": "tensor" if flops / (pk["bf16_sus"] or pk["bf16"]) / 1e12 >
+                                    bytes_ / pk["hbm"] / 1e9 else "hbm",
+                                    "partial_bytes": 2 * s.B * s.Hq * s.N * (s.K + 3) * (s.d * 2 + 4)}}
+        del q, k, v, kk, vv, sel, at, idx
+        torch.cuda.empty_cache()
+    res["workload"] = ("B=1, Hq=16 Hkv=4 d=128 K=8 bf16; v iid N(0,1); dense = torch SDPA causal "
+                       "(flash) with k, v repeated over the GQA group")
+    return res
+
+
 def side_measurements(args, dev, st, rank):
     """Sweep points, the flat comparator and the decode step (not the
     headline; each timed with CUDA events after warm-up)."""
@@ -419,6 +485,7 @@ def side_measurements(args, dev, st, rank):
         return a.elapsed_time(b) / reps
 
     sweep = {}
+    attention = attention_measurements(dev, st, tm)
     for N in (65536, 131072, 262144):
         s = W.sweep(N)
         g = torch.Generator(device=dev)
@@ -475,7 +542,7 @@ def side_measurements(args, dev, st, rank):
     pk = peaks()
     del kc
     torch.cuda.empty_cache()
-    return {"sweep": sweep, "decode": {"us_per_step": us, "steps": W.DECODE_STEPS,
+    return {"sweep": sweep, "attention": attention, "decode": {"us_per_step": us, "steps": W.DECODE_STEPS,
                                        "workload": "B=64, 131072 cached keys, Hq=32 Hkv=8 d=128 bf16 K=32",
                                        "leaf_key_bytes_per_step": leaf_bytes,
                                        "leaf_key_GBps": leaf_bytes / (us * 1e-6) / 1e9,

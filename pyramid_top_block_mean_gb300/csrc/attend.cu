@@ -364,31 +364,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_after();
       const float inv = any ? 1.0f / l : 0.0f;
       const int64_t bh = info.x;
-      uint16_t* dst = part_o + ((((bh * pr.N + t) * W + slot) * G + g) * D);
+      // this row's partial; the rows are written four at a time below
+      uint16_t* dst = valid ? part_o + ((((bh * pr.N + t) * W + slot) * G + g) * D) : nullptr;
+      const uint32_t srow = ptx::smem_u32(sm.p[grp]) + (q4 * 32) * 128;
 #pragma unroll
       for (int half = 0; half < D / 64; ++half) {
-        uint32_t v0[32], v1[32];
-        ptx::tmem_ld32(lane_base + 128 + grp * D + half * 64, v0);
-        ptx::tmem_ld32(lane_base + 128 + grp * D + half * 64 + 32, v1);
-        ptx::tmem_ld_wait();
-        if (half == D / 64 - 1) {
-          ptx::tc_fence_before();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[grp]));
-        }
-        if (valid) {
-          uint32_t pk[32];
+        if (half > 0) __syncwarp();  // the previous half has been read back
+        // stage the 64 bf16 of this half in this warp's 32 rows of the P
+        // tile (free: the O MMA that read it has completed), swizzled so the
+        // 16-byte writes of 8 consecutive rows hit distinct banks
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            pk[j] = pack_bf16(__uint_as_float(v0[2 * j]) * inv, __uint_as_float(v0[2 * j + 1]) * inv);
-            pk[16 + j] = pack_bf16(__uint_as_float(v1[2 * j]) * inv, __uint_as_float(v1[2 * j + 1]) * inv);
+        for (int piece = 0; piece < 2; ++piece) {
+          uint32_t v0[32];
+          ptx::tmem_ld32(lane_base + 128 + grp * D + half * 64 + piece * 32, v0);
+          ptx::tmem_ld_wait();
+          if (half == D / 64 - 1 && piece == 1) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[grp]));
           }
-          uint4* o4 = reinterpret_cast<uint4*>(dst + half * 64);
+          uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) o4[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          for (int j = 0; j < 16; ++j)
+            pk[j] = pack_bf16(__uint_as_float(v0[2 * j]) * inv, __uint_as_float(v0[2 * j + 1]) * inv);
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int c = piece * 4 + c4;
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(srow + lane * 128 + ((c ^ (lane & 7)) << 4)),
+                         "r"(pk[4 * c4]), "r"(pk[4 * c4 + 1]), "r"(pk[4 * c4 + 2]), "r"(pk[4 * c4 + 3])
+                         : "memory");
+          }
+        }
+        __syncwarp();
+        // read back four rows per instruction (eight lanes per 128-byte row)
+        // and store full 128-byte lines
+        const int c = lane & 7;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int rr = 4 * k + (lane >> 3);
+          const uint64_t dp = __shfl_sync(0xffffffffu, reinterpret_cast<uint64_t>(dst), rr);
+          uint32_t a0, a1, a2, a3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                       : "r"(srow + rr * 128 + ((c ^ (rr & 7)) << 4))
+                       : "memory");
+          if (dp) reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(dp) + half * 64)[c] = make_uint4(a0, a1, a2, a3);
         }
       }
       if (valid) part_lse[((bh * pr.N + t) * W + slot) * G + g] = any ? m + ptx::lg2(l) : -INFINITY;
+      __syncwarp();  // the staged rows are read before the next tile's P overwrites them
     }
   }
 
@@ -400,12 +424,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // One thread per (query, head, 8 output dims): merges the query head's block
-// partials with weights exp2(lse_b - max_b lse_b).  A block listed twice in a
-// query's row counts once; entries outside [0, nb) are empty.  A query with
-// no attended key gets zeros.
-template <int D>
-__global__ void __launch_bounds__(256) attend_combine_kernel(Prob pr, int64_t nb, const int32_t* __restrict__ idx,
-                                                              const float* __restrict__ part_lse,
+// partials with weights exp2(lse_b - max_b lse_b).  The bucketing dropped
+// empty, out-of-range and repeated slots, whose lse keeps the NaN fill of
+// the workspace; slots whose block held no key at or before t have lse =
+// -inf.  Both are skipped, so no index row is read and every load of a
+// query head's partials is issued at once (BATCH slots in flight; a running
+// maximum when the row is longer).  A query with no attended key gets zeros.
+template <int D, int BATCH>
+__global__ void __launch_bounds__(256) attend_combine_kernel(Prob pr, const float* __restrict__ part_lse,
                                                               const uint16_t* __restrict__ part_o,
                                                               uint16_t* __restrict__ out) {
   constexpr int CH = D / 8;
@@ -416,28 +442,35 @@ __global__ void __launch_bounds__(256) attend_combine_kernel(Prob pr, int64_t nb
     const int64_t rg = i / CH;
     const int g = (int)(rg % G);
     const int64_t qi = rg / G;  // (b * Hkv + h) * N + t
-    const int32_t* row = idx + qi * W;
-    uint64_t use = 0;  // slots that hold a new block
-    float m = -INFINITY;
-    for (int s = 0; s < W; ++s) {
-      const int32_t j = row[s];
-      if (j < 0 || j >= nb) continue;
-      bool dup = false;
-      for (int u = 0; u < s; ++u) dup |= row[u] == j;
-      if (dup) continue;
-      use |= 1ull << s;
-      m = fmaxf(m, part_lse[(qi * W + s) * G + g]);
-    }
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, l = 0.0f;
-    if (m > -INFINITY) {
-      for (int s = 0; s < W; ++s) {
-        if (!((use >> s) & 1ull)) continue;
-        const float lse = part_lse[(qi * W + s) * G + g];
-        if (lse == -INFINITY) continue;
-        const float w = ptx::ex2(lse - m);
+    const float* lrow = part_lse + qi * W * G + g;
+    const uint16_t* orow = part_o + (qi * W * G + g) * D + ch * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, l = 0.0f, m = -INFINITY;
+    for (int s0 = 0; s0 < W; s0 += BATCH) {
+      float ls[BATCH];
+      uint4 v[BATCH];
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        const int s = s0 + u;
+        ls[u] = s < W ? lrow[(int64_t)s * G] : -INFINITY;
+        v[u] = s < W ? *reinterpret_cast<const uint4*>(orow + (int64_t)s * G * D) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      float bm = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u)
+        if (ls[u] > bm) bm = ls[u];  // NaN (empty slot) never wins
+      if (bm > m) {
+        const float f = m == -INFINITY ? 0.0f : ptx::ex2(m - bm);
+        l *= f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[j] *= f;
+        m = bm;
+      }
+#pragma unroll
+      for (int u = 0; u < BATCH; ++u) {
+        if (!(ls[u] > -INFINITY)) continue;  // empty (NaN) or keyless (-inf)
+        const float w = ptx::ex2(ls[u] - m);
         l += w;
-        const uint4 v = *reinterpret_cast<const uint4*>(part_o + ((qi * W + s) * G + g) * D + ch * 8);
-        const uint32_t u4[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t u4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           acc[2 * j] = fmaf(w, __uint_as_float(u4[j] << 16), acc[2 * j]);
@@ -482,7 +515,7 @@ cudaError_t launch_attend(const Prob& pr, const Pyr& s, const AttendWs& w, char*
     BucketJob j{};
     j.lists = idx;
     j.nq = nq; j.N = pr.N; j.n2 = s.nb; j.nchunk = w.nchunk; j.nbuckets = w.nbuckets;
-    j.width = pr.K + 3; j.shift = kPairShift; j.Q = kRows / pr.G;
+    j.width = pr.K + 3; j.shift = kPairShift; j.dedup = 1; j.Q = kRows / pr.G;
     j.counts = (int32_t*)(ws + w.counts);
     j.offsets = (int32_t*)(ws + w.offsets);
     j.cursor = (int32_t*)(ws + w.cursor);
@@ -491,6 +524,9 @@ cudaError_t launch_attend(const Prob& pr, const Pyr& s, const AttendWs& w, char*
     j.tile_info = (int4*)(ws + w.tile_info);
     j.clear_bytes = w.tile_off - w.counts;
     e = launch_buckets(j, num_sms, st);
+    if (e != cudaSuccess) return e;
+    // slots the kernel does not write keep a NaN lse: the combine skips them
+    e = cudaMemsetAsync(ws + w.part_lse, 0xFF, (size_t)nq * (pr.K + 3) * pr.G * sizeof(float), st);
     if (e != cudaSuccess) return e;
     CUtensorMap kmap, vmap;
     if (!make_tmap_rows(&kmap, k, nq, pr.d, kKeys) || !make_tmap_rows(&vmap, v, nq, pr.d, kKeys))
@@ -506,13 +542,18 @@ cudaError_t launch_attend(const Prob& pr, const Pyr& s, const AttendWs& w, char*
   }
   const int64_t threads = nq * pr.G * (pr.d / 8);
   const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div64(threads, 256), (int64_t)num_sms * 64);
+  const float* pl = (const float*)(ws + w.part_lse);
+  const uint16_t* po = (const uint16_t*)(ws + w.part_o);
+  uint16_t* o = (uint16_t*)out;
   note_launch();
-  if (pr.d == 128)
-    attend_combine_kernel<128><<<blocks, 256, 0, st>>>(pr, s.nb, idx, (const float*)(ws + w.part_lse),
-                                                       (const uint16_t*)(ws + w.part_o), (uint16_t*)out);
-  else
-    attend_combine_kernel<64><<<blocks, 256, 0, st>>>(pr, s.nb, idx, (const float*)(ws + w.part_lse),
-                                                      (const uint16_t*)(ws + w.part_o), (uint16_t*)out);
+  const bool short_row = pr.K + 3 <= 12;
+  if (pr.d == 128) {
+    if (short_row) attend_combine_kernel<128, 12><<<blocks, 256, 0, st>>>(pr, pl, po, o);
+    else attend_combine_kernel<128, 20><<<blocks, 256, 0, st>>>(pr, pl, po, o);
+  } else {
+    if (short_row) attend_combine_kernel<64, 12><<<blocks, 256, 0, st>>>(pr, pl, po, o);
+    else attend_combine_kernel<64, 20><<<blocks, 256, 0, st>>>(pr, pl, po, o);
+  }
   return cudaGetLastError();
 }
 

@@ -67,7 +67,20 @@ struct BucketArgs {
   int64_t nq, N, n2, nchunk;
   int32_t K;      // entries per query
   int32_t shift;  // a pair is (t << shift) | slot, read as uint32
+  int32_t dedup;  // skip an entry equal to an earlier one of its query
 };
+
+// Does entry e of a flat [.., K] list count: in [0, n2) and, with dedup, not
+// equal to an earlier entry of the same query?
+__device__ __forceinline__ bool entry_counts(const BucketArgs& a, const int32_t* list, int64_t e, int32_t p) {
+  if (p < 0 || p >= a.n2) return false;
+  if (a.dedup) {
+    const int64_t e0 = e - e % a.K;
+    for (int64_t u = e0; u < e; ++u)
+      if (list[u] == p) return false;
+  }
+  return true;
+}
 
 __device__ __forceinline__ int32_t encode_pair(const BucketArgs& a, int64_t t, int64_t slot) {
   return (int32_t)(((uint32_t)t << a.shift) | (uint32_t)slot);
@@ -82,7 +95,7 @@ __global__ void count_kernel(BucketArgs a, const int32_t* __restrict__ kept2, in
   const int64_t n = a.nq * a.K;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t p = kept2[i];
-    if (p >= 0 && p < a.n2) atomicAdd(&counts[bucket_of(a, i / a.K, p)], 1);
+    if (entry_counts(a, kept2, i, p)) atomicAdd(&counts[bucket_of(a, i / a.K, p)], 1);
   }
 }
 
@@ -104,7 +117,7 @@ __global__ void __launch_bounds__(512) count_smem_kernel(BucketArgs a, const int
   const int32_t* src = kept2 + (bh * a.N + t0) * K;
   for (int e = threadIdx.x; e < ne; e += blockDim.x) {
     const int32_t p = src[e];
-    if (p >= 0 && p < n2) atomicAdd(&hist[p], 1);
+    if (entry_counts(a, src, e, p)) atomicAdd(&hist[p], 1);
   }
   __syncthreads();
   int32_t* dst = counts + (bh * a.nchunk + (t0 >> kChunkShift)) * a.n2;
@@ -124,7 +137,7 @@ __global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const i
   const int32_t* src = kept2 + (bh * a.N + t0) * K;
   for (int e = threadIdx.x; e < ne; e += blockDim.x) {
     const int32_t p = src[e];
-    if (p >= 0 && p < n2) atomicAdd(&hist[p], 1);
+    if (entry_counts(a, src, e, p)) atomicAdd(&hist[p], 1);
   }
   __syncthreads();
   // reserve this CTA's range in every bucket it touches
@@ -136,7 +149,7 @@ __global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const i
   __syncthreads();
   for (int e = threadIdx.x; e < ne; e += blockDim.x) {
     const int32_t p = src[e];
-    if (p >= 0 && p < n2) {
+    if (entry_counts(a, src, e, p)) {
       const int qn = e / K;
       pairs[atomicAdd(&hist[p], 1)] = encode_pair(a, t0 + qn, e - qn * K);
     }
@@ -215,7 +228,7 @@ __global__ void scatter_kernel(BucketArgs a, const int32_t* __restrict__ kept2, 
   const int64_t n = a.nq * a.K;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t p = kept2[i];
-    if (p < 0 || p >= a.n2) continue;
+    if (!entry_counts(a, kept2, i, p)) continue;
     const int64_t qi = i / a.K;
     const int64_t bk = bucket_of(a, qi, p);
     const int32_t pos = offsets[bk] + atomicAdd(&cursor[bk], 1);
@@ -725,7 +738,7 @@ static cudaError_t launch_leaf_tc_t(const Prob& pr, const PrefillWs& w, char* ws
 }
 
 cudaError_t launch_buckets(const BucketJob& j, int num_sms, cudaStream_t st) {
-  BucketArgs a{j.nq, j.N, j.n2, j.nchunk, j.width, j.shift};
+  BucketArgs a{j.nq, j.N, j.n2, j.nchunk, j.width, j.shift, j.dedup};
   // counts, offsets and cursor are contiguous: clear all three at once
   cudaError_t e = cudaMemsetAsync(j.counts, 0, j.clear_bytes, st);
   if (e != cudaSuccess) return e;

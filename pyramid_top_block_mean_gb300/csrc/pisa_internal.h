@@ -36,12 +36,13 @@ struct PrefillWs {
 
 // Counting sort of (query, entry) pairs into buckets (sequence, key head,
 // query chunk, node) and the tile list over them (leaf_tc.cu).  lists holds
-// `width` entries per query (negative or >= n2: none); a pair is stored as
+// `width` entries per query (negative or >= n2: none; with dedup, an entry
+// equal to an earlier one of its query is dropped too); a pair is stored as
 // (t << shift) | slot; tiles hold at most Q pairs.
 struct BucketJob {
   const int32_t* lists;
   int64_t nq, N, n2, nchunk, nbuckets;
-  int32_t width, shift, Q;
+  int32_t width, shift, dedup, Q;
   int32_t *counts, *offsets, *cursor, *tile_off, *pairs;
   int4* tile_info;
   size_t clear_bytes;  // bytes from counts to the end of cursor
