@@ -70,15 +70,13 @@ struct BucketArgs {
   int32_t dedup;  // skip an entry equal to an earlier one of its query
 };
 
-// Does entry e of a flat [.., K] list count: in [0, n2) and, with dedup, not
-// equal to an earlier entry of the same query?
-__device__ __forceinline__ bool entry_counts(const BucketArgs& a, const int32_t* list, int64_t e, int32_t p) {
+// Does entry `slot` of a query's row count: in [0, n2) and, with dedup, not
+// equal to an earlier entry of the row?
+__device__ __forceinline__ bool entry_counts(const BucketArgs& a, const int32_t* row, int slot, int32_t p) {
   if (p < 0 || p >= a.n2) return false;
-  if (a.dedup) {
-    const int64_t e0 = e - e % a.K;
-    for (int64_t u = e0; u < e; ++u)
-      if (list[u] == p) return false;
-  }
+  if (a.dedup)
+    for (int u = 0; u < slot; ++u)
+      if (row[u] == p) return false;
   return true;
 }
 
@@ -95,7 +93,9 @@ __global__ void count_kernel(BucketArgs a, const int32_t* __restrict__ kept2, in
   const int64_t n = a.nq * a.K;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t p = kept2[i];
-    if (entry_counts(a, kept2, i, p)) atomicAdd(&counts[bucket_of(a, i / a.K, p)], 1);
+    const int64_t qi = i / a.K;
+    const int slot = (int)(i - qi * a.K);
+    if (entry_counts(a, kept2 + qi * a.K, slot, p)) atomicAdd(&counts[bucket_of(a, qi, p)], 1);
   }
 }
 
@@ -117,7 +117,8 @@ __global__ void __launch_bounds__(512) count_smem_kernel(BucketArgs a, const int
   const int32_t* src = kept2 + (bh * a.N + t0) * K;
   for (int e = threadIdx.x; e < ne; e += blockDim.x) {
     const int32_t p = src[e];
-    if (entry_counts(a, src, e, p)) atomicAdd(&hist[p], 1);
+    const int qn = e / K;
+    if (entry_counts(a, src + qn * K, e - qn * K, p)) atomicAdd(&hist[p], 1);
   }
   __syncthreads();
   int32_t* dst = counts + (bh * a.nchunk + (t0 >> kChunkShift)) * a.n2;
@@ -137,7 +138,8 @@ __global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const i
   const int32_t* src = kept2 + (bh * a.N + t0) * K;
   for (int e = threadIdx.x; e < ne; e += blockDim.x) {
     const int32_t p = src[e];
-    if (entry_counts(a, src, e, p)) atomicAdd(&hist[p], 1);
+    const int qn = e / K;
+    if (entry_counts(a, src + qn * K, e - qn * K, p)) atomicAdd(&hist[p], 1);
   }
   __syncthreads();
   // reserve this CTA's range in every bucket it touches
@@ -149,8 +151,8 @@ __global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const i
   __syncthreads();
   for (int e = threadIdx.x; e < ne; e += blockDim.x) {
     const int32_t p = src[e];
-    if (entry_counts(a, src, e, p)) {
-      const int qn = e / K;
+    const int qn = e / K;
+    if (entry_counts(a, src + qn * K, e - qn * K, p)) {
       pairs[atomicAdd(&hist[p], 1)] = encode_pair(a, t0 + qn, e - qn * K);
     }
   }
@@ -228,8 +230,8 @@ __global__ void scatter_kernel(BucketArgs a, const int32_t* __restrict__ kept2, 
   const int64_t n = a.nq * a.K;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t p = kept2[i];
-    if (!entry_counts(a, kept2, i, p)) continue;
     const int64_t qi = i / a.K;
+    if (!entry_counts(a, kept2 + qi * a.K, (int)(i - qi * a.K), p)) continue;
     const int64_t bk = bucket_of(a, qi, p);
     const int32_t pos = offsets[bk] + atomicAdd(&cursor[bk], 1);
     pairs[pos] = encode_pair(a, qi % a.N, i % a.K);
