@@ -38,7 +38,7 @@ def parse():
     ap.add_argument("--N", type=int, default=262144)
     ap.add_argument("--no-extras", action="store_true", help="skip the sweep, flat and decode side measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
-    ap.add_argument("--profile-case", choices=["prefill64k", "decode8"], default=None,
+    ap.add_argument("--profile-case", choices=["prefill64k", "decode8", "attend256k"], default=None,
                     help="run one small invocation of every kernel (for ncu captures) and exit")
     ap.add_argument("--configs", action="store_true",
                     help="time every listed workload (GPU and CPU oracle), one JSON line each, and exit")
@@ -633,8 +633,10 @@ def run_reference(args, ws, rank):
 
 def profile_case(name: str):
     """One small invocation per kernel, sized for profiler captures: the 64K
-    prefill point (build, route, leaves, flat; inputs 335 MB > L2) or one
-    decode step of 8 sequences x 131073 keys (2.1 GB cache)."""
+    prefill point (build, route, leaves, flat, attention over the selection;
+    inputs 400 MB > L2), one decode step of 8 sequences x 131073 keys (2.1 GB
+    cache), or the 256K selection followed by two attention calls (for the
+    attention's launch list; 15 GB on the device, one-pass metrics only)."""
     import torch
     from pyramid_top_block_mean_gb300 import pisa
     from pyramid_top_block_mean_gb300 import workloads as W
@@ -652,8 +654,25 @@ def profile_case(name: str):
         fs = pisa.Selector(p, mode="flat")
         fs.build(k)
         pisa.select_flat(p, q, fs.pyramid, fs.ws, fs.out_idx, fs.out_score)
+        v = torch.randn(s.B, s.Hkv, s.N, s.d, device="cuda", generator=g).to(torch.bfloat16)
+        at = pisa.Attention(p)
+        at(q, k, v, sel.out_idx)
         torch.cuda.synchronize()
-        status = max(sel.device_status(), fs.device_status())
+        status = max(sel.device_status(), fs.device_status(), at.device_status())
+    elif name == "attend256k":
+        s = W.sweep(262144)
+        g.manual_seed(11 + s.N)
+        q = torch.randn(s.B, s.Hq, s.N, s.d, device="cuda", generator=g).to(torch.bfloat16)
+        k = torch.randn(s.B, s.Hkv, s.N, s.d, device="cuda", generator=g).to(torch.bfloat16)
+        v = torch.randn(s.B, s.Hkv, s.N, s.d, device="cuda", generator=g).to(torch.bfloat16)
+        p = pisa.params_from_shape(s)
+        sel = pisa.Selector(p, with_scores=False)
+        idx, _ = sel.prefill(q, k)
+        at = pisa.Attention(p)
+        for _ in range(2):
+            at(q, k, v, idx)
+        torch.cuda.synchronize()
+        status = max(sel.device_status(), at.device_status())
     else:
         s = W.Shape(B=8, N=W.DECODE_CACHED + 16, Hq=32, Hkv=8, d=128, K=32)
         g.manual_seed(4)
