@@ -29,7 +29,9 @@
  *  - a node is eligible when its leaf range meets E = [1, qb-2]; summaries
  *    themselves are not masked (prefill summaries include later keys);
  *  - "LSE" is the literal log-sum-exp, summed over the query heads of a GQA
- *    group; the scale is 1/sqrt(d) unless another is given;
+ *    group; the scale is 1/sqrt(d) unless another is given; the PISA-1 and
+ *    PISA-2 scorers replace it by its first- and second-order cumulant
+ *    truncations over the same summands (po_reduce);
  *  - forced blocks F = {0, qb-1, qb} are added to the Top-K of the rest;
  *  - ties in Top-K go to the lower node index;
  *  - attention over the selection (po_sparse_attention) reads the keys of the
@@ -55,6 +57,7 @@ typedef struct {
   int32_t C;      /* leaf block size */
   int32_t K;      /* Top-K per level */
   double scale;   /* score scale inside exp(); <= 0 means 1/sqrt(d) */
+  int32_t scorer; /* 0: log-sum-exp; 1: PISA-1; 2: PISA-2 (po_reduce) */
 } po_params;
 
 /* ---------------------------------------------------------------- tree shape
@@ -155,6 +158,26 @@ static double po_lse(const double* x, int64_t n) {
   return m + log(s);
 }
 
+/* The block score over n summands x_i (scaled dots with child summaries or
+ * raw keys) [AGI LSE paragraph: "PISA-1 keeps only the mean; PISA-2 adds the
+ * variance term from the LSE Taylor expansion"; RCAP "The scoring rule
+ * matters": truncations at first and second order].  Writing
+ * LSE(x) = log n + log((1/n) sum_i exp(x_i)) and expanding the second term
+ * in cumulants of the x_i around their mean:
+ *   scorer 0: LSE(x) itself;
+ *   scorer 1: log n + mean(x);
+ *   scorer 2: log n + mean(x) + var(x) / 2, var the population variance. */
+static double po_reduce(const double* x, int64_t n, int scorer) {
+  double mean = 0.0, var = 0.0;
+  if (scorer == 0 || n <= 0) return po_lse(x, n);
+  for (int64_t i = 0; i < n; ++i) mean += x[i];
+  mean /= (double)n;
+  if (scorer == 1) return log((double)n) + mean;
+  for (int64_t i = 0; i < n; ++i) var += (x[i] - mean) * (x[i] - mean);
+  var /= (double)n;
+  return log((double)n) + mean + 0.5 * var;
+}
+
 /* Context of one query: batch b, key head h, position t, sequence length
  * len (prefill: N; decode: the sequence's current length). */
 typedef struct {
@@ -209,7 +232,7 @@ static double po_score(const po_query* Q, int level, int64_t j,
     for (int g = 0; g < Q->G; ++g) {
       double x[2];
       for (int i = 0; i < nk; ++i) x[i] = Q->s * po_dot(Q->qrow[g], kids[i], d);
-      total += po_lse(x, nk);
+      total += po_reduce(x, nk, Q->p->scorer);
     }
     return total;
   }
@@ -225,7 +248,7 @@ static double po_score(const po_query* Q, int level, int64_t j,
     for (int g = 0; g < Q->G; ++g) {
       for (int64_t i = 0; i < n; ++i)
         x[i] = Q->s * po_dot(Q->qrow[g], kh + (lo + i) * d, d);
-      total += po_lse(x, n);
+      total += po_reduce(x, n, Q->p->scorer);
     }
     free(x);
     return total;
