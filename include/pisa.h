@@ -65,7 +65,7 @@
 extern "C" {
 #endif
 
-#define PISA_ABI_VERSION 1
+#define PISA_ABI_VERSION 2
 
 typedef enum {
   PISA_OK = 0,
@@ -78,6 +78,22 @@ typedef enum {
 } pisa_status;
 
 typedef enum { PISA_BF16 = 0, PISA_FP32 = 1 } pisa_dtype;
+
+/* Block scorer of the walk and the leaves (agihunt.info summary, LSE
+ * paragraph; rcap.io, "The scoring rule matters").  Over the n summands x_i
+ * of a candidate (scaled dots with its eligible children's summaries above
+ * the leaves, with its raw keys at the leaves):
+ *   PISA_SCORER_LSE       log sum_i exp(x_i)                 (PISA)
+ *   PISA_SCORER_MEAN      log n + mean(x)                    (PISA-1)
+ *   PISA_SCORER_MEAN_VAR  log n + mean(x) + var(x) / 2        (PISA-2)
+ * the first- and second-order truncations of the cumulant expansion of the
+ * log-sum-exp around the mean (var: population variance).  The flat
+ * comparator and the attention ignore it. */
+typedef enum {
+  PISA_SCORER_LSE = 0,
+  PISA_SCORER_MEAN = 1,
+  PISA_SCORER_MEAN_VAR = 2
+} pisa_scorer;
 
 typedef enum {
   PISA_MODE_PREFILL = 0,
@@ -105,6 +121,7 @@ typedef struct {
   int32_t K;            /* blocks kept per level */
   int32_t qtile;        /* queries sharing one leaf tile (reuse only) */
   float scale;          /* score scale inside exp(); 0 means 1/sqrt(d) */
+  int32_t scorer;       /* pisa_scorer (0: the log-sum-exp of PISA) */
 } pisa_params;
 
 /* ABI version of the loaded library (PISA_ABI_VERSION). */

@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
             float bb = 0.0f;
             if (s1 >= 0) bb = sm.y[s1][g];
             else if (s1 == -2) bb = ((n0 + n1) * sm.x[tid][g] - n0 * a) / n1;
-            sc += (s0 >= 0 && s1 != -1) ? lse2_pair(a, bb) : (s0 >= 0 ? a : bb);
+            sc += (s0 >= 0 && s1 != -1) ? pair_score(pr.scorer, a, bb) : (s0 >= 0 ? a : bb);
           }
           sm.score[tid] = sc != sc ? -INFINITY : sc;  // NaN ranks as -inf
         }
@@ -413,6 +413,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
       int issued = 0, waited = 0;
       for (; issued < nch && issued < kNBuf - 1; ++issued) issue(issued);
       float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;  // heads 2t, 2t+1
+      Moments w0{0.0f, 0.0f, 0.0f}, w1{0.0f, 0.0f, 0.0f};            // PISA-1 / PISA-2
+      const bool lse_scorer = pr.scorer == PISA_SCORER_LSE;
       const float sc = pr.scale2;
       for (int c = 0; c < nch; ++c) {
         if (c + kNBuf - 1 < nch) {
@@ -426,7 +428,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
         lphase ^= 1u << bf;
         waited = c + 1;
         if (!__all_sync(0xffffffffu, ok)) { *abort = 1; break; }
-        if (c % cpl == 0) { m0 = -INFINITY; s0 = 0.0f; m1 = -INFINITY; s1 = 0.0f; }
+        if (c % cpl == 0) {
+          m0 = -INFINITY; s0 = 0.0f; m1 = -INFINITY; s1 = 0.0f;
+          w0 = Moments{0.0f, 0.0f, 0.0f};
+          w1 = Moments{0.0f, 0.0f, 0.0f};
+        }
         const unsigned char* buf = st + bf * kChunkBytes;
 #pragma unroll
         for (int mt = 0; mt < KPC / 16; ++mt) {
@@ -442,27 +448,48 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
           }
           // d[0], d[1]: key r0, heads 2t, 2t+1; d[2], d[3]: key r1
           const float x00 = d[0] * sc, x01 = d[1] * sc, x10 = d[2] * sc, x11 = d[3] * sc;
-          const float n0 = fmaxf(m0, fmaxf(x00, x10)), n1 = fmaxf(m1, fmaxf(x01, x11));
-          s0 = s0 * ptx::ex2(m0 - n0) + ptx::ex2(x00 - n0) + ptx::ex2(x10 - n0);
-          s1 = s1 * ptx::ex2(m1 - n1) + ptx::ex2(x01 - n1) + ptx::ex2(x11 - n1);
-          m0 = n0;
-          m1 = n1;
+          if (lse_scorer) {
+            const float n0 = fmaxf(m0, fmaxf(x00, x10)), n1 = fmaxf(m1, fmaxf(x01, x11));
+            s0 = s0 * ptx::ex2(m0 - n0) + ptx::ex2(x00 - n0) + ptx::ex2(x10 - n0);
+            s1 = s1 * ptx::ex2(m1 - n1) + ptx::ex2(x01 - n1) + ptx::ex2(x11 - n1);
+            m0 = n0;
+            m1 = n1;
+          } else {
+            mom_add(w0, x00);
+            mom_add(w0, x10);
+            mom_add(w1, x01);
+            mom_add(w1, x11);
+          }
         }
         if (c % cpl == cpl - 1) {
           // combine the 8 lanes (groups) of each head, then sum the G heads
-#pragma unroll
-          for (int o = 4; o <= 16; o <<= 1) {
-            const float mo0 = __shfl_xor_sync(0xffffffffu, m0, o), so0 = __shfl_xor_sync(0xffffffffu, s0, o);
-            const float mo1 = __shfl_xor_sync(0xffffffffu, m1, o), so1 = __shfl_xor_sync(0xffffffffu, s1, o);
-            const float a0 = fmaxf(m0, mo0), a1 = fmaxf(m1, mo1);
-            s0 = s0 * ptx::ex2(m0 - a0) + so0 * ptx::ex2(mo0 - a0);
-            s1 = s1 * ptx::ex2(m1 - a1) + so1 * ptx::ex2(mo1 - a1);
-            m0 = a0;
-            m1 = a1;
-          }
           float lse = 0.0f;
-          if (2 * tig < G) lse += m0 + ptx::lg2(s0);
-          if (2 * tig + 1 < G) lse += m1 + ptx::lg2(s1);
+          if (lse_scorer) {
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+              const float mo0 = __shfl_xor_sync(0xffffffffu, m0, o), so0 = __shfl_xor_sync(0xffffffffu, s0, o);
+              const float mo1 = __shfl_xor_sync(0xffffffffu, m1, o), so1 = __shfl_xor_sync(0xffffffffu, s1, o);
+              const float a0 = fmaxf(m0, mo0), a1 = fmaxf(m1, mo1);
+              s0 = s0 * ptx::ex2(m0 - a0) + so0 * ptx::ex2(mo0 - a0);
+              s1 = s1 * ptx::ex2(m1 - a1) + so1 * ptx::ex2(mo1 - a1);
+              m0 = a0;
+              m1 = a1;
+            }
+            if (2 * tig < G) lse += m0 + ptx::lg2(s0);
+            if (2 * tig + 1 < G) lse += m1 + ptx::lg2(s1);
+          } else {
+#pragma unroll
+            for (int o = 4; o <= 16; o <<= 1) {
+              const float n0o = __shfl_xor_sync(0xffffffffu, w0.n, o), u0 = __shfl_xor_sync(0xffffffffu, w0.mean, o),
+                          v0 = __shfl_xor_sync(0xffffffffu, w0.m2, o);
+              const float n1o = __shfl_xor_sync(0xffffffffu, w1.n, o), u1 = __shfl_xor_sync(0xffffffffu, w1.mean, o),
+                          v1 = __shfl_xor_sync(0xffffffffu, w1.m2, o);
+              mom_merge(w0, n0o, u0, v0);
+              mom_merge(w1, n1o, u1, v1);
+            }
+            if (2 * tig < G) lse += moment_score(pr.scorer, w0.n, w0.mean, w0.m2);
+            if (2 * tig + 1 < G) lse += moment_score(pr.scorer, w1.n, w1.mean, w1.m2);
+          }
           lse += __shfl_xor_sync(0xffffffffu, lse, 1);
           lse += __shfl_xor_sync(0xffffffffu, lse, 2);
           if (lane == 0) sm.lscore[warp + (c / cpl) * kDecWarps] = lse != lse ? -INFINITY : lse;
@@ -495,6 +522,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
     int issued = 0, waited = 0;
     for (; issued < nch && issued < kNBuf - 1; ++issued) issue(issued);
     float m = -INFINITY, ssum = 0.0f;  // this lane's head: lane % G
+    Moments wm{0.0f, 0.0f, 0.0f};      // PISA-1 / PISA-2
     for (int c = 0; c < nch; ++c) {
       if (c + kNBuf - 1 < nch) {
         __syncwarp();  // every lane is done with the buffer this copy overwrites
@@ -507,7 +535,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
       lphase ^= 1u << bf;
       waited = c + 1;
       if (!__all_sync(0xffffffffu, ok)) { *abort = 1; break; }
-      if (c % cpl == 0) { m = -INFINITY; ssum = 0.0f; }
+      if (c % cpl == 0) { m = -INFINITY; ssum = 0.0f; wm = Moments{0.0f, 0.0f, 0.0f}; }
       const unsigned char* buf = st + bf * kChunkBytes;
       for (int k1 = 0; k1 < kpc; k1 += NB) {
         float v[32];
@@ -538,22 +566,35 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
         }
         const float x = warp_transpose_sum32(v);  // key k1 + lane/G, head lane%G
         if (k1 + lane / G < kpc) {  // a batch may run past a short chunk
-          const float mn = fmaxf(m, x);
-          ssum = ssum * ptx::ex2(m - mn) + ptx::ex2(x - mn);
-          m = mn;
+          if (pr.scorer == PISA_SCORER_LSE) {
+            const float mn = fmaxf(m, x);
+            ssum = ssum * ptx::ex2(m - mn) + ptx::ex2(x - mn);
+            m = mn;
+          } else {
+            mom_add(wm, x);
+          }
         }
       }
       if (c % cpl == cpl - 1) {
         // combine the lanes of each head, then sum the heads
-        float mh = m, sh = ssum;
+        float lse;
+        if (pr.scorer == PISA_SCORER_LSE) {
+          float mh = m, sh = ssum;
 #pragma unroll
-        for (int o = 16; o >= G; o >>= 1) {
-          const float mo = __shfl_xor_sync(0xffffffffu, mh, o), so = __shfl_xor_sync(0xffffffffu, sh, o);
-          const float mn = fmaxf(mh, mo);
-          sh = sh * ptx::ex2(mh - mn) + so * ptx::ex2(mo - mn);
-          mh = mn;
+          for (int o = 16; o >= G; o >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, mh, o), so = __shfl_xor_sync(0xffffffffu, sh, o);
+            const float mn = fmaxf(mh, mo);
+            sh = sh * ptx::ex2(mh - mn) + so * ptx::ex2(mo - mn);
+            mh = mn;
+          }
+          lse = mh + ptx::lg2(sh);
+        } else {
+#pragma unroll
+          for (int o = 16; o >= G; o >>= 1)
+            mom_merge(wm, __shfl_xor_sync(0xffffffffu, wm.n, o), __shfl_xor_sync(0xffffffffu, wm.mean, o),
+                      __shfl_xor_sync(0xffffffffu, wm.m2, o));
+          lse = moment_score(pr.scorer, wm.n, wm.mean, wm.m2);
         }
-        float lse = mh + ptx::lg2(sh);
 #pragma unroll
         for (int o = G / 2; o >= 1; o >>= 1) lse += __shfl_xor_sync(0xffffffffu, lse, o);
         if (lane == 0) sm.lscore[warp + (c / cpl) * kDecWarps] = lse != lse ? -INFINITY : lse;

@@ -102,18 +102,35 @@ __global__ void __launch_bounds__(kLeafWarps * 32) leaf_simt_kernel(Prob pr, Pyr
       }
       vals[bt] = warp_transpose_sum32(v);  // lane: key bt*NB + lane/G, head lane%G
     }
-    // per head (lanes sharing lane % G): log2-sum-exp2 over the 64 keys
-    float m = vals[0];
+    float lse;
+    if (pr.scorer == PISA_SCORER_LSE) {
+      // per head (lanes sharing lane % G): log2-sum-exp2 over the 64 keys
+      float m = vals[0];
 #pragma unroll
-    for (int bt = 1; bt < NBAT; ++bt) m = fmaxf(m, vals[bt]);
+      for (int bt = 1; bt < NBAT; ++bt) m = fmaxf(m, vals[bt]);
 #pragma unroll
-    for (int o = 16; o >= G; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float sum = 0.0f;
+      for (int o = 16; o >= G; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float sum = 0.0f;
 #pragma unroll
-    for (int bt = 0; bt < NBAT; ++bt) sum += exp2f(vals[bt] - m);
+      for (int bt = 0; bt < NBAT; ++bt) sum += exp2f(vals[bt] - m);
 #pragma unroll
-    for (int o = 16; o >= G; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    float lse = m + __log2f(sum);
+      for (int o = 16; o >= G; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+      lse = m + __log2f(sum);
+    } else {
+      // PISA-1 / PISA-2: mean, then centred second moment, of the 64 scaled dots
+      float s1 = 0.0f;
+#pragma unroll
+      for (int bt = 0; bt < NBAT; ++bt) s1 += vals[bt];
+#pragma unroll
+      for (int o = 16; o >= G; o >>= 1) s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      const float mean = s1 * (1.0f / 64.0f);
+      float s2 = 0.0f;
+#pragma unroll
+      for (int bt = 0; bt < NBAT; ++bt) s2 = fmaf(vals[bt] - mean, vals[bt] - mean, s2);
+#pragma unroll
+      for (int o = 16; o >= G; o >>= 1) s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+      lse = moment_score(pr.scorer, 64.0f, mean, s2);
+    }
     // sum over the G heads (lanes 0..G-1 hold distinct heads)
 #pragma unroll
     for (int o = G / 2; o >= 1; o >>= 1) lse += __shfl_xor_sync(0xffffffffu, lse, o);

@@ -534,17 +534,30 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
         x[j] = __uint_as_float(v0[j]);
         x[32 + j] = __uint_as_float(v1[j]);
       }
-      float mm[8];
+      float lse;
+      if (pr.scorer == PISA_SCORER_LSE) {
+        float mm[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) mm[u] = x[u];
+        for (int u = 0; u < 8; ++u) mm[u] = x[u];
 #pragma unroll
-      for (int j = 8; j < 64; ++j) mm[j & 7] = fmaxf(mm[j & 7], x[j]);
-      const float m = fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
-                            fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7]))) * sc;
-      float ss[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int j = 8; j < 64; ++j) mm[j & 7] = fmaxf(mm[j & 7], x[j]);
+        const float m = fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
+                              fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7]))) * sc;
+        float ss[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int j = 0; j < 64; ++j) ss[j & 3] += ptx::ex2(fmaf(x[j], sc, -m));
-      float lse = m + ptx::lg2((ss[0] + ss[1]) + (ss[2] + ss[3]));
+        for (int j = 0; j < 64; ++j) ss[j & 3] += ptx::ex2(fmaf(x[j], sc, -m));
+        lse = m + ptx::lg2((ss[0] + ss[1]) + (ss[2] + ss[3]));
+      } else {
+        // PISA-1 / PISA-2: mean and centred second moment of the 64 dots
+        float s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int j = 0; j < 64; ++j) s1[j & 3] += x[j];
+        const float mean = ((s1[0] + s1[1]) + (s1[2] + s1[3])) * (1.0f / 64.0f);
+        float s2[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int j = 0; j < 64; ++j) s2[j & 3] = fmaf(x[j] - mean, x[j] - mean, s2[j & 3]);
+        lse = moment_score(pr.scorer, 64.0f, mean * sc, ((s2[0] + s2[1]) + (s2[2] + s2[3])) * (sc * sc));
+      }
 #pragma unroll
       for (int o = 1; o < G; o <<= 1) lse += __shfl_xor_sync(0xffffffffu, lse, o);
       if ((r % G) == 0 && qr < info.z) {

@@ -109,6 +109,7 @@ static pisa_status check_params(const pisa_params* p, Prob* pr, Pyr* s) {
     return PISA_ERR_INVALID_ARG;
   if (p->H_q % p->H_kv != 0) return PISA_ERR_INVALID_ARG;
   if (!(p->scale >= 0.0f) || isinf(p->scale)) return PISA_ERR_INVALID_ARG;
+  if (p->scorer < PISA_SCORER_LSE || p->scorer > PISA_SCORER_MEAN_VAR) return PISA_ERR_INVALID_ARG;
   if (p->dtype != PISA_BF16 && p->dtype != PISA_FP32) return PISA_ERR_UNSUPPORTED;
   const int G = p->H_q / p->H_kv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return PISA_ERR_UNSUPPORTED;
@@ -117,7 +118,7 @@ static pisa_status check_params(const pisa_params* p, Prob* pr, Pyr* s) {
   if (p->N > kMaxN) return PISA_ERR_UNSUPPORTED;
   if (!make_pyr(p->N, p->C, s)) return PISA_ERR_INVALID_ARG;
   pr->B = p->B; pr->N = p->N; pr->Hq = p->H_q; pr->Hkv = p->H_kv; pr->G = G;
-  pr->d = p->d; pr->C = p->C; pr->K = p->K; pr->dtype = p->dtype;
+  pr->d = p->d; pr->C = p->C; pr->K = p->K; pr->dtype = p->dtype; pr->scorer = p->scorer;
   const float sc = p->scale > 0.0f ? p->scale : 1.0f / sqrtf((float)p->d);
   pr->scale2 = sc * kLog2e;
   return PISA_OK;

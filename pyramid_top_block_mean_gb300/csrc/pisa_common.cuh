@@ -32,6 +32,7 @@ struct Prob {
   int32_t Hq, Hkv, G, d, C, K;
   float scale2;     // score scale times log2(e): exponents are taken base 2
   int32_t dtype;    // PISA_BF16 / PISA_FP32
+  int32_t scorer;   // pisa_scorer
 };
 
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -134,6 +135,52 @@ __device__ __forceinline__ float warp_sum(float x) {
 __device__ __forceinline__ float lse2_pair(float a, float b) {
   const float m = fmaxf(a, b), n = fminf(a, b);
   return m + __log2f(1.0f + exp2f(n - m));
+}
+
+// Block scorers (agihunt.info summary, LSE paragraph: PISA-1 keeps only the
+// mean, PISA-2 adds the variance term of the LSE Taylor expansion; rcap.io,
+// "The scoring rule matters": truncations at first and second order).  Over
+// n summands y_i in log2 units (scaled dots times log2 e):
+//   PISA_SCORER_LSE:      log2 sum 2^y_i
+//   PISA_SCORER_MEAN:     log2 n + mean(y)
+//   PISA_SCORER_MEAN_VAR: log2 n + mean(y) + (ln 2 / 2) var(y)
+// which are the natural-log log n + mean(x) (+ var(x) / 2) times log2 e.
+constexpr float kHalfLn2 = 0.34657359027997264f;
+
+// Score of a node from the scaled dots (log2 units) of its two eligible children.
+__device__ __forceinline__ float pair_score(int scorer, float a, float b) {
+  if (scorer == PISA_SCORER_LSE) return lse2_pair(a, b);
+  const float mean = 0.5f * (a + b);
+  if (scorer == PISA_SCORER_MEAN) return 1.0f + mean;
+  const float h = 0.5f * (a - b);
+  return 1.0f + mean + kHalfLn2 * (h * h);
+}
+
+// PISA-1 / PISA-2 score from n summands with mean `mean` and centred second
+// moment m2 = sum (y_i - mean)^2 (log2 units).
+__device__ __forceinline__ float moment_score(int scorer, float n, float mean, float m2) {
+  const float r = __log2f(n) + mean;
+  return scorer == PISA_SCORER_MEAN_VAR ? r + kHalfLn2 * (m2 / n) : r;
+}
+
+// Running count, mean and centred second moment (Welford's update; Chan's
+// merge of two partial sets).
+struct Moments {
+  float n, mean, m2;
+};
+__device__ __forceinline__ void mom_add(Moments& s, float y) {
+  s.n += 1.0f;
+  const float d = y - s.mean;
+  s.mean += d / s.n;
+  s.m2 = fmaf(d, y - s.mean, s.m2);
+}
+__device__ __forceinline__ void mom_merge(Moments& a, float nb, float meanb, float m2b) {
+  const float n = a.n + nb;
+  if (nb == 0.0f || n == 0.0f) return;
+  const float d = meanb - a.mean;
+  a.mean = fmaf(d, nb / n, a.mean);
+  a.m2 = a.m2 + m2b + d * d * (a.n * nb / n);
+  a.n = n;
 }
 
 // Record the first device fault in the workspace status word.

@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(WARPS * 32) route_kernel(Prob pr, Pyr s, const
           float bb = 0.0f;
           if (s1 >= 0) bb = sm.y[s1][g];
           else if (s1 == -2) bb = sibling_dot(sm.x[cur][i][g], a, n0, n1);
-          sc += (s0 >= 0 && s1 != -1) ? lse2_pair(a, bb) : (s0 >= 0 ? a : bb);
+          sc += (s0 >= 0 && s1 != -1) ? pair_score(pr.scorer, a, bb) : (s0 >= 0 ? a : bb);
         }
         if (sc != sc) sc = -INFINITY;  // NaN ranks last
         key[sl] = ((uint64_t)orderable(sc) << 32) | (uint32_t)(~(uint32_t)sm.cand[cur][i]);

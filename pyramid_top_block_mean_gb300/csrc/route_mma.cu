@@ -113,7 +113,9 @@ __global__ void split_pyramid_kernel(int64_t n, int D, const float* __restrict__
 // dims 32 bb + 8 t + {0..7} of its half (one 16-byte load; words x, y for the
 // first step and z, w for the second).  With the permuted row layout the
 // eight lanes of a node read one contiguous 128-byte line per load.
-template <int D, int KM, int WARPS>
+// kLse: the log-sum-exp scorer (the PISA default), compiled on its own so the
+// truncated scorers cost it nothing.
+template <int D, int KM, int WARPS, bool kLse>
 __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob pr, Pyr s, const uint16_t* __restrict__ q,
                                                                const uint16_t* __restrict__ phi,
                                                                const uint16_t* __restrict__ plo,
@@ -302,10 +304,18 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob 
                                sib_dot(xv.z, ya[sl].z, n0, n1), sib_dot(xv.w, ya[sl].w, n0, n1));
         }
         float scv = 0.0f;
+        if constexpr (kLse) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float a = comp(ya[sl], g), bb = comp(yb[sl], g);
-          scv += (s0 >= 0 && s1 != -1) ? lse2_pair(a, bb) : (s0 >= 0 ? a : bb);
+          for (int g = 0; g < G; ++g) {
+            const float a = comp(ya[sl], g), bb = comp(yb[sl], g);
+            scv += (s0 >= 0 && s1 != -1) ? lse2_pair(a, bb) : (s0 >= 0 ? a : bb);
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float a = comp(ya[sl], g), bb = comp(yb[sl], g);
+            scv += (s0 >= 0 && s1 != -1) ? pair_score(pr.scorer, a, bb) : (s0 >= 0 ? a : bb);
+          }
         }
         if (scv == 0.0f) scv = 0.0f;        // -0 ranks like +0
         if (scv != scv) scv = -INFINITY;     // NaN ranks last (keys stay <= 0xff800000)
@@ -368,11 +378,11 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS) route_mma_kernel(Prob 
   }
 }
 
-template <int D, int KM, int WARPS>
+template <int D, int KM, int WARPS, bool kLse>
 static cudaError_t launch_route_mma_t(const Prob& pr, const Pyr& s, const void* q, const uint16_t* phi,
                                       const uint16_t* plo, int32_t* kept2, int32_t* trace, cudaStream_t st) {
   const size_t smem = sizeof(RouteMmaQPad<2 * KM>) * 2 * WARPS;
-  auto kern = route_mma_kernel<D, KM, WARPS>;
+  auto kern = route_mma_kernel<D, KM, WARPS, kLse>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t nq = pr.B * pr.Hkv * pr.N;
@@ -395,13 +405,13 @@ cudaError_t launch_route_mma(const Prob& pr, const Pyr& s, const void* q, const 
       n, pr.d, pyr, (__nv_bfloat16*)phi, (__nv_bfloat16*)plo);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-#define PISA_RM_CASE(DD)                                                                                  \
-  if (pr.d == DD) {                                                                                       \
-    if (pr.K <= 8) return launch_route_mma_t<DD, 8, 8>(pr, s, q, phi, plo, kept2, trace, st);             \
-    if (pr.K <= 16) return launch_route_mma_t<DD, 16, 8>(pr, s, q, phi, plo, kept2, trace, st);           \
-    return launch_route_mma_t<DD, 32, 4>(pr, s, q, phi, plo, kept2, trace, st);                           \
+#define PISA_RM_CASE(DD, LSE)                                                                             \
+  if (pr.d == DD && (pr.scorer == PISA_SCORER_LSE) == LSE) {                                              \
+    if (pr.K <= 8) return launch_route_mma_t<DD, 8, 8, LSE>(pr, s, q, phi, plo, kept2, trace, st);        \
+    if (pr.K <= 16) return launch_route_mma_t<DD, 16, 8, LSE>(pr, s, q, phi, plo, kept2, trace, st);      \
+    return launch_route_mma_t<DD, 32, 4, LSE>(pr, s, q, phi, plo, kept2, trace, st);                      \
   }
-  PISA_RM_CASE(128) PISA_RM_CASE(64)
+  PISA_RM_CASE(128, true) PISA_RM_CASE(64, true) PISA_RM_CASE(128, false) PISA_RM_CASE(64, false)
 #undef PISA_RM_CASE
   return cudaErrorInvalidValue;
 }

@@ -28,6 +28,7 @@ STATUS_NAMES = {0: "PISA_OK", -1: "PISA_ERR_INVALID_ARG", -2: "PISA_ERR_UNSUPPOR
                 -3: "PISA_ERR_MISALIGNED", -4: "PISA_ERR_WORKSPACE", -5: "PISA_ERR_CUDA",
                 -6: "PISA_ERR_DEVICE"}
 BF16, FP32 = 0, 1
+SCORER_LSE, SCORER_MEAN, SCORER_MEAN_VAR = 0, 1, 2
 MODE_PREFILL, MODE_DECODE, MODE_FLAT, MODE_ATTEND = 0, 1, 2, 3
 DEV_OK, DEV_BAD_SEQ_LEN, DEV_TIMEOUT, DEV_BAD_INDEX = 0, 1, 2, 3
 
@@ -43,7 +44,7 @@ class Params(ctypes.Structure):
                 ("B", ctypes.c_int64), ("N", ctypes.c_int64),
                 ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("d", ctypes.c_int32),
                 ("C", ctypes.c_int32), ("g", ctypes.c_int32), ("K", ctypes.c_int32),
-                ("qtile", ctypes.c_int32), ("scale", ctypes.c_float)]
+                ("qtile", ctypes.c_int32), ("scale", ctypes.c_float), ("scorer", ctypes.c_int32)]
 
 
 _P = ctypes.POINTER(Params)
@@ -102,13 +103,15 @@ def kernel_launches() -> int:
 
 
 def make_params(B: int, N: int, H_q: int, H_kv: int, d: int, C: int = 64, g: int = 2, K: int = 8,
-                qtile: int = 4, dtype: str = "bf16", scale: float = 0.0) -> Params:
+                qtile: int = 4, dtype: str = "bf16", scale: float = 0.0, scorer: int = 0) -> Params:
+    """scorer: SCORER_LSE (PISA), SCORER_MEAN (PISA-1) or SCORER_MEAN_VAR (PISA-2)."""
     return Params(ctypes.sizeof(Params), BF16 if dtype == "bf16" else FP32, B, N, H_q, H_kv, d, C, g, K,
-                  qtile, scale)
+                  qtile, scale, scorer)
 
 
-def params_from_shape(s, N: Optional[int] = None) -> Params:
-    return make_params(s.B, s.N if N is None else N, s.Hq, s.Hkv, s.d, s.C, s.g, s.K, s.qtile, s.dtype)
+def params_from_shape(s, N: Optional[int] = None, scorer: int = 0) -> Params:
+    return make_params(s.B, s.N if N is None else N, s.Hq, s.Hkv, s.d, s.C, s.g, s.K, s.qtile, s.dtype,
+                       scorer=scorer)
 
 
 def pyramid_levels(p: Params) -> int:

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(pisa):
 
 
 def test_abi_version_and_status_strings(pisa):
-    assert pisa.abi_version() == 1
+    assert pisa.abi_version() == 2
     for code in range(-6, 1):
         assert pisa.status_string(code).startswith(pisa.STATUS_NAMES[code])
 
@@ -45,7 +45,7 @@ def test_size_queries_match_the_pyramid_shape(pisa):
         assert pisa.pyramid_nodes(p) == oracle.lib().po_num_nodes(N, 64)
         assert pisa.pyramid_levels(p) == oracle.lib().po_num_levels(N, 64)
         assert pisa.pyramid_bytes(p) == 2 * 4 * pisa.pyramid_nodes(p) * 128 * 4
-        for mode in (0, 1, 2):
+        for mode in (0, 1, 2, 3):
             assert pisa.workspace_bytes(p, mode) >= 256
 
 
@@ -53,7 +53,7 @@ def test_size_queries_match_the_pyramid_shape(pisa):
     ("H_q", 15, -1), ("H_kv", 0, -1), ("K", 0, -1), ("N", -1, -1), ("B", -1, -1), ("qtile", 0, -1),
     ("scale", -1.0, -1), ("d", 96, -2), ("C", 32, -2), ("g", 3, -2), ("K", 33, -2), ("dtype", 7, -2),
     ("H_q", 48, -2),  # G = 12
-    ("N", (1 << 26) + 1, -2), ("struct_size", 8, -1),
+    ("N", (1 << 26) + 1, -2), ("struct_size", 8, -1), ("scorer", 3, -1), ("scorer", -1, -1),
 ])
 def test_bad_params_are_rejected(pisa, field, value, code):
     p = pisa.make_params(1, 4096, 16, 4, 128, K=8)
@@ -91,3 +91,12 @@ def test_empty_problems_are_no_ops(pisa):
         p = pisa.make_params(B, N, 16, 4, 128, K=8)
         assert L.pisa_select_prefill(ctypes.byref(p), None, None, None, None, 0, None, None, None, None) == 0
         assert L.pisa_build_pyramid(ctypes.byref(p), None, None, None, None) == 0
+
+
+def test_params_without_the_scorer_field_are_rejected(pisa):
+    # a caller built against the first ABI passes the shorter struct
+    p = pisa.make_params(1, 4096, 16, 4, 128, K=8)
+    p.struct_size = pisa.Params.scorer.offset
+    assert pisa.workspace_bytes(p, 0) == 0
+    for sc in (0, 1, 2):
+        assert pisa.workspace_bytes(pisa.make_params(1, 4096, 16, 4, 128, K=8, scorer=sc), 0) > 0
