@@ -214,6 +214,34 @@ pisa_status pisa_select_decode(const pisa_params* p, const void* q,
                                int32_t* out_idx, float* out_score,
                                int32_t* trace, void* stream);
 
+/* Paged key cache (the production decode layout; SURVEY's NEXT row on paged
+ * decode).  The raw keys live in a pool of pages of C keys,
+ *   k_pages  [num_pages, H_kv, C, d] (DEVICE, dtype of p): page j of
+ *            sequence b is page_table[b * ceil(N / C) + j] and holds that
+ *            sequence's keys [j C, (j + 1) C) for every key head;
+ *   page_table int32 [B, ceil(N / C)] (DEVICE), N the capacity of p.
+ * Only the pages of leaves that hold keys (j C < seq_lens[b]) are read.  A
+ * page index outside [0, num_pages) sets PISA_DEV_BAD_INDEX in the status
+ * word and is never dereferenced: the build treats that leaf as empty, the
+ * decode step writes -1 / -INFINITY for that sequence.  The pyramid stays
+ * in its capacity layout [B, H_kv, P, d].  Results equal those of the
+ * contiguous calls on the same keys bit for bit.
+ *   pisa_build_pyramid_paged: pisa_build_pyramid from pages; ws holds the
+ *     status word (at least pisa_workspace_bytes(p, PISA_MODE_DECODE)).
+ *   pisa_select_decode_paged: pisa_select_decode from pages. */
+pisa_status pisa_build_pyramid_paged(const pisa_params* p, const void* k_pages,
+                                     int64_t num_pages,
+                                     const int32_t* page_table,
+                                     const int32_t* seq_lens, float* pyramid,
+                                     void* ws, size_t ws_bytes, void* stream);
+pisa_status pisa_select_decode_paged(const pisa_params* p, const void* q,
+                                     const void* k_pages, int64_t num_pages,
+                                     const int32_t* page_table,
+                                     const int32_t* seq_lens, float* pyramid,
+                                     void* ws, size_t ws_bytes,
+                                     int32_t* out_idx, float* out_score,
+                                     int32_t* trace, void* stream);
+
 /* Flat BSA-style comparator (agihunt.info summary, model paragraph: "BSA
  * (NSA's selected branch with mean summaries)"; rcap.io: "scores every query
  * against every block summary", O(N^2/C)).  Every query head h' scores every

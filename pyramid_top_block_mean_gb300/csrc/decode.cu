@@ -81,7 +81,7 @@ __device__ __forceinline__ int scan64(int v, int32_t* scratch, int* total) {
 
 template <int D, int G>
 __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, const void* __restrict__ q,
-                                                             const void* __restrict__ kc,
+                                                             const void* __restrict__ kc, KeyPages kp,
                                                              const int32_t* __restrict__ seq_lens, float* pyr,
                                                              int32_t* __restrict__ status, int32_t* __restrict__ out_idx,
                                                              float* __restrict__ out_score, int32_t* __restrict__ trace) {
@@ -106,6 +106,19 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
   const bool bf16 = pr.dtype == PISA_BF16;
   const int esz = bf16 ? 2 : 4;
   const int64_t t = len - 1, qb = t / s.C;
+  if (kp.table) {
+    // every page the step can read (leaves 0..qb) must be in the pool
+    bool bad = false;
+    for (int64_t j = tid; j <= qb; j += kDecThreads) {
+      const int32_t pg = kp.table[b * kp.max_pages + j];
+      bad |= pg < 0 || pg >= kp.num_pages;
+    }
+    if (__syncthreads_or(bad)) {
+      if (tid == 0) set_status(status, PISA_DEV_BAD_INDEX);
+      for (int i = tid; i < W; i += kDecThreads) { oi[i] = -1; if (os) os[i] = -INFINITY; }
+      return;
+    }
+  }
   float* ph = pyr + bh * s.P * D;
   volatile int32_t* abort = &sm.abort;
 
@@ -124,7 +137,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
     unsigned char* keys = &sm.stage[0][0];  // up to C*D*4 = 32 KB
     float* sib = reinterpret_cast<float*>(&sm.stage[0][0] + 32768);  // one row per level (16 KB)
     const int64_t n_leaf = len - qb * s.C;
-    const char* src = reinterpret_cast<const char*>(kc) + ((bh * s.N + qb * s.C) * D) * esz;
+    const char* src = reinterpret_cast<const char*>(kc) + (leaf_row(kp, pr.Hkv, s.N, s.C, b, h, qb) * D) * esz;
     const int chunks = (int)(n_leaf * D * esz / 16);
     for (int c = tid; c < chunks; c += kDecThreads) ptx::cp_async_16(ptx::smem_u32(keys + 16 * c), src + 16 * c);
     for (int w = tid; w < s.L * (D / 4); w += kDecThreads) {
@@ -406,7 +419,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
           const uint32_t bar = ptx::smem_u32(&sm.bar_leaf[warp][c % kNBuf]);
           ptx::mbar_arrive_expect_tx(bar, KPC * D * 2);
           ptx::bulk_g2s(ptx::smem_u32(st + (c % kNBuf) * kChunkBytes),
-                        reinterpret_cast<const uint16_t*>(kc) + (bh * s.N + leaf * s.C + (c % cpl) * KPC) * D,
+                        reinterpret_cast<const uint16_t*>(kc) +
+                            (leaf_row(kp, pr.Hkv, s.N, s.C, b, h, leaf) + (c % cpl) * KPC) * D,
                         KPC * D * 2, bar);
         }
       };
@@ -516,7 +530,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
         const uint32_t bar = ptx::smem_u32(&sm.bar_leaf[warp][c % kNBuf]);
         ptx::mbar_arrive_expect_tx(bar, chunk_bytes);
         ptx::bulk_g2s(ptx::smem_u32(st + (c % kNBuf) * kChunkBytes),
-                      reinterpret_cast<const char*>(kc) + ((bh * s.N + leaf * s.C + k0) * D) * esz, chunk_bytes, bar);
+                      reinterpret_cast<const char*>(kc) + ((leaf_row(kp, pr.Hkv, s.N, s.C, b, h, leaf) + k0) * D) * esz,
+                      chunk_bytes, bar);
       }
     };
     int issued = 0, waited = 0;
@@ -639,25 +654,26 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
 
 template <int D, int G>
 static cudaError_t launch_decode_t(const Prob& pr, const Pyr& s, const void* q, const void* kc,
-                                   const int32_t* seq_lens, float* pyr, int32_t* status, int32_t* out_idx,
+                                   const KeyPages& kp, const int32_t* seq_lens, float* pyr, int32_t* status, int32_t* out_idx,
                                    float* out_score, int32_t* trace, cudaStream_t st) {
   const size_t smem = sizeof(DecSmem<G>) + 128;
   auto kern = decode_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   note_launch();
-  kern<<<(unsigned)(pr.B * pr.Hkv), kDecThreads, smem, st>>>(pr, s, q, kc, seq_lens, pyr, status, out_idx,
+  kern<<<(unsigned)(pr.B * pr.Hkv), kDecThreads, smem, st>>>(pr, s, q, kc, kp, seq_lens, pyr, status, out_idx,
                                                               out_score, trace);
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const Prob& pr, const Pyr& s, const void* q, const void* kc, const int32_t* seq_lens,
+cudaError_t launch_decode(const Prob& pr, const Pyr& s, const void* q, const void* kc, const KeyPages& kp,
+                          const int32_t* seq_lens,
                           float* pyr, int32_t* status, int32_t* out_idx, float* out_score, int32_t* trace,
                           cudaStream_t st) {
   if (s.L * pr.d * 4 > 16384) return cudaErrorInvalidValue;  // sibling rows must fit their staging slot
 #define PISA_DEC_CASE(DD, GG) \
   if (pr.d == DD && pr.G == GG)  \
-    return launch_decode_t<DD, GG>(pr, s, q, kc, seq_lens, pyr, status, out_idx, out_score, trace, st);
+    return launch_decode_t<DD, GG>(pr, s, q, kc, kp, seq_lens, pyr, status, out_idx, out_score, trace, st);
   PISA_DEC_CASE(128, 1) PISA_DEC_CASE(128, 2) PISA_DEC_CASE(128, 4) PISA_DEC_CASE(128, 8)
   PISA_DEC_CASE(64, 1) PISA_DEC_CASE(64, 2) PISA_DEC_CASE(64, 4) PISA_DEC_CASE(64, 8)
 #undef PISA_DEC_CASE

@@ -193,7 +193,39 @@ pisa_status pisa_build_pyramid(const pisa_params* p, const void* k, const int32_
   if (pr.B * pr.Hkv * pr.N == 0) return PISA_OK;
   if (!k || !pyramid) return PISA_ERR_INVALID_ARG;
   if (!aligned16(k) || !aligned16(pyramid)) return PISA_ERR_MISALIGNED;
-  return cuda_status(launch_build_pyramid(pr, s, k, seq_lens, pyramid, (cudaStream_t)stream));
+  return cuda_status(launch_build_pyramid(pr, s, k, KeyPages{nullptr, 0, 0}, seq_lens, pyramid, nullptr,
+                                          (cudaStream_t)stream));
+}
+
+// Checks of a paged key pool shared by the paged entry points.
+static pisa_status paged_checks(const Prob& pr, const Pyr& s, const void* k_pages, int64_t num_pages,
+                                const int32_t* page_table, KeyPages* kp) {
+  if (!k_pages || !page_table || num_pages < 1) return PISA_ERR_INVALID_ARG;
+  if (!aligned16(k_pages) || ((uintptr_t)page_table & 3u)) return PISA_ERR_MISALIGNED;
+  if (num_pages > ((int64_t)1 << 31) - 1) return PISA_ERR_UNSUPPORTED;
+  kp->table = page_table;
+  kp->max_pages = s.nb;
+  kp->num_pages = num_pages;
+  (void)pr;
+  return PISA_OK;
+}
+
+pisa_status pisa_build_pyramid_paged(const pisa_params* p, const void* k_pages, int64_t num_pages,
+                                     const int32_t* page_table, const int32_t* seq_lens, float* pyramid, void* ws,
+                                     size_t ws_bytes, void* stream) {
+  Prob pr; Pyr s;
+  pisa_status rc = check_params(p, &pr, &s);
+  if (rc != PISA_OK) return rc;
+  if (pr.B * pr.Hkv * pr.N == 0) return PISA_OK;
+  if (!pyramid || !ws) return PISA_ERR_INVALID_ARG;
+  if (!aligned16(pyramid) || !aligned16(ws) || ((uintptr_t)seq_lens & 3u)) return PISA_ERR_MISALIGNED;
+  if (ws_bytes < decode_ws_bytes(pr, s)) return PISA_ERR_WORKSPACE;
+  KeyPages kp;
+  rc = paged_checks(pr, s, k_pages, num_pages, page_table, &kp);
+  if (rc != PISA_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return PISA_ERR_CUDA;
+  return cuda_status(launch_build_pyramid(pr, s, k_pages, kp, seq_lens, pyramid, (int32_t*)ws, st));
 }
 
 // Checks shared by the prefill entry points.
@@ -287,7 +319,32 @@ pisa_status pisa_select_decode(const pisa_params* p, const void* q, const void* 
   int32_t* status = (int32_t*)ws;
   cudaError_t e = cudaMemsetAsync(status, 0, 256, st);
   if (e != cudaSuccess) return PISA_ERR_CUDA;
-  return cuda_status(launch_decode(pr, s, q, k_cache, seq_lens, pyramid, status, out_idx, out_score, trace, st));
+  return cuda_status(launch_decode(pr, s, q, k_cache, KeyPages{nullptr, 0, 0}, seq_lens, pyramid, status, out_idx,
+                                   out_score, trace, st));
+}
+
+pisa_status pisa_select_decode_paged(const pisa_params* p, const void* q, const void* k_pages, int64_t num_pages,
+                                     const int32_t* page_table, const int32_t* seq_lens, float* pyramid, void* ws,
+                                     size_t ws_bytes, int32_t* out_idx, float* out_score, int32_t* trace,
+                                     void* stream) {
+  Prob pr; Pyr s;
+  pisa_status rc = check_params(p, &pr, &s);
+  if (rc != PISA_OK) return rc;
+  if (pr.B * pr.Hkv == 0) return PISA_OK;
+  if (pr.N == 0) return PISA_ERR_INVALID_ARG;
+  if (!q || !seq_lens || !pyramid || !ws || !out_idx) return PISA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(pyramid) || !aligned16(ws)) return PISA_ERR_MISALIGNED;
+  if (((uintptr_t)out_idx & 3u) || ((uintptr_t)out_score & 3u) || ((uintptr_t)seq_lens & 3u) ||
+      ((uintptr_t)trace & 3u))
+    return PISA_ERR_MISALIGNED;
+  if (ws_bytes < decode_ws_bytes(pr, s)) return PISA_ERR_WORKSPACE;
+  KeyPages kp;
+  rc = paged_checks(pr, s, k_pages, num_pages, page_table, &kp);
+  if (rc != PISA_OK) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  int32_t* status = (int32_t*)ws;
+  if (cudaMemsetAsync(status, 0, 256, st) != cudaSuccess) return PISA_ERR_CUDA;
+  return cuda_status(launch_decode(pr, s, q, k_pages, kp, seq_lens, pyramid, status, out_idx, out_score, trace, st));
 }
 
 pisa_status pisa_select_flat(const pisa_params* p, const void* q, const float* pyramid, void* ws, size_t ws_bytes,

@@ -183,6 +183,20 @@ __device__ __forceinline__ void mom_merge(Moments& a, float nb, float meanb, flo
   a.n = n;
 }
 
+// Where the raw keys of leaf `leaf` of (sequence b, key head h) start, in rows
+// of d elements: the contiguous cache [B, Hkv, N, d], or a pool of pages of C
+// keys laid out [num_pages, Hkv, C, d] and addressed through a page table
+// [B, max_pages] (page j of a sequence holds its leaf j).
+struct KeyPages {
+  const int32_t* table;  // null: contiguous
+  int64_t max_pages, num_pages;
+};
+__device__ __forceinline__ int64_t leaf_row(const KeyPages& kp, int64_t Hkv, int64_t N, int64_t C, int64_t b,
+                                            int64_t h, int64_t leaf) {
+  if (!kp.table) return (b * Hkv + h) * N + leaf * C;
+  return ((int64_t)kp.table[b * kp.max_pages + leaf] * Hkv + h) * C;
+}
+
 // Record the first device fault in the workspace status word.
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);

@@ -81,8 +81,8 @@ void note_launch();
 // 128-byte swizzle (the K-major operand layout of the tcgen05 MMAs).
 bool make_tmap_rows(CUtensorMap* m, const void* base, int64_t rows, int d, int box_rows);
 
-cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, const int32_t* seq_lens,
-                                 float* pyr, cudaStream_t st);
+cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, const KeyPages& kp,
+                                 const int32_t* seq_lens, float* pyr, int32_t* status, cudaStream_t st);
 cudaError_t launch_route(const Prob& pr, const Pyr& s, const void* q, const float* pyr, int32_t* kept2,
                          int32_t* trace, int32_t* status, cudaStream_t st);
 bool route_mma_supported(const Prob& pr);
@@ -92,7 +92,8 @@ cudaError_t launch_leaf_simt(const Prob& pr, const Pyr& s, const void* q, const 
                              int32_t* out_idx, float* out_score, cudaStream_t st);
 cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, char* ws, const void* q,
                            const void* k, int32_t* out_idx, float* out_score, int num_sms, cudaStream_t st);
-cudaError_t launch_decode(const Prob& pr, const Pyr& s, const void* q, const void* kc, const int32_t* seq_lens,
+cudaError_t launch_decode(const Prob& pr, const Pyr& s, const void* q, const void* kc, const KeyPages& kp,
+                          const int32_t* seq_lens,
                           float* pyr, int32_t* status, int32_t* out_idx, float* out_score, int32_t* trace,
                           cudaStream_t st);
 cudaError_t launch_attend(const Prob& pr, const Pyr& s, const AttendWs& w, char* ws, const void* q, const void* k,

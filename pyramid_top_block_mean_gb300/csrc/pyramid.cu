@@ -3,6 +3,8 @@
 // Log-Linear Complexity", pyramid paragraph; rcap.io post, "Think of the keys
 // as leaves of a tree".
 //
+// The keys are the contiguous cache or a pool of pages (KeyPages).
+//
 // Two launches per call:
 //  build_lower: one CTA per 16 consecutive leaves of one (sequence, key head).
 //    It streams the CTA's 1024 keys once (16-byte vector loads, 16 threads per
@@ -54,9 +56,9 @@ __device__ __forceinline__ void leaf_mean_dims(const void* keys, int64_t row_str
 }
 
 template <int D>
-__global__ void __launch_bounds__(256) build_lower_kernel(Prob pr, Pyr s, const void* __restrict__ k,
+__global__ void __launch_bounds__(256) build_lower_kernel(Prob pr, Pyr s, const void* __restrict__ k, KeyPages kp,
                                                           const int32_t* __restrict__ seq_lens,
-                                                          float* __restrict__ pyr) {
+                                                          float* __restrict__ pyr, int32_t* __restrict__ status) {
   constexpr int TPL = 16;            // threads per leaf row
   constexpr int DPT = D / TPL;       // dims per thread (8 or 4)
   __shared__ float sm[kLeavesPerCta][D];
@@ -72,12 +74,20 @@ __global__ void __launch_bounds__(256) build_lower_kernel(Prob pr, Pyr s, const 
 
   // level 1: leaf means
   {
-    const int64_t cnt = leaf < s.nb ? node_count(s, 1, leaf, len) : 0;
+    int64_t cnt = leaf < s.nb ? node_count(s, 1, leaf, len) : 0;
     const size_t esz = bf16 ? 2 : 4;
-    const char* kp = reinterpret_cast<const char*>(k) +
-                     ((bh * s.N + leaf * s.C) * D + c0) * esz;
+    if (kp.table && cnt > 0) {
+      const int32_t pg = kp.table[b * kp.max_pages + leaf];
+      if (pg < 0 || pg >= kp.num_pages) {  // a page outside the pool is not read
+        if (c0 == 0) set_status(status, PISA_DEV_BAD_INDEX);
+        cnt = 0;
+      }
+    }
+    const char* kb = cnt > 0 ? reinterpret_cast<const char*>(k) +
+                                   (leaf_row(kp, pr.Hkv, s.N, s.C, b, h, leaf) * D + c0) * esz
+                             : nullptr;
     float m[DPT];
-    leaf_mean_dims<DPT>(kp, D, bf16, cnt, m);
+    leaf_mean_dims<DPT>(kb, D, bf16, cnt, m);
 #pragma unroll
     for (int c = 0; c < DPT; ++c) sm[ll][c0 + c] = m[c];
     if (leaf < s.nb) {
@@ -152,13 +162,13 @@ __global__ void __launch_bounds__(256) build_upper_kernel(Prob pr, Pyr s, const 
   }
 }
 
-cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, const int32_t* seq_lens,
-                                 float* pyr, cudaStream_t st) {
+cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, const KeyPages& kp,
+                                 const int32_t* seq_lens, float* pyr, int32_t* status, cudaStream_t st) {
   if (pr.B == 0 || pr.Hkv == 0 || s.nb == 0) return cudaSuccess;
   dim3 g1((unsigned)ceil_div64(s.nb, kLeavesPerCta), (unsigned)pr.Hkv, (unsigned)pr.B);
   note_launch();
-  if (pr.d == 128) build_lower_kernel<128><<<g1, 256, 0, st>>>(pr, s, k, seq_lens, pyr);
-  else build_lower_kernel<64><<<g1, 256, 0, st>>>(pr, s, k, seq_lens, pyr);
+  if (pr.d == 128) build_lower_kernel<128><<<g1, 256, 0, st>>>(pr, s, k, kp, seq_lens, pyr, status);
+  else build_lower_kernel<64><<<g1, 256, 0, st>>>(pr, s, k, kp, seq_lens, pyr, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || s.L <= kLowerLevels) return e;
   dim3 g2((unsigned)pr.Hkv, (unsigned)pr.B);

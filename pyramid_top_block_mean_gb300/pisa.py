@@ -36,7 +36,7 @@ EXPORTED = ["pisa_abi_version", "pisa_status_string", "pisa_pyramid_levels", "pi
             "pisa_pyramid_bytes", "pisa_workspace_bytes", "pisa_build_pyramid", "pisa_select_prefill",
             "pisa_prefill_route", "pisa_prefill_leaves", "pisa_select_decode", "pisa_select_flat",
             "pisa_read_device_status", "pisa_select_prefill_static", "pisa_kernel_launches",
-            "pisa_attend_prefill"]
+            "pisa_attend_prefill", "pisa_build_pyramid_paged", "pisa_select_decode_paged"]
 
 
 class Params(ctypes.Structure):
@@ -73,6 +73,11 @@ _lib.pisa_select_decode.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t
 _lib.pisa_select_decode.restype = ctypes.c_int
 _lib.pisa_select_flat.argtypes = [_P, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
 _lib.pisa_select_flat.restype = ctypes.c_int
+_lib.pisa_build_pyramid_paged.argtypes = [_P, _vp, ctypes.c_int64, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+_lib.pisa_build_pyramid_paged.restype = ctypes.c_int
+_lib.pisa_select_decode_paged.argtypes = [_P, _vp, _vp, ctypes.c_int64, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp,
+                                          _vp, _vp, _vp]
+_lib.pisa_select_decode_paged.restype = ctypes.c_int
 _lib.pisa_attend_prefill.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
 _lib.pisa_attend_prefill.restype = ctypes.c_int
 _lib.pisa_read_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32), _vp]
@@ -198,6 +203,27 @@ def select_flat(p: Params, q, pyramid, ws, out_idx, out_score=None, stream=None,
     return rc
 
 
+def build_pyramid_paged(p: Params, k_pages, page_table, pyramid, ws, seq_lens=None, stream=None,
+                        check: bool = True) -> int:
+    """k_pages [num_pages, H_kv, C, d]; page_table int32 [B, ceil(N / C)]."""
+    rc = _lib.pisa_build_pyramid_paged(ctypes.byref(p), _ptr(k_pages), k_pages.shape[0], _ptr(page_table),
+                                       _ptr(seq_lens), _ptr(pyramid), _ptr(ws), ws.numel() * ws.element_size(),
+                                       _stream(stream))
+    if check:
+        _check(rc, "pisa_build_pyramid_paged")
+    return rc
+
+
+def select_decode_paged(p: Params, q, k_pages, page_table, seq_lens, pyramid, ws, out_idx, out_score=None,
+                        trace=None, stream=None, check: bool = True) -> int:
+    rc = _lib.pisa_select_decode_paged(ctypes.byref(p), _ptr(q), _ptr(k_pages), k_pages.shape[0], _ptr(page_table),
+                                       _ptr(seq_lens), _ptr(pyramid), _ptr(ws), ws.numel() * ws.element_size(),
+                                       _ptr(out_idx), _ptr(out_score), _ptr(trace), _stream(stream))
+    if check:
+        _check(rc, "pisa_select_decode_paged")
+    return rc
+
+
 def attend_prefill(p: Params, q, k, v, idx, ws, out, stream=None, check: bool = True) -> int:
     rc = _lib.pisa_attend_prefill(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(idx), _ptr(ws),
                                   0 if ws is None else ws.numel() * ws.element_size(), _ptr(out),
@@ -247,6 +273,14 @@ class Selector:
     def decode(self, q, k_cache, seq_lens, trace=None, stream=None):
         select_decode(self.p, q, k_cache, seq_lens, self.pyramid, self.ws, self.out_idx, self.out_score, trace,
                       stream)
+        return self.out_idx, self.out_score
+
+    def build_paged(self, k_pages, page_table, seq_lens=None, stream=None):
+        build_pyramid_paged(self.p, k_pages, page_table, self.pyramid, self.ws, seq_lens, stream)
+
+    def decode_paged(self, q, k_pages, page_table, seq_lens, trace=None, stream=None):
+        select_decode_paged(self.p, q, k_pages, page_table, seq_lens, self.pyramid, self.ws, self.out_idx,
+                            self.out_score, trace, stream)
         return self.out_idx, self.out_score
 
     def flat(self, q, k=None, stream=None, build: bool = True):

@@ -100,3 +100,23 @@ def test_params_without_the_scorer_field_are_rejected(pisa):
     assert pisa.workspace_bytes(p, 0) == 0
     for sc in (0, 1, 2):
         assert pisa.workspace_bytes(pisa.make_params(1, 4096, 16, 4, 128, K=8, scorer=sc), 0) > 0
+
+
+def test_paged_entry_points_check_their_pool_before_launch(pisa):
+    L = pisa.lib()
+    p = pisa.make_params(2, 4096, 16, 4, 128, K=8)
+    a = ctypes.c_void_p(0x10000)
+    mis = ctypes.c_void_p(0x10008)
+    odd = ctypes.c_void_p(0x10002)
+    big = 1 << 40
+    # build: null table, no pages, misaligned pool or table, small workspace
+    assert L.pisa_build_pyramid_paged(ctypes.byref(p), a, 10, None, None, a, a, big, None) == -1
+    assert L.pisa_build_pyramid_paged(ctypes.byref(p), a, 0, a, None, a, a, big, None) == -1
+    assert L.pisa_build_pyramid_paged(ctypes.byref(p), mis, 10, a, None, a, a, big, None) == -3
+    assert L.pisa_build_pyramid_paged(ctypes.byref(p), a, 10, odd, None, a, a, big, None) == -3
+    assert L.pisa_build_pyramid_paged(ctypes.byref(p), a, 10, a, None, a, a, 16, None) == -4
+    # decode: the same, plus the decode arguments
+    assert L.pisa_select_decode_paged(ctypes.byref(p), a, a, 10, None, a, a, a, big, a, None, None, None) == -1
+    assert L.pisa_select_decode_paged(ctypes.byref(p), a, a, 0, a, a, a, a, big, a, None, None, None) == -1
+    assert L.pisa_select_decode_paged(ctypes.byref(p), a, mis, 10, a, a, a, a, big, a, None, None, None) == -3
+    assert L.pisa_select_decode_paged(ctypes.byref(p), a, a, 10, a, None, a, a, big, a, None, None, None) == -1
