@@ -304,6 +304,25 @@ pisa_status pisa_attend_prefill(const pisa_params* p, const void* q,
                                 const int32_t* idx, void* ws, size_t ws_bytes,
                                 void* out, void* stream);
 
+/* Attention of one decode step over its selection (the decode counterpart
+ * of pisa_attend_prefill).  For sequence b the query sits at position
+ * t = seq_lens[b] - 1; each query head g of key head h's group gets
+ *   out[b, h*G+g] = sum_i softmax_i(s q . k_i) v_i
+ * over the key positions i <= t of the blocks listed in idx[b, h, :].
+ *   q    bf16 [B, H_q, d];  k_cache, v_cache bf16 [B, H_kv, N, d] (DEVICE)
+ *   idx  int32 [B, H_kv, K+3] (DEVICE), e.g. out_idx of pisa_select_decode;
+ *        the same entry rules as pisa_attend_prefill
+ *   out  bf16 [B, H_q, d] (DEVICE); ws at least
+ *        pisa_workspace_bytes(p, PISA_MODE_DECODE) bytes (status word).
+ * dtype must be PISA_BF16 and the capacity N a multiple of 16
+ * (PISA_ERR_UNSUPPORTED otherwise).  A sequence length outside [1, N] sets
+ * PISA_DEV_BAD_SEQ_LEN and writes a zero row. */
+pisa_status pisa_attend_decode(const pisa_params* p, const void* q,
+                               const void* k_cache, const void* v_cache,
+                               const int32_t* seq_lens, const int32_t* idx,
+                               void* ws, size_t ws_bytes, void* out,
+                               void* stream);
+
 /* Synchronises `stream`, then copies the workspace status word into
  * *device_code (PISA_DEV_*).  Returns PISA_ERR_DEVICE when it is non-zero. */
 pisa_status pisa_read_device_status(const void* ws, int32_t* device_code,

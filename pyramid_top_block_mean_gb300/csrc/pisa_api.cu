@@ -389,6 +389,25 @@ pisa_status pisa_attend_prefill(const pisa_params* p, const void* q, const void*
   return cuda_status(launch_attend(pr, s, w, (char*)ws, q, k, v, idx, out, sm_count(dev), st));
 }
 
+pisa_status pisa_attend_decode(const pisa_params* p, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* seq_lens, const int32_t* idx, void* ws, size_t ws_bytes, void* out,
+                               void* stream) {
+  Prob pr; Pyr s;
+  pisa_status rc = check_params(p, &pr, &s);
+  if (rc != PISA_OK) return rc;
+  if (pr.B * pr.Hkv == 0) return PISA_OK;
+  if (pr.N == 0) return PISA_ERR_INVALID_ARG;
+  if (pr.dtype != PISA_BF16 || pr.N % 16 != 0) return PISA_ERR_UNSUPPORTED;  // 16-key chunks never pass N
+  if (!q || !k_cache || !v_cache || !seq_lens || !idx || !ws || !out) return PISA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(ws) || !aligned16(out) ||
+      ((uintptr_t)seq_lens & 3u) || ((uintptr_t)idx & 3u))
+    return PISA_ERR_MISALIGNED;
+  if (ws_bytes < decode_ws_bytes(pr, s)) return PISA_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return PISA_ERR_CUDA;
+  return cuda_status(launch_attend_decode(pr, s, q, k_cache, v_cache, seq_lens, idx, out, (int32_t*)ws, st));
+}
+
 pisa_status pisa_read_device_status(const void* ws, int32_t* device_code, void* stream) {
   if (!ws || !device_code) return PISA_ERR_INVALID_ARG;
   int32_t v = 0;

@@ -98,6 +98,9 @@ cudaError_t launch_decode(const Prob& pr, const Pyr& s, const void* q, const voi
                           cudaStream_t st);
 cudaError_t launch_attend(const Prob& pr, const Pyr& s, const AttendWs& w, char* ws, const void* q, const void* k,
                           const void* v, const int32_t* idx, void* out, int num_sms, cudaStream_t st);
+cudaError_t launch_attend_decode(const Prob& pr, const Pyr& s, const void* q, const void* k, const void* v,
+                                 const int32_t* seq_lens, const int32_t* idx, void* out, int32_t* status,
+                                 cudaStream_t st);
 cudaError_t launch_flat(const Prob& pr, const Pyr& s, const void* q, const float* pyr, char* ws,
                         int32_t* out_idx, float* out_score, int num_sms, cudaStream_t st);
 

@@ -36,7 +36,7 @@ EXPORTED = ["pisa_abi_version", "pisa_status_string", "pisa_pyramid_levels", "pi
             "pisa_pyramid_bytes", "pisa_workspace_bytes", "pisa_build_pyramid", "pisa_select_prefill",
             "pisa_prefill_route", "pisa_prefill_leaves", "pisa_select_decode", "pisa_select_flat",
             "pisa_read_device_status", "pisa_select_prefill_static", "pisa_kernel_launches",
-            "pisa_attend_prefill", "pisa_build_pyramid_paged", "pisa_select_decode_paged"]
+            "pisa_attend_prefill", "pisa_build_pyramid_paged", "pisa_select_decode_paged", "pisa_attend_decode"]
 
 
 class Params(ctypes.Structure):
@@ -78,6 +78,8 @@ _lib.pisa_build_pyramid_paged.restype = ctypes.c_int
 _lib.pisa_select_decode_paged.argtypes = [_P, _vp, _vp, ctypes.c_int64, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp,
                                           _vp, _vp, _vp]
 _lib.pisa_select_decode_paged.restype = ctypes.c_int
+_lib.pisa_attend_decode.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
+_lib.pisa_attend_decode.restype = ctypes.c_int
 _lib.pisa_attend_prefill.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp, _vp]
 _lib.pisa_attend_prefill.restype = ctypes.c_int
 _lib.pisa_read_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32), _vp]
@@ -233,6 +235,15 @@ def attend_prefill(p: Params, q, k, v, idx, ws, out, stream=None, check: bool = 
     return rc
 
 
+def attend_decode(p: Params, q, k_cache, v_cache, seq_lens, idx, ws, out, stream=None, check: bool = True) -> int:
+    rc = _lib.pisa_attend_decode(ctypes.byref(p), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), _ptr(idx),
+                                 _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _ptr(out),
+                                 _stream(stream))
+    if check:
+        _check(rc, "pisa_attend_decode")
+    return rc
+
+
 def read_device_status(ws: torch.Tensor, stream=None) -> int:
     code = ctypes.c_int32(0)
     rc = _lib.pisa_read_device_status(_ptr(ws), ctypes.byref(code), _stream(stream))
@@ -295,16 +306,24 @@ class Selector:
 
 class Attention:
     """Owns the workspace and output of block-sparse attention over a
-    selection (pisa_attend_prefill) for one problem shape."""
+    selection for one problem shape: prefill (pisa_attend_prefill, every
+    query position) or decode (pisa_attend_decode, one query per sequence)."""
 
-    def __init__(self, p: Params, device="cuda"):
+    def __init__(self, p: Params, device="cuda", mode: str = "prefill"):
         self.p = p
+        self.mode = mode
         self.device = torch.device(device)
-        self.ws = torch.empty(max(workspace_bytes(p, MODE_ATTEND), 256), dtype=torch.uint8, device=self.device)
-        self.out = torch.empty(p.B, p.H_q, p.N, p.d, dtype=torch.bfloat16, device=self.device)
+        m = MODE_ATTEND if mode == "prefill" else MODE_DECODE
+        self.ws = torch.empty(max(workspace_bytes(p, m), 256), dtype=torch.uint8, device=self.device)
+        shape = (p.B, p.H_q, p.N, p.d) if mode == "prefill" else (p.B, p.H_q, p.d)
+        self.out = torch.empty(shape, dtype=torch.bfloat16, device=self.device)
 
     def __call__(self, q, k, v, idx, stream=None):
         attend_prefill(self.p, q, k, v, idx, self.ws, self.out, stream)
+        return self.out
+
+    def decode(self, q, k_cache, v_cache, seq_lens, idx, stream=None):
+        attend_decode(self.p, q, k_cache, v_cache, seq_lens, idx, self.ws, self.out, stream)
         return self.out
 
     def device_status(self, stream=None) -> int:

@@ -1,12 +1,15 @@
-"""GPU parity of block-sparse attention over a selection (pisa_attend_prefill)
-against the fp64 oracle, through the C ABI.
+"""GPU parity of block-sparse attention over a selection (pisa_attend_prefill
+for every query position, pisa_attend_decode for one decode query per
+sequence) against the fp64 oracle, through the C ABI.
 
 Tolerance.  The kernel rounds three times to bf16: the probabilities fed to
 the P V product (relative 2^-9 each, so at most 2^-9 max|v| on a block's
 normalised output), each block's normalised partial (2^-9 of a convex
 combination of values) and the final output (2^-9 |o|).  The fp32 score
 accumulation and ex2/lg2 approximations add relative errors near 1e-5 to the
-weights.  The bound used is 3 * 2^-9 * max|v| + 1e-4 per element.
+weights.  The bound used is 3 * 2^-9 * max|v| + 1e-4 per element.  The
+decode kernel keeps its running output in fp32 and rounds only P and the
+output, so the same bound covers it.
 """
 import numpy as np
 import pytest
@@ -142,4 +145,66 @@ def test_attend_full_size_sampled(pisa, N):
     got = torch.stack([outc[0, h * G:(h + 1) * G, t] for (_, h, t) in sel]).double().numpy()
     err = np.abs(got - ref).max()
     print(f"N={N}: max err {err:.3e} over {len(sel)} queries (tol {tol(v):.3e})")
+    assert err <= tol(v), err
+
+
+def decode_reference(s, qd, kc, v, lens, idx_rows):
+    """The oracle's attention for the decode queries: the idx rows [B, Hkv, W]
+    placed at t = len - 1 of a full -1 array, q passed as rows."""
+    Wd = s.K + 3
+    full = np.full((s.B, s.Hkv, s.N, Wd), -1, np.int32)
+    sel = []
+    for b in range(s.B):
+        for h in range(s.Hkv):
+            full[b, h, lens[b] - 1] = idx_rows[b, h]
+            sel.append((b, h, lens[b] - 1))
+    G = s.G
+    rows = np.stack([qd[b, h * G:(h + 1) * G].double().numpy() for (b, h, _) in sel])
+    o = oracle.Oracle.from_shape(s)
+    return o.attend(rows, kc, v, full, sel=sel, qrows=True)  # [B*Hkv, G, d]
+
+
+@pytest.mark.parametrize("d,G,K", [(128, 4, 8), (64, 2, 4), (128, 8, 32), (64, 1, 16)])
+def test_attend_decode_matches_oracle(pisa, d, G, K):
+    s = W.Shape(B=5, N=4096 + 64, Hq=2 * G, Hkv=2, d=d, K=K)
+    q_steps, kc = W.decode_inputs(s, 30 + K, steps=1)
+    v = W.values(s, 30 + K)
+    lens = [4096 + 1, 2048 + 64, 1025, 130, 3]
+    p = pisa.params_from_shape(s)
+    sel = pisa.Selector(p, mode="decode", with_scores=False)
+    kcd, vd = kc.cuda(), v.cuda()
+    ld = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    sel.build(kcd, ld - 1)
+    idx, _ = sel.decode(q_steps[0].cuda(), kcd, ld)
+    at = pisa.Attention(p, mode="decode")
+    out = at.decode(q_steps[0].cuda(), kcd, vd, ld, idx)
+    torch.cuda.synchronize()
+    assert sel.device_status() == 0 and at.device_status() == 0
+    ref = decode_reference(s, q_steps[0], kc, v, lens, idx.cpu().numpy())
+    got = out.cpu().double().numpy().reshape(s.B * s.Hkv, G, d)
+    err = np.abs(got - ref).max()
+    print(f"decode d={d} G={G} K={K}: max err {err:.3e} (tol {tol(v):.3e})")
+    assert err <= tol(v), err
+
+
+def test_attend_decode_hand_made_rows(pisa):
+    s = W.Shape(B=4, N=1024, Hq=8, Hkv=2, d=128, K=4)
+    q_steps, kc = W.decode_inputs(s, 8, steps=1)
+    v = W.values(s, 8)
+    lens = [1000, 640, 65, 1]
+    Wd = s.K + 3
+    g = torch.Generator().manual_seed(3)
+    idx = torch.randint(-3, 20, (s.B, s.Hkv, Wd), generator=g, dtype=torch.int32)
+    for b, n in enumerate(lens):
+        idx[b, :, 0] = (n - 1) // 64  # the query's own block
+        idx[b, :, 1] = idx[b, :, 0]   # repeated
+    p = pisa.params_from_shape(s)
+    at = pisa.Attention(p, mode="decode")
+    ld = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = at.decode(q_steps[0].cuda(), kc.cuda(), v.cuda(), ld, idx.cuda())
+    torch.cuda.synchronize()
+    assert at.device_status() == 0
+    ref = decode_reference(s, q_steps[0], kc, v, lens, idx.numpy())
+    got = out.cpu().double().numpy().reshape(s.B * s.Hkv, s.G, s.d)
+    err = np.abs(got - ref).max()
     assert err <= tol(v), err
