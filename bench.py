@@ -540,7 +540,37 @@ def side_measurements(args, dev, st, rank):
     walk_bytes = s.B * s.Hkv * rows * s.d * 4
     step_bytes = leaf_bytes + walk_bytes + s.B * s.Hq * s.d * 2
     pk = peaks()
-    del kc
+    # attention of the same decode steps over their selections (values iid N(0,1))
+    vc = torch.randn(s.B, s.Hkv, s.N, s.d, device=dev, generator=g, dtype=torch.bfloat16)
+    at = pisa.Attention(p, device=dev, mode="decode")
+    idx_steps = []
+    ds.build(kc, torch.full((s.B,), W.DECODE_CACHED, dtype=torch.int32, device=dev))
+    for i in range(W.DECODE_STEPS):
+        ds.decode(qd[i], kc, lens[i], stream=st)
+        idx_steps.append(ds.out_idx.clone())
+    torch.cuda.synchronize(dev)
+    for _ in range(2):
+        at.decode(qd[0], kc, vc, lens[0], idx_steps[0], stream=st)
+    torch.cuda.synchronize(dev)
+    a.record(st)
+    for i in range(W.DECODE_STEPS):
+        at.decode(qd[i], kc, vc, lens[i], idx_steps[i], stream=st)
+    b.record(st)
+    torch.cuda.synchronize(dev)
+    at_us = a.elapsed_time(b) / W.DECODE_STEPS * 1e3
+    # keys read: 64 per listed block before the query's own block, t mod 64 + 1 in it
+    n_keys = 0
+    for i in range(W.DECODE_STEPS):
+        t_ = W.DECODE_CACHED + i
+        ids = idx_steps[i]
+        qb_ = t_ // s.C
+        n_keys += int(((ids >= 0) & (ids < qb_)).sum().item()) * s.C + int((ids == qb_).sum().item()) * (t_ % s.C + 1)
+    at_bytes = n_keys / W.DECODE_STEPS * s.d * 2 * 2 + 2 * s.B * s.Hq * s.d * 2
+    attn = {"us_per_step": at_us, "selection_plus_attention_us": us + at_us,
+            "roofline": {"bound": "hbm", "bytes_per_step": at_bytes, "achieved": at_bytes / (at_us * 1e-6) / 1e9,
+                         "peak": pk["hbm"], "unit": "GB/s", "frac": at_bytes / (at_us * 1e-6) / 1e9 / pk["hbm"],
+                         "bytes": "keys and values of the attended positions, q and the output"}}
+    del kc, vc, at
     torch.cuda.empty_cache()
     return {"sweep": sweep, "attention": attention, "decode": {"us_per_step": us, "steps": W.DECODE_STEPS,
                                        "workload": "B=64, 131072 cached keys, Hq=32 Hkv=8 d=128 bf16 K=32",
@@ -550,7 +580,8 @@ def side_measurements(args, dev, st, rank):
                                                     "achieved": step_bytes / (us * 1e-6) / 1e9,
                                                     "peak": pk["hbm"], "unit": "GB/s",
                                                     "frac": step_bytes / (us * 1e-6) / 1e9 / pk["hbm"],
-                                                    "bytes": "leaf keys + walked child rows (fp32) + q"}}}
+                                                    "bytes": "leaf keys + walked child rows (fp32) + q"},
+                                       "attention": attn}}
 
 
 # ----------------------------------------------------------- CPU oracle
@@ -635,7 +666,8 @@ def profile_case(name: str):
     """One small invocation per kernel, sized for profiler captures: the 64K
     prefill point (build, route, leaves, flat, attention over the selection;
     inputs 400 MB > L2), one decode step of 8 sequences x 131073 keys (2.1 GB
-    cache), or the 256K selection followed by two attention calls (for the
+    cache each for keys and values, with the attention over the selection),
+    or the 256K selection followed by two attention calls (for the
     attention's launch list; 15 GB on the device, one-pass metrics only)."""
     import torch
     from pyramid_top_block_mean_gb300 import pisa
@@ -681,9 +713,13 @@ def profile_case(name: str):
         p = pisa.params_from_shape(s)
         ds = pisa.Selector(p, mode="decode")
         ds.build(kc, torch.full((s.B,), W.DECODE_CACHED, dtype=torch.int32, device="cuda"))
-        ds.decode(qd, kc, torch.full((s.B,), W.DECODE_CACHED + 1, dtype=torch.int32, device="cuda"))
+        ln = torch.full((s.B,), W.DECODE_CACHED + 1, dtype=torch.int32, device="cuda")
+        ds.decode(qd, kc, ln)
+        vc = torch.randn(s.B, s.Hkv, s.N, s.d, device="cuda", generator=g, dtype=torch.bfloat16)
+        at = pisa.Attention(p, mode="decode")
+        at.decode(qd, kc, vc, ln, ds.out_idx)
         torch.cuda.synchronize()
-        status = ds.device_status()
+        status = max(ds.device_status(), at.device_status())
     print(json.dumps({"profile_case": name, "device_status": status}))
     if status != 0:
         sys.exit(1)

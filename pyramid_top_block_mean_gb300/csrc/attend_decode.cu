@@ -41,7 +41,8 @@ struct AdSmem {
   uint16_t p[kWarps][kKeysPerChunk][8];  // P tile: [key][head]
   float m[kWarps][8], l[kWarps][8];
   int64_t chunk_key[kWarps][(kMaxSlots / kWarps) * 4];  // first key of each chunk a warp streams
-  int32_t nchunks[kWarps];
+  int32_t blocks[kMaxSlots];
+  int32_t nblocks;
   uint64_t bar[kWarps][kStages];
   int32_t abort;
   int32_t zero;
@@ -94,37 +95,59 @@ __global__ void __launch_bounds__(kThreads) attend_decode_kernel(Prob pr, Pyr s,
   }
   const int64_t t = len - 1, qb = t / s.C;
   volatile int32_t* abort = &sm.abort;
-  if (tid == 0) {
-    // the distinct blocks of the row that hold a key at or before t, dealt
-    // round-robin to the warps; each block is streamed in chunks of 16 keys
-    // up to the chunk that holds t (the capacity is a multiple of 16, so no
-    // chunk runs past it)
+  if (warp == 0) {
+    // the distinct blocks of the row that hold a key at or before t, in slot
+    // order: lane i takes slots i and i + 32; a slot repeating an earlier
+    // one is dropped
     const int32_t* row = idx + bh * W;
-    int32_t blocks[kMaxSlots];
-    int n = 0;
-    for (int i = 0; i < W && i < kMaxSlots; ++i) {
-      const int32_t j = row[i];
-      if (j < 0 || j > qb) continue;
-      bool dup = false;
-      for (int u = 0; u < n; ++u) dup |= blocks[u] == j;
-      if (!dup) blocks[n++] = j;
+    const int32_t r0 = lane < W ? row[lane] : -1, r1 = lane + 32 < W ? row[lane + 32] : -1;
+    const bool ok0 = r0 >= 0 && r0 <= qb, ok1 = r1 >= 0 && r1 <= qb;
+    const unsigned below = (1u << lane) - 1u;
+    const unsigned m0 = __match_any_sync(0xffffffffu, ok0 ? r0 : -1 - lane);  // invalid slots match nothing
+    const unsigned m1 = __match_any_sync(0xffffffffu, ok1 ? r1 : -1 - lane);
+    bool dup1 = (m1 & below) != 0u;
+    for (int u = 0; u < 32; ++u) {
+      const int32_t o = __shfl_sync(0xffffffffu, ok0 ? r0 : -1, u);  // every lane takes part
+      dup1 |= ok1 && o == r1;
     }
-    for (int w = 0; w < kWarps; ++w) sm.nchunks[w] = 0;
-    for (int i = 0; i < n; ++i) {
-      const int w = i % kWarps;
-      const int64_t k0 = (int64_t)blocks[i] * s.C;
-      const int64_t kend = k0 + s.C - 1 < t ? k0 + s.C - 1 : t;  // last key read
-      for (int64_t kk = k0; kk <= kend; kk += kKeysPerChunk) sm.chunk_key[w][sm.nchunks[w]++] = kk;
+    const bool keep0 = ok0 && (m0 & below) == 0u, keep1 = ok1 && !dup1;
+    const unsigned b0 = __ballot_sync(0xffffffffu, keep0), b1 = __ballot_sync(0xffffffffu, keep1);
+    if (keep0) sm.blocks[__popc(b0 & below)] = r0;
+    if (keep1) sm.blocks[__popc(b0) + __popc(b1 & below)] = r1;
+    if (lane == 0) {
+      sm.nblocks = __popc(b0) + __popc(b1);
+      for (int w = 0; w < kWarps; ++w)
+        for (int u = 0; u < kStages; ++u) ptx::mbar_init(ptx::smem_u32(&sm.bar[w][u]), 1);
+      sm.abort = 0;
+      sm.zero = 0;
+      ptx::fence_mbar_init();
+      ptx::fence_proxy_async_smem();
     }
-    for (int w = 0; w < kWarps; ++w)
-      for (int u = 0; u < kStages; ++u) ptx::mbar_init(ptx::smem_u32(&sm.bar[w][u]), 1);
-    sm.abort = 0;
-    sm.zero = 0;
-    ptx::fence_mbar_init();
-    ptx::fence_proxy_async_smem();
   }
   __syncthreads();
-  const int nch = sm.nchunks[warp];
+  // the blocks are dealt round-robin to the warps; lane k of a warp lists the
+  // 16-key chunks of the warp's k-th block, up to the chunk that holds t (the
+  // capacity is a multiple of 16, so no chunk runs past it)
+  int nch;
+  {
+    const int i = warp + kWarps * lane;
+    int cnt = 0;
+    int64_t k0 = 0;
+    if (i < sm.nblocks) {
+      k0 = (int64_t)sm.blocks[i] * s.C;
+      const int64_t kend = k0 + s.C - 1 < t ? k0 + s.C - 1 : t;  // last key read
+      cnt = (int)((kend - k0) / kKeysPerChunk) + 1;
+    }
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    for (int c = 0; c < cnt; ++c) sm.chunk_key[warp][x - cnt + c] = k0 + (int64_t)kKeysPerChunk * c;
+    nch = __shfl_sync(0xffffffffu, x, 31);
+    __syncwarp();
+  }
 
   // q fragments (the B operand of S = K q): head grp (zero past G), dims
   // 32 kk + 8 tig + {0..7}
@@ -166,14 +189,16 @@ __global__ void __launch_bounds__(kThreads) attend_decode_kernel(Prob pr, Pyr s,
     const unsigned char* kbuf = reinterpret_cast<const unsigned char*>(sm.u.kv[warp][st][0]);
     const int64_t key0 = sm.chunk_key[warp][c];
     // S = K q: keys grp and grp + 8 of the chunk, heads 2 tig and 2 tig + 1
-    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f}, e[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // two independent chains
 #pragma unroll
     for (int kk = 0; kk < KT; ++kk) {
       const uint4 a0 = *reinterpret_cast<const uint4*>(kbuf + grp * D * 2 + 64 * kk + 16 * tig);
       const uint4 a1 = *reinterpret_cast<const uint4*>(kbuf + (grp + 8) * D * 2 + 64 * kk + 16 * tig);
       mma16816(d, a0.x, a1.x, a0.y, a1.y, bq[kk][0], bq[kk][1]);
-      mma16816(d, a0.z, a1.z, a0.w, a1.w, bq[kk][2], bq[kk][3]);
+      mma16816(e, a0.z, a1.z, a0.w, a1.w, bq[kk][2], bq[kk][3]);
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) d[j] += e[j];
     // causal mask inside the query's own block, then the online softmax
     const bool v0 = key0 + grp <= t, v1 = key0 + grp + 8 <= t;
     const float x00 = v0 ? d[0] * sc : -INFINITY, x01 = v0 ? d[1] * sc : -INFINITY;

@@ -55,7 +55,9 @@ __device__ __forceinline__ void leaf_mean_dims(const void* keys, int64_t row_str
   for (int c = 0; c < DPT; ++c) out[c] = __fdiv_rn(out[c], n);
 }
 
-template <int D>
+// kPaged: keys through a page table (compiled separately, so the contiguous
+// kernel keeps its registers and occupancy).
+template <int D, bool kPaged>
 __global__ void __launch_bounds__(256) build_lower_kernel(Prob pr, Pyr s, const void* __restrict__ k, KeyPages kp,
                                                           const int32_t* __restrict__ seq_lens,
                                                           float* __restrict__ pyr, int32_t* __restrict__ status) {
@@ -76,16 +78,15 @@ __global__ void __launch_bounds__(256) build_lower_kernel(Prob pr, Pyr s, const 
   {
     int64_t cnt = leaf < s.nb ? node_count(s, 1, leaf, len) : 0;
     const size_t esz = bf16 ? 2 : 4;
-    if (kp.table && cnt > 0) {
+    if (kPaged && cnt > 0) {
       const int32_t pg = kp.table[b * kp.max_pages + leaf];
       if (pg < 0 || pg >= kp.num_pages) {  // a page outside the pool is not read
         if (c0 == 0) set_status(status, PISA_DEV_BAD_INDEX);
         cnt = 0;
       }
     }
-    const char* kb = cnt > 0 ? reinterpret_cast<const char*>(k) +
-                                   (leaf_row(kp, pr.Hkv, s.N, s.C, b, h, leaf) * D + c0) * esz
-                             : nullptr;
+    const int64_t row = kPaged ? (cnt > 0 ? leaf_row(kp, pr.Hkv, s.N, s.C, b, h, leaf) : 0) : bh * s.N + leaf * s.C;
+    const char* kb = reinterpret_cast<const char*>(k) + (row * D + c0) * esz;
     float m[DPT];
     leaf_mean_dims<DPT>(kb, D, bf16, cnt, m);
 #pragma unroll
@@ -167,8 +168,13 @@ cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, co
   if (pr.B == 0 || pr.Hkv == 0 || s.nb == 0) return cudaSuccess;
   dim3 g1((unsigned)ceil_div64(s.nb, kLeavesPerCta), (unsigned)pr.Hkv, (unsigned)pr.B);
   note_launch();
-  if (pr.d == 128) build_lower_kernel<128><<<g1, 256, 0, st>>>(pr, s, k, kp, seq_lens, pyr, status);
-  else build_lower_kernel<64><<<g1, 256, 0, st>>>(pr, s, k, kp, seq_lens, pyr, status);
+  if (kp.table) {
+    if (pr.d == 128) build_lower_kernel<128, true><<<g1, 256, 0, st>>>(pr, s, k, kp, seq_lens, pyr, status);
+    else build_lower_kernel<64, true><<<g1, 256, 0, st>>>(pr, s, k, kp, seq_lens, pyr, status);
+  } else {
+    if (pr.d == 128) build_lower_kernel<128, false><<<g1, 256, 0, st>>>(pr, s, k, kp, seq_lens, pyr, status);
+    else build_lower_kernel<64, false><<<g1, 256, 0, st>>>(pr, s, k, kp, seq_lens, pyr, status);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || s.L <= kLowerLevels) return e;
   dim3 g2((unsigned)pr.Hkv, (unsigned)pr.B);
