@@ -120,3 +120,24 @@ def test_paged_entry_points_check_their_pool_before_launch(pisa):
     assert L.pisa_select_decode_paged(ctypes.byref(p), a, a, 0, a, a, a, a, big, a, None, None, None) == -1
     assert L.pisa_select_decode_paged(ctypes.byref(p), a, mis, 10, a, a, a, a, big, a, None, None, None) == -3
     assert L.pisa_select_decode_paged(ctypes.byref(p), a, a, 10, a, None, a, a, big, a, None, None, None) == -1
+
+
+def test_attention_entry_points_check_their_arguments(pisa):
+    L = pisa.lib()
+    a = ctypes.c_void_p(0x10000)
+    mis = ctypes.c_void_p(0x10008)
+    big = 1 << 40
+    p = pisa.make_params(2, 4096, 16, 4, 128, K=8)
+    # prefill: null and misaligned pointers, a small workspace, fp32 inputs
+    assert L.pisa_attend_prefill(ctypes.byref(p), a, a, None, a, a, big, a, None) == -1
+    assert L.pisa_attend_prefill(ctypes.byref(p), a, a, mis, a, a, big, a, None) == -3
+    assert L.pisa_attend_prefill(ctypes.byref(p), a, a, a, a, a, 16, a, None) == -4
+    f32 = pisa.make_params(2, 4096, 16, 4, 128, K=8, dtype="fp32")
+    assert L.pisa_attend_prefill(ctypes.byref(f32), a, a, a, a, a, big, a, None) == -2
+    assert pisa.workspace_bytes(p, pisa.MODE_ATTEND) > 2 * 2 * 16 * 4096 * 11 * 128
+    # decode: the capacity must be a multiple of 16
+    odd = pisa.make_params(2, 4096 + 8, 16, 4, 128, K=8)
+    assert L.pisa_attend_decode(ctypes.byref(odd), a, a, a, a, a, a, big, a, None) == -2
+    assert L.pisa_attend_decode(ctypes.byref(p), a, a, None, a, a, a, big, a, None) == -1
+    assert L.pisa_attend_decode(ctypes.byref(p), a, a, a, a, a, a, 16, a, None) == -4
+    assert L.pisa_attend_decode(ctypes.byref(f32), a, a, a, a, a, a, big, a, None) == -2

@@ -76,3 +76,18 @@ def test_clock_sampler_parses_reasons():
                 "garbage"]
     r = cs.stop()
     assert r["sm_mhz"] == 1850 and r["sm_max_mhz"] == 2070 and r["reasons"] == ["sw_power_cap"]
+
+
+def test_attention_work_counts_attended_keys_by_brute_force():
+    s = W.Shape(B=1, N=64 * 9 + 21, Hq=8, Hkv=2, d=16, K=3)
+    g = torch.Generator().manual_seed(2)
+    idx = torch.randint(-2, 12, (s.B, s.Hkv, s.N, s.K + 3), generator=g, dtype=torch.int32)
+    flops, bytes_, n_keys = bench.attention_work(s, idx)
+    n = 0
+    for h in range(s.Hkv):
+        for t in range(s.N):
+            for j in idx[0, h, t].tolist():
+                n += sum(1 for i in range(j * s.C, (j + 1) * s.C) if 0 <= j and i <= t)
+    assert n_keys == n
+    assert flops == 4.0 * s.d * n * s.G
+    assert bytes_ == 2 * (s.Hq * s.N * s.d * 2) + 2 * (s.Hkv * s.N * s.d * 2) + idx.numel() * 4
