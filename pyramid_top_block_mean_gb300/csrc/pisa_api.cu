@@ -243,8 +243,10 @@ static pisa_status prefill_checks(const pisa_params* p, Prob* pr, Pyr* s, Prefil
   if (((uintptr_t)out_idx & 3u) || ((uintptr_t)out_score & 3u) || ((uintptr_t)trace & 3u))
     return PISA_ERR_MISALIGNED;
   if (ws_bytes < w->total) return PISA_ERR_WORKSPACE;
-  // pair counts and TMA row coordinates are 32-bit
+  // pair counts, tile indices and TMA row coordinates are 32-bit; the bucket
+  // grid (query chunks x level-2 nodes) grows with N^2
   if (pr->B * pr->Hkv * pr->N * pr->K >= ((int64_t)1 << 31)) return PISA_ERR_UNSUPPORTED;
+  if (w->max_tiles >= ((int64_t)1 << 31)) return PISA_ERR_UNSUPPORTED;
   return PISA_OK;
 }
 
@@ -380,8 +382,10 @@ pisa_status pisa_attend_prefill(const pisa_params* p, const void* q, const void*
     return PISA_ERR_MISALIGNED;
   const AttendWs w = attend_ws_layout(pr, s);
   if (ws_bytes < w.total) return PISA_ERR_WORKSPACE;
-  // pair counts, tile indices and TMA row coordinates are 32-bit
+  // pair counts, tile indices and TMA row coordinates are 32-bit; the bucket
+  // grid (query chunks x blocks) grows with N^2
   if (pr.B * pr.Hkv * pr.N * (pr.K + 3) >= ((int64_t)1 << 31)) return PISA_ERR_UNSUPPORTED;
+  if (w.max_tiles >= ((int64_t)1 << 31)) return PISA_ERR_UNSUPPORTED;
   cudaStream_t st = (cudaStream_t)stream;
   if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return PISA_ERR_CUDA;
   int dev = 0;

@@ -141,3 +141,15 @@ def test_attention_entry_points_check_their_arguments(pisa):
     assert L.pisa_attend_decode(ctypes.byref(p), a, a, None, a, a, a, big, a, None) == -1
     assert L.pisa_attend_decode(ctypes.byref(p), a, a, a, a, a, a, 16, a, None) == -4
     assert L.pisa_attend_decode(ctypes.byref(f32), a, a, a, a, a, a, big, a, None) == -2
+
+
+def test_bucket_grids_beyond_32_bit_tiles_are_refused_before_launch(pisa):
+    # B * H_kv * N * K fits in 32 bits, but the (query chunk x node) bucket
+    # grid, which grows with N^2, does not
+    L = pisa.lib()
+    a = ctypes.c_void_p(0x10000)
+    huge = 1 << 62
+    p = pisa.make_params(1, 1 << 26, 8, 8, 128, K=1)
+    assert L.pisa_select_prefill(ctypes.byref(p), a, a, a, a, huge, a, None, None, None) == -2
+    pa = pisa.make_params(1, 1 << 26, 4, 4, 128, K=1)
+    assert L.pisa_attend_prefill(ctypes.byref(pa), a, a, a, a, a, huge, a, None) == -2
