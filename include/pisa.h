@@ -214,8 +214,8 @@ pisa_status pisa_select_decode(const pisa_params* p, const void* q,
                                int32_t* out_idx, float* out_score,
                                int32_t* trace, void* stream);
 
-/* Paged key cache (the production decode layout; SURVEY's NEXT row on paged
- * decode).  The raw keys live in a pool of pages of C keys,
+/* Paged key cache (the usual layout of a serving decode cache).  The raw
+ * keys live in a pool of pages of C keys,
  *   k_pages  [num_pages, H_kv, C, d] (DEVICE, dtype of p): page j of
  *            sequence b is page_table[b * ceil(N / C) + j] and holds that
  *            sequence's keys [j C, (j + 1) C) for every key head;
