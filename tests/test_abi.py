@@ -153,3 +153,15 @@ def test_bucket_grids_beyond_32_bit_tiles_are_refused_before_launch(pisa):
     assert L.pisa_select_prefill(ctypes.byref(p), a, a, a, a, huge, a, None, None, None) == -2
     pa = pisa.make_params(1, 1 << 26, 4, 4, 128, K=1)
     assert L.pisa_attend_prefill(ctypes.byref(pa), a, a, a, a, a, huge, a, None) == -2
+
+
+def test_the_product_package_never_touches_the_oracle():
+    # the library and its binding stand alone: no module of the package
+    # imports, loads or builds anything under oracle/
+    import pathlib
+    import re
+    root = pathlib.Path(__file__).resolve().parent.parent / "pyramid_top_block_mean_gb300"
+    pat = re.compile(r"\b(import\s+oracle|from\s+oracle|pisa_oracle|libpisa_oracle)\b")
+    hits = [str(f) for f in root.rglob("*") if f.suffix in (".py", ".cu", ".cuh", ".h", ".cpp")
+            and pat.search(f.read_text(errors="ignore"))]
+    assert hits == []
