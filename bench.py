@@ -212,8 +212,20 @@ def algorithmic_work(s, kept2):
         n = -(-n // 2)
     bytes_ = (s.B * s.Hq * s.N * d * 2 + s.B * s.Hkv * s.N * d * 2 + 2 * s.B * s.Hkv * P * d * 4
               + s.B * s.Hkv * s.N * (K + 3) * 8)
+    q_bytes = s.B * s.Hq * s.N * d * 2
+    k_bytes = s.B * s.Hkv * s.N * d * 2
+    pyr_bytes = s.B * s.Hkv * P * d * 4
+    kept_bytes = s.B * s.Hkv * s.N * K * 4
+    out_bytes = s.B * s.Hkv * s.N * (K + 3) * 8
     return dict(leaf_candidates=int(ncand), leaf_flops=leaf_flops, route_flops=route_flops, bytes=bytes_,
-                pyramid_bytes=s.B * s.Hkv * s.N * d * 2 + s.B * s.Hkv * P * d * 4)
+                pyramid_bytes=k_bytes + pyr_bytes,
+                # route: q read once, the pyramid read once, the kept level-2 nodes written
+                route_bytes=q_bytes + pyr_bytes + kept_bytes,
+                # leaves: q and k read once, the kept nodes read, the outputs written
+                leaf_bytes=q_bytes + k_bytes + kept_bytes + out_bytes)
+
+
+ROUTE_KERNEL = "route_mma_kernel"
 
 
 def load_traffic(name):
@@ -225,6 +237,50 @@ def load_traffic(name):
         return json.load(open(path)).get(name)
     except (OSError, ValueError):
         return None
+
+
+def run_config(s, ws):
+    """The `config` object of both arms' JSON lines (identical by design)."""
+    return {"workload": f"prefill selection, B={s.B} N={s.N} Hq={s.Hq} Hkv={s.Hkv} d={s.d} C={s.C} "
+                        f"g=2 K={s.K} bf16 (build + route + leaf LSE + Top-K)",
+            "B": s.B, "N": s.N, "H_q": s.Hq, "H_kv": s.Hkv, "d": s.d, "C": s.C, "K": s.K,
+            "l2": "inputs (1.3 GB at N=262144) larger than L2; no flush", "parallelism": f"replicas x{ws}"}
+
+
+def stage_rooflines(s, work, stage_ms, pk):
+    """Roofline of each prefill stage and of the whole selector, from the
+    algorithmic work of one step (algorithmic_work) and the measured stage
+    times.  Each stage's roofline time is the slower of its algorithmic bytes
+    at the measured HBM copy bandwidth and its algorithmic flops at the
+    measured bf16 burst peak (the step lasts milliseconds); `bound` names the
+    slower term, `achieved` is that term's work divided by the stage time and
+    frac = achieved / peak = roofline time / stage time."""
+    def one(kernel, bytes_, flops, ms, traffic_name):
+        t_hbm = bytes_ / (pk["hbm"] * 1e9) * 1e3
+        t_tc = flops / (pk["bf16"] * 1e12) * 1e3
+        if t_hbm >= t_tc:
+            r = {"bound": "hbm", "achieved": bytes_ / (ms * 1e-3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
+                 "peak_source": f"{pk['source']} HBM copy"}
+        else:
+            r = {"bound": "tensor", "achieved": flops / (ms * 1e-3) / 1e12, "peak": pk["bf16"], "unit": "TFLOP/s",
+                 "peak_source": f"{pk['source']} bf16 burst"}
+        r.update({"kernel": kernel, "frac": r["achieved"] / r["peak"], "t_roof_ms": max(t_hbm, t_tc),
+                  "t_hbm_ms": t_hbm, "t_tensor_ms": t_tc, "measured_ms": ms, "algorithmic_bytes": bytes_,
+                  "algorithmic_flops": flops,
+                  "traffic": load_traffic(traffic_name) if traffic_name else None})
+        return r
+    out = {
+        "build": one("build_lower_kernel + build_upper_kernel", work["pyramid_bytes"], 0.0, stage_ms["build"],
+                     "build_lower_kernel"),
+        "route": one("route stage (pyramid split + routing kernel)", work["route_bytes"], work["route_flops"],
+                     stage_ms["route"], ROUTE_KERNEL),
+        "leaves": one("leaf stage (bucketing + leaf_tc_kernel + finalize)", work["leaf_bytes"], work["leaf_flops"],
+                      stage_ms["leaves"], "leaf_tc_kernel"),
+    }
+    t_roof = max(work["bytes"] / (pk["hbm"] * 1e9), (work["leaf_flops"] + work["route_flops"]) /
+                 (pk["bf16"] * 1e12)) * 1e3
+    out["selector"] = {"t_roof_ms": t_roof}
+    return out
 
 
 # ------------------------------------------------------------- GPU arm
@@ -290,30 +346,9 @@ def run_pisa(args, ws, rank, local):
     kept2 = sel.ws[256:256 + s.B * s.Hkv * s.N * s.K * 4].view(torch.int32).cpu().numpy()
     work = algorithmic_work(s, kept2)
     pk = peaks()
-    t_roof_ms = max(work["bytes"] / (pk["hbm"] * 1e9), (work["leaf_flops"] + work["route_flops"]) /
-                    (pk["bf16_sus"] * 1e12)) * 1e3
-    # dominant stage and its roofline
-    dom = max(stage, key=stage.get)
-    if dom == "leaves":
-        achieved = work["leaf_flops"] / (stage["leaves"] * 1e-3) / 1e12
-        roof = {"kernel": "leaf stage (bucketing + leaf_tc_kernel + finalize)", "bound": "tensor",
-                "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_sus"], "traffic": load_traffic("leaf_tc_kernel"),
-                "peak_source": f"{pk['source']} bf16 sustained"}
-    elif dom == "route":
-        # the child dot products run on the tensor cores (bf16 MMA, fp32 accumulate)
-        achieved = work["route_flops"] / (stage["route"] * 1e-3) / 1e12
-        roof = {"kernel": "route stage (split_pyramid_kernel + route_mma_kernel)", "bound": "tensor",
-                "achieved": achieved, "peak": pk["bf16_sus"], "unit": "TFLOP/s",
-                "frac": achieved / pk["bf16_sus"], "traffic": load_traffic("route_mma_kernel"),
-                "peak_source": f"{pk['source']} bf16 sustained",
-                "note": "algorithmic flops = 2 d G per child summary scored; the kernel is bound by L1 "
-                        "data-pipe wavefronts and issue, not by the tensor pipe"}
-    else:
-        achieved = work["pyramid_bytes"] / (stage["build"] * 1e-3) / 1e9
-        roof = {"kernel": "build_lower_kernel + build_upper_kernel", "bound": "hbm", "achieved": achieved,
-                "peak": pk["hbm"], "unit": "GB/s", "frac": achieved / pk["hbm"],
-                "traffic": load_traffic("build_lower_kernel"), "peak_source": f"{pk['source']} copy"}
+    rl = stage_rooflines(s, work, stage, pk)
+    t_roof_ms = rl["selector"]["t_roof_ms"]
+    roof = rl[max(stage, key=stage.get)]
 
     # end to end through the public API with host buffers: every step copies
     # its q and k from pinned host memory and reads its indices back.  Steps
@@ -383,14 +418,12 @@ def run_pisa(args, ws, rank, local):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded iid N(0,1) q and k)",
-            "config": {"workload": f"prefill selection, B={s.B} N={s.N} Hq={s.Hq} Hkv={s.Hkv} d={s.d} C={s.C} "
-                                   f"g=2 K={s.K} bf16 (build + route + leaf LSE + Top-K)",
-                       "B": s.B, "N": s.N, "H_q": s.Hq, "H_kv": s.Hkv, "d": s.d, "C": s.C, "K": s.K,
-                       "l2": "inputs (1.3 GB) larger than L2; no flush", "parallelism": f"replicas x{ws}"},
+            "config": run_config(s, ws),
             "stage_ms": stage, "selector_roofline": {
                 "t_roof_ms": t_roof_ms, "frac": t_roof_ms / ms_max, "bytes": work["bytes"],
                 "flops": work["leaf_flops"] + work["route_flops"], "leaf_candidates": work["leaf_candidates"],
-                "rule": "max(bytes / HBM, flops / bf16 tensor peak), measured peaks"},
+                "rule": "max(bytes / HBM, flops / bf16 tensor burst peak), measured peaks"},
+            "stage_rooflines": {k_: v for k_, v in rl.items() if k_ != "selector"},
             "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clk}
     line.update(extras)
     if rank == 0 and not args.no_cpu:
@@ -450,11 +483,11 @@ def attention_measurements(dev, st, tm):
             with torch.cuda.stream(st):
                 torch.nn.functional.scaled_dot_product_attention(q, kk, vv, is_causal=True)
         t_dense = tm(dense, 2)
-        t_roof = max(bytes_ / (pk["hbm"] * 1e9), flops / ((pk["bf16_sus"] or pk["bf16"]) * 1e12)) * 1e3
+        t_roof = max(bytes_ / (pk["hbm"] * 1e9), flops / (pk["bf16"] * 1e12)) * 1e3
         res[str(N)] = {"attend_ms": t_at, "select_plus_attend_ms": t_both, "dense_sdpa_ms": t_dense,
                        "dense_over_sparse": t_dense / t_both, "attended_keys_per_query": n_keys / (s.B * s.Hkv * s.N),
                        "roofline": {"t_roof_ms": t_roof, "frac": t_roof / t_at, "flops": flops, "bytes": bytes_,
-                                    "bound": "tensor" if flops / (pk["bf16_sus"] or pk["bf16"]) / 1e12 >
+                                    "bound": "tensor" if flops / pk["bf16"] / 1e12 >
                                     bytes_ / pk["hbm"] / 1e9 else "hbm",
                                     "partial_bytes": 2 * s.B * s.Hq * s.N * (s.K + 3) * (s.d * 2 + 4)}}
         del q, k, v, kk, vv, sel, at, idx
@@ -585,80 +618,131 @@ def side_measurements(args, dev, st, rank):
 
 
 # ----------------------------------------------------------- CPU oracle
-def cpu_baseline(s, q_h, k_h, budget_s=15.0):
-    """The fp64 oracle as it stands, on the host cores: the full fp64
-    pyramid plus the selection of every query of a growing set of evenly
-    spaced leaf blocks (all key heads), refined until about `budget_s`
-    seconds of selection work, extrapolated to all N query positions."""
-    import numpy as np
-    import oracle
+ORACLE_CHUNK = 64  # queries per OpenMP work item in the oracle's selection loop
 
-    o = oracle.Oracle.from_shape(s)
-    kn = k_h.double().numpy()
-    t0 = time.perf_counter()
-    pyr = o.pyramid(kn)
-    t_pyr = time.perf_counter() - t0
+
+def oracle_sample(s, q_h, nblocks, offset=0):
+    """Every (query position, key head) pair of `nblocks` evenly spaced leaf
+    blocks (counted from the last block), as one selection batch: the sel
+    triples and the matching [n, G, d] fp64 head rows."""
+    import numpy as np
+    import torch
     nb = -(-s.N // s.C)
-    done = set()
-    t_sel, n_sel = 0.0, 0
-    stride = max(1, nb // 16)
-    while True:
-        blocks = [blk for blk in range(nb - 1, -1, -stride) if blk not in done]
-        for blk in blocks:
-            sel = [(0, h, t) for h in range(s.Hkv) for t in range(blk * s.C, min((blk + 1) * s.C, s.N))]
-            qn = np.stack([q_h[b, h * s.G:(h + 1) * s.G, t].double().numpy() for (b, h, t) in sel])
+    stride = max(1, nb // max(1, nblocks))
+    blocks = [blk for blk in range(nb - 1 - offset, -1, -stride)][:nblocks]
+    ts = np.concatenate([np.arange(blk * s.C, min((blk + 1) * s.C, s.N)) for blk in blocks])
+    hs = np.repeat(np.arange(s.Hkv), len(ts))
+    tt = np.tile(ts, s.Hkv)
+    sel = np.stack([np.zeros_like(hs), hs, tt], axis=1)
+    qv = q_h[0].reshape(s.Hkv, s.G, s.N, s.d)
+    rows = qv[torch.from_numpy(hs), :, torch.from_numpy(tt)].double().numpy()
+    return sel, rows, len(blocks)
+
+
+def oracle_rate(s, q_h, k_h, budget_s, threads=None, kn=None, pyr=None, t_pyr=None):
+    """The fp64 oracle as it stands on `threads` host threads (all when None):
+    the fp64 pyramid of all keys, then selection batches of whole leaf blocks
+    (all key heads) until about `budget_s` seconds of selection work.  Every
+    batch holds at least ORACLE_CHUNK pairs per thread, so every thread
+    works.  Returns the throughput that implies for the whole workload
+    (pyramid once, plus the measured cost per (query, key head) pair for all
+    B N Hkv pairs) and what was timed."""
+    import oracle
+    o = oracle.Oracle.from_shape(s)
+    prev = oracle.num_threads()
+    if threads:
+        oracle.set_num_threads(threads)
+    try:
+        nthr = oracle.num_threads()
+        if kn is None:
+            kn = k_h.double().numpy()
+        if pyr is None:
             t0 = time.perf_counter()
-            o.select(qn, kn, pyr, sel=sel, qrows=True)
+            pyr = o.pyramid(kn)  # the oracle builds its pyramid on one thread
+            t_pyr = time.perf_counter() - t0
+        pyr_ = pyr
+        # blocks per batch: >= ORACLE_CHUNK pairs per thread (a block gives C * Hkv pairs)
+        per_batch = max(1, -(-ORACLE_CHUNK * nthr // (s.C * s.Hkv)))
+        t_sel, n_sel, n_blocks, calls = 0.0, 0, 0, 0
+        while t_sel < budget_s and n_blocks < -(-s.N // s.C):
+            sel, rows, nbk = oracle_sample(s, q_h, per_batch, offset=calls)
+            t0 = time.perf_counter()
+            o.select(rows, kn, pyr_, sel=sel, qrows=True)
             t_sel += time.perf_counter() - t0
             n_sel += len(sel)
-            done.add(blk)
-        if t_sel >= budget_s or stride == 1:
-            break
-        stride = max(1, stride // 2)
-    per_query = t_sel / n_sel  # per (query position, key head)
-    total = t_pyr + per_query * s.N * s.Hkv * s.B
-    return {"value": s.B * s.N / total, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"fp64 pyramid of all {s.N} keys ({t_pyr:.1f} s) + all {n_sel} (query, key head) "
-                      f"selections of {len(done)} evenly spaced leaf blocks ({t_sel:.1f} s), extrapolated "
-                      f"to all {s.N * s.Hkv * s.B} (query, key head) pairs",
-            "seconds_measured": t_pyr + t_sel}
+            n_blocks += nbk
+            calls += 1
+        per_pair = t_sel / n_sel
+        total = t_pyr + per_pair * s.B * s.N * s.Hkv
+        busy = min(nthr, -(-n_sel // calls // ORACLE_CHUNK))
+        return dict(value=s.B * s.N / total, t_pyr=t_pyr, t_sel=t_sel, n_sel=n_sel, n_blocks=n_blocks,
+                    calls=calls, threads=nthr, busy_threads=busy, per_pair_us=per_pair * 1e6,
+                    kn=kn, pyr=pyr_)
+    finally:
+        oracle.set_num_threads(prev)
+
+
+def cpu_baseline(s, q_h, k_h, budget_s=15.0, one_core_budget_s=6.0):
+    """The fp64 oracle as it stands, on all host cores and on one core (see
+    oracle_rate); `value` is the all-core figure."""
+    import platform
+    r = oracle_rate(s, q_h, k_h, budget_s)
+    r1 = oracle_rate(s, q_h, k_h, one_core_budget_s, threads=1, kn=r["kn"], pyr=r["pyr"], t_pyr=r["t_pyr"])
+    return {"value": r["value"], "unit": UNIT, "cores": r["busy_threads"], "kind": "oracle",
+            "sample": f"fp64 pyramid of all {s.N} keys ({r['t_pyr']:.1f} s) + the selections of every "
+                      f"(query, key head) pair of {r['n_blocks']} evenly spaced leaf blocks ({r['n_sel']} pairs, "
+                      f"{r['t_sel']:.1f} s, {r['calls']} batches of >= {ORACLE_CHUNK} pairs per thread); "
+                      f"value = B N / (pyramid s + s per pair x B N Hkv)",
+            "per_pair_us": r["per_pair_us"], "threads": r["threads"],
+            "one_core": {"value": r1["value"], "unit": UNIT, "cores": 1, "per_pair_us": r1["per_pair_us"],
+                         "sample": f"{r1['n_sel']} pairs of {r1['n_blocks']} leaf blocks ({r1['t_sel']:.1f} s) "
+                                   f"on one thread, plus the same single-threaded pyramid"},
+            "host": f"{platform.machine()}, {os.cpu_count()} cpus",
+            "seconds_measured": r["t_pyr"] + r["t_sel"] + r1["t_pyr"] + r1["t_sel"]}
 
 
 def run_reference(args, ws, rank):
-    """--impl reference: the CPU oracle on this config, rank 0 only."""
+    """--impl reference: the fp64 CPU oracle on this config (rank 0 only).
+    One step is real and timed as a whole: the fp64 pyramid of all keys plus
+    the selections of a fixed sample of whole leaf blocks (all key heads),
+    in one batch that keeps every thread busy.  ms_per_step is that measured
+    step; value is the whole-workload throughput the step's own timings
+    imply (pyramid once, plus its cost per pair for all B N Hkv pairs)."""
     if rank != 0:
         return None
     s, q_h, k_h = workload(args.N, 0)
-    import numpy as np
     import oracle
     o = oracle.Oracle.from_shape(s)
     kn = k_h.double().numpy()
-    nb = -(-s.N // s.C)
-    blocks = list(range(nb - 1, -1, -max(1, nb // 16)))
-    sel = [(0, h, t) for blk in blocks for h in range(s.Hkv) for t in range(blk * s.C, min((blk + 1) * s.C, s.N), 4)]
-    qn = np.stack([q_h[0, h * s.G:(h + 1) * s.G, t].double().numpy() for (_, h, t) in sel])
+    nthr = oracle.num_threads()
+    nblocks = max(1, -(-16 * ORACLE_CHUNK * nthr // (s.C * s.Hkv)))
+    sel, rows, nbk = oracle_sample(s, q_h, nblocks)
 
     def step():
         t0 = time.perf_counter()
         pyr = o.pyramid(kn)
         t1 = time.perf_counter()
-        o.select(qn, kn, pyr, sel=sel, qrows=True)
+        o.select(rows, kn, pyr, sel=sel, qrows=True)
         t2 = time.perf_counter()
-        return (t1 - t0) + (t2 - t1) / len(sel) * s.N * s.Hkv * s.B
+        return t2 - t0, (t1 - t0) + (t2 - t1) / len(sel) * s.B * s.N * s.Hkv
 
     for _ in range(args.warmup):
         step()
-    times = [step() for _ in range(args.steps)]
-    sec = statistics.mean(times)
-    val = s.B * s.N / sec
+    meas = [step() for _ in range(args.steps)]
+    step_s = statistics.mean(m[0] for m in meas)
+    work_s = statistics.mean(m[1] for m in meas)
+    val = s.B * s.N / work_s
+    cfg = run_config(s, ws)
     return {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded iid N(0,1) q and k)",
-            "config": {"workload": f"prefill selection, B={s.B} N={s.N} Hq={s.Hq} Hkv={s.Hkv} d={s.d} C={s.C} "
-                                   f"g=2 K={s.K} (fp64 CPU oracle)", "N": s.N, "K": s.K},
-            "cpu_baseline": {"kind": "oracle", "cores": oracle.num_threads(), "value": val, "unit": UNIT,
-                             "sample": f"per step: full fp64 pyramid + {len(sel)} sampled (query, key head) "
-                                       f"selections extrapolated to all {s.N * s.Hkv}"},
+            "config": cfg,
+            "cpu_baseline": {"kind": "oracle", "cores": min(nthr, -(-len(sel) // ORACLE_CHUNK)), "value": val,
+                             "unit": UNIT,
+                             "sample": f"per step (timed whole, {step_s:.2f} s): fp64 pyramid of all {s.N} keys + "
+                                       f"the selections of all {len(sel)} (query, key head) pairs of {nbk} evenly "
+                                       f"spaced leaf blocks in one batch; value = B N / (pyramid s + s per pair x "
+                                       f"{s.B * s.N * s.Hkv} pairs)"},
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -760,6 +844,15 @@ def configs_table():
         qd, kd = q.cuda(), k.cuda()
         reps = 20 if s.N <= 65536 else 5
         t_pisa = _cuda_ms(lambda: sel.prefill(qd, kd, stream=st), reps, st)
+        kept2 = sel.ws[256:256 + s.B * s.Hkv * s.N * s.K * 4].view(torch.int32).cpu().numpy()
+        work = algorithmic_work(s, kept2)
+        pk = peaks()
+        t_roof = max(work["bytes"] / (pk["hbm"] * 1e9), (work["leaf_flops"] + work["route_flops"]) /
+                     (pk["bf16"] * 1e12)) * 1e3
+        roof = {"t_roof_ms": t_roof, "frac": t_roof / t_pisa, "bytes": work["bytes"],
+                "flops": work["leaf_flops"] + work["route_flops"],
+                "bound": "tensor" if t_roof > work["bytes"] / (pk["hbm"] * 1e9) * 1e3 else "hbm",
+                "rule": "max(bytes / HBM copy, flops / bf16 burst), measured peaks; time = build + select"}
         t_flat = None
         if s.dtype == "bf16":
             fs = pisa.Selector(p, mode="flat")
@@ -774,12 +867,16 @@ def configs_table():
             o.select(q.double().numpy(), k.double().numpy(), pyr)
             cpu_ms, cpu_how = (_t.perf_counter() - t0) * 1e3, "full"
         else:
-            cb = cpu_baseline(s, q, k, budget_s=5.0)
-            cpu_ms, cpu_how = s.B * s.N / cb["value"] * 1e3, "sampled: " + cb["sample"]
+            cb = oracle_rate(s, q, k, 5.0)
+            cpu_ms = s.B * s.N / cb["value"] * 1e3
+            cpu_how = (f"sampled: fp64 pyramid ({cb['t_pyr']:.1f} s) + {cb['n_sel']} (query, key head) pairs of "
+                       f"{cb['n_blocks']} leaf blocks ({cb['t_sel']:.1f} s), {cb['busy_threads']} threads busy; "
+                       f"ms = pyramid + per-pair cost x all pairs")
         rows.append({"config": name, "N": s.N, "K": s.K, "dtype": s.dtype, "pisa_ms": t_pisa,
-                     "pisa_queries_per_s": s.B * s.N / t_pisa * 1e3, "flat_ms": t_flat,
+                     "pisa_queries_per_s": s.B * s.N / t_pisa * 1e3, "roofline": roof, "flat_ms": t_flat,
                      "pisa_over_flat": (t_flat / t_pisa) if t_flat else None,
-                     "cpu_oracle_ms": cpu_ms, "cpu_cores": oracle.num_threads(), "cpu_how": cpu_how})
+                     "cpu_oracle_ms": cpu_ms, "cpu_cores": (oracle.num_threads() if cpu_full else cb["busy_threads"]),
+                     "cpu_how": cpu_how})
         print(json.dumps(rows[-1]), flush=True)
 
     q, k = W.iid(W.TINY, 0)
@@ -829,9 +926,10 @@ def configs_table():
     t2 = _t.perf_counter()
     rows.append({"config": "decode B=64 x 131072 cached, 32/8 d=128 bf16 K=32", "pisa_us_per_step": us,
                  "cpu_oracle_ms_per_step": (t2 - t1) * 64 * 1e3,
-                 "cpu_how": f"oracle select of one sequence (8 key heads) x 64; its fp64 pyramid rebuild "
-                            f"({(t1 - t0) * 1e3:.0f} ms per sequence) not included",
-                 "cpu_cores": oracle.num_threads()})
+                 "cpu_how": f"oracle select of one sequence (8 key heads: one OpenMP work item, so one "
+                            f"thread) x 64; its fp64 pyramid rebuild ({(t1 - t0) * 1e3:.0f} ms per sequence) "
+                            f"not included",
+                 "cpu_cores": 1})
     print(json.dumps(rows[-1]), flush=True)
 
 

@@ -44,7 +44,8 @@
  *    on failure, returns a negative status and launches nothing.  Launch
  *    failures return PISA_ERR_CUDA.  Calls are asynchronous on `stream`
  *    (a cudaStream_t; NULL is the legacy default stream), never allocate
- *    memory and never synchronise, except pisa_read_device_status.
+ *    memory and never synchronise, except pisa_read_device_status and
+ *    pisa_read_static_status.
  *  - The workspace is caller-owned scratch of at least
  *    pisa_workspace_bytes(params, mode) bytes.  Its first 256 bytes hold a
  *    device status word that kernels set on faults they detect (a decode
@@ -264,17 +265,31 @@ pisa_status pisa_select_flat(const pisa_params* p, const void* q,
  *    on every GPU that loads it until the process exits.  Problems needing
  *    more (pisa_workspace_bytes(p, PISA_MODE_PREFILL) > 64 MiB) get
  *    PISA_ERR_WORKSPACE and nothing is launched.
- *  - The first call on a device looks up the array's device address (with
- *    that device current) and caches it; make that first call before any
- *    stream capture on the device.
- *  - Calls never allocate.  All calls on a device share the array, and each
- *    call clears what must start at zero; calls that overlap on the GPU
+ *  - The array's 64 MiB are reserved when the CUDA module holding it is
+ *    loaded on a device.  Under CUDA's default lazy module loading that
+ *    happens inside the first call of this function (or of
+ *    pisa_read_static_status) on that device, which also looks up and caches
+ *    the array's device address with the device current; under eager loading
+ *    it happens when the library is loaded.  Make that first call where
+ *    allocation is still allowed (at initialisation, for instance) and before
+ *    any stream capture on the device.
+ *  - Later calls never allocate.  All calls on a device share the array, and
+ *    each call clears what must start at zero; calls that overlap on the GPU
  *    (other streams, other threads) race on it and must be serialised by the
- *    caller. */
+ *    caller.
+ *  - The array starts with the same device status word as any workspace;
+ *    pisa_read_static_status reads it. */
 pisa_status pisa_select_prefill_static(const pisa_params* p, const void* q,
                                        const void* k, const float* pyramid,
                                        int32_t* out_idx, float* out_score,
                                        void* stream);
+
+/* Device status word of the current device's fixed array used by
+ * pisa_select_prefill_static (faults its kernels detected, such as an
+ * exhausted bounded wait): synchronises `stream`, then copies the word into
+ * *device_code (PISA_DEV_*).  Returns PISA_ERR_DEVICE when it is non-zero.
+ * The paper has no counterpart. */
+pisa_status pisa_read_static_status(int32_t* device_code, void* stream);
 
 /* Block-sparse attention over a selection (agihunt.info summary, opening
  * paragraph: each query reads only its selected tiles of C keys, so the

@@ -58,3 +58,12 @@ extern "C" pisa_status pisa_select_prefill_static(const pisa_params* p, const vo
   // everything else in the workspace is fully rewritten by every call.
   return pisa_select_prefill(p, q, k, pyramid, ws, kStaticScratchBytes, out_idx, out_score, nullptr, stream);
 }
+
+extern "C" pisa_status pisa_read_static_status(int32_t* device_code, void* stream) {
+  if (!device_code) return PISA_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  const pisa_status rc = scratch_address(&ws);
+  if (rc != PISA_OK) return rc;
+  // the status word is the first 256 bytes of the array, as in any workspace
+  return pisa_read_device_status(ws, device_code, stream);
+}

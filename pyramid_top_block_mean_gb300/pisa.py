@@ -36,7 +36,8 @@ EXPORTED = ["pisa_abi_version", "pisa_status_string", "pisa_pyramid_levels", "pi
             "pisa_pyramid_bytes", "pisa_workspace_bytes", "pisa_build_pyramid", "pisa_select_prefill",
             "pisa_prefill_route", "pisa_prefill_leaves", "pisa_select_decode", "pisa_select_flat",
             "pisa_read_device_status", "pisa_select_prefill_static", "pisa_kernel_launches",
-            "pisa_attend_prefill", "pisa_build_pyramid_paged", "pisa_select_decode_paged", "pisa_attend_decode"]
+            "pisa_attend_prefill", "pisa_build_pyramid_paged", "pisa_select_decode_paged", "pisa_attend_decode",
+            "pisa_read_static_status"]
 
 
 class Params(ctypes.Structure):
@@ -84,6 +85,10 @@ _lib.pisa_attend_prefill.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_
 _lib.pisa_attend_prefill.restype = ctypes.c_int
 _lib.pisa_read_device_status.argtypes = [_vp, ctypes.POINTER(ctypes.c_int32), _vp]
 _lib.pisa_read_device_status.restype = ctypes.c_int
+_lib.pisa_select_prefill_static.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp]
+_lib.pisa_select_prefill_static.restype = ctypes.c_int
+_lib.pisa_read_static_status.argtypes = [ctypes.POINTER(ctypes.c_int32), _vp]
+_lib.pisa_read_static_status.restype = ctypes.c_int
 
 
 class PisaError(RuntimeError):

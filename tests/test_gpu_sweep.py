@@ -1,0 +1,96 @@
+"""GPU parity on every point of the long-prefill sweep (B = 1, N in {4K, 16K,
+64K, 128K, 256K}, 16 query / 4 key heads, d = 128, bf16, C = 64, g = 2,
+K = 8, iid N(0, 1) q and k from seed 3): the benchmark's own inputs, run in
+the launch configuration the benchmark times (pyramid build, then the route
+and leaf stages on one workspace), against the fp64 oracle.
+
+Coverage per point (agihunt.info summary, latency paragraph: the selection
+sweep from 4K to 256K tokens at C = 64, K = 8):
+  * 4K and 16K: every (query, key head) pair;
+  * 64K: every pair -- one whole 65,536-query bucketing chunk per key head;
+  * 128K: the whole second chunk plus the last 2,048 positions of the first,
+    for every key head, so both chunk boundaries are crossed;
+  * 256K: the 128 positions on each side of every chunk boundary, the last
+    two leaf blocks and 25,000 random positions, for every key head
+    (over 100,000 pairs).
+The rule is the selector's tolerance (tests/parity.py): identical index sets
+except where the oracle's K-th and (K+1)-th scores differ by < 1e-3 on some
+level, scores within 2e-3, tie-exempt queries re-checked level by level from
+the GPU trace.  The oracle gets large batches so that every host core works.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from pyramid_top_block_mean_gb300 import workloads as W
+
+from parity import Report, compare
+
+pytestmark = pytest.mark.gpu
+
+CHUNK = 1 << 16  # queries per bucketing chunk of the leaf stage
+
+
+@pytest.fixture(scope="module")
+def pisa():
+    from pyramid_top_block_mean_gb300 import pisa as m
+    return m
+
+
+def positions(N):
+    """Query positions checked for every key head at sweep point N."""
+    if N <= CHUNK:
+        return np.arange(N)
+    if N == 2 * CHUNK:
+        return np.arange(CHUNK - 2048, N)
+    gen = np.random.default_rng(17)
+    ts = set(gen.integers(0, N, 25000).tolist()) | set(range(N - 128, N))
+    for c in range(1, N // CHUNK):
+        ts |= set(range(c * CHUNK - 128, c * CHUNK + 128))
+    return np.array(sorted(ts))
+
+
+@pytest.mark.parametrize("N", W.SWEEP_NS)
+def test_sweep_point_matches_oracle(pisa, N):
+    s = W.sweep(N)
+    q, k = W.iid(s, 3)
+    p = pisa.params_from_shape(s)
+    sel = pisa.Selector(p)
+    L = pisa.pyramid_levels(p)
+    qd, kd = q.cuda(), k.cuda()
+    tr = torch.full((s.B, s.Hkv, s.N, L, s.K), -7, dtype=torch.int32, device="cuda")
+    pisa.build_pyramid(p, kd, sel.pyramid)
+    pisa.prefill_route(p, qd, sel.pyramid, sel.ws, tr)
+    pisa.prefill_leaves(p, qd, kd, sel.ws, sel.out_idx, sel.out_score)
+    torch.cuda.synchronize()
+    assert sel.device_status() == 0
+
+    ts = positions(N)
+    hs = np.repeat(np.arange(s.Hkv), len(ts))
+    tt = np.tile(ts, s.Hkv)
+    rows = torch.from_numpy(hs * s.N + tt).cuda()
+    W_ = s.K + 3
+    idx = sel.out_idx.reshape(-1, W_)[rows].cpu().numpy()
+    score = sel.out_score.reshape(-1, W_)[rows].cpu().double().numpy()
+    trace = tr.reshape(s.B * s.Hkv * s.N, L, s.K)[rows].cpu().numpy()
+    del tr, sel, qd, kd
+    torch.cuda.empty_cache()
+
+    o = oracle.Oracle.from_shape(s)
+    kn = k.double().numpy()
+    pyr = o.pyramid(kn)
+    qv = q[0].reshape(s.Hkv, s.G, s.N, s.d)
+    rep = Report()
+    step = 1 << 16
+    for a in range(0, len(hs), step):
+        b_ = min(len(hs), a + step)
+        keys = [(0, int(h), int(t)) for h, t in zip(hs[a:b_], tt[a:b_])]
+        qsel = qv[torch.from_numpy(hs[a:b_]), :, torch.from_numpy(tt[a:b_])].double().numpy()
+        ref = o.select(qsel, kn, pyr, sel=keys, qrows=True)
+        compare(o, qsel, kn, pyr, ref, idx[a:b_], score[a:b_], trace[a:b_], keys, rep, qmode="rows")
+    print(f"N={N}: {rep}")
+    assert rep.n == len(hs)
+    if N >= 4 * CHUNK:
+        assert rep.n >= 100000
+    assert rep.ok(), str(rep)
