@@ -27,7 +27,7 @@ _i64p = ctypes.POINTER(ctypes.c_int64)
 class _Params(ctypes.Structure):
     _fields_ = [("B", _i64), ("N", _i64), ("Hq", _i32), ("Hkv", _i32),
                 ("d", _i32), ("C", _i32), ("K", _i32), ("scale", ctypes.c_double),
-                ("scorer", _i32)]
+                ("scorer", _i32), ("prefix", _i32)]
 
 
 def build(force: bool = False) -> str:
@@ -91,17 +91,21 @@ def _ptr(a: np.ndarray, t):
 
 
 class Oracle:
-    """Oracle bound to one problem shape (B, N, Hq, Hkv, d, C, K, scale) and
-    block scorer (0: log-sum-exp, 1: PISA-1, 2: PISA-2)."""
+    """Oracle bound to one problem shape (B, N, Hq, Hkv, d, C, K, scale), block
+    scorer (0: log-sum-exp, 1: PISA-1, 2: PISA-2) and summary reading
+    (prefix=False: node summaries over all keys of the span; prefix=True: a
+    prefill query at position t reads summaries of the keys at positions
+    <= t only, the prefix-consistent reading)."""
 
-    def __init__(self, B, N, Hq, Hkv, d, C, K, scale: float = 0.0, scorer: int = 0):
-        self.p = _Params(B, N, Hq, Hkv, d, C, K, scale, scorer)
+    def __init__(self, B, N, Hq, Hkv, d, C, K, scale: float = 0.0, scorer: int = 0, prefix: bool = False):
+        self.p = _Params(B, N, Hq, Hkv, d, C, K, scale, scorer, int(bool(prefix)))
         self.B, self.N, self.Hq, self.Hkv, self.d, self.C, self.K = B, N, Hq, Hkv, d, C, K
         self.scorer = scorer
+        self.prefix = bool(prefix)
 
     @classmethod
-    def from_shape(cls, s, scale: float = 0.0, scorer: int = 0):
-        return cls(s.B, s.N, s.Hq, s.Hkv, s.d, s.C, s.K, scale, scorer)
+    def from_shape(cls, s, scale: float = 0.0, scorer: int = 0, prefix: bool = False):
+        return cls(s.B, s.N, s.Hq, s.Hkv, s.d, s.C, s.K, scale, scorer, prefix)
 
     @property
     def num_levels(self) -> int:

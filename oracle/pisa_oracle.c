@@ -27,7 +27,12 @@
  *  - the walk starts at the root and keeps everything while a level has at
  *    most K candidates [RCAP pisa_select sketch, "start at coarsest level"];
  *  - a node is eligible when its leaf range meets E = [1, qb-2]; summaries
- *    themselves are not masked (prefill summaries include later keys);
+ *    themselves are not masked (prefill summaries include later keys), unless
+ *    the prefix-consistent reading is asked for (po_params.prefix): then every
+ *    summary a query at position t reads is the mean of its span's keys at
+ *    positions <= t, the pyramid of the sequence's first t + 1 keys, which is
+ *    what a decode step at length t + 1 sees [AGI pyramid paragraph, decode
+ *    routing; RCAP pisa_select sketch];
  *  - "LSE" is the literal log-sum-exp, summed over the query heads of a GQA
  *    group; the scale is 1/sqrt(d) unless another is given; the PISA-1 and
  *    PISA-2 scorers replace it by its first- and second-order cumulant
@@ -58,6 +63,9 @@ typedef struct {
   int32_t K;      /* Top-K per level */
   double scale;   /* score scale inside exp(); <= 0 means 1/sqrt(d) */
   int32_t scorer; /* 0: log-sum-exp; 1: PISA-1; 2: PISA-2 (po_reduce) */
+  int32_t prefix; /* 0: node summaries over all keys of the span (default);
+                     1: over the span's keys at positions <= t (prefix-
+                     consistent prefill, po_summary) */
 } po_params;
 
 /* ---------------------------------------------------------------- tree shape
@@ -209,6 +217,32 @@ static const double* po_node(const po_query* Q, int level, int64_t j) {
   return Q->pyr + (((Q->b * Q->p->Hkv + Q->h) * Q->P) + off + j) * Q->p->d;
 }
 
+/* Summary of node (level, j) as query Q reads it.  Default: its pyramid row
+ * (the mean of the keys of its span present in the sequence).  With
+ * p->prefix, a span that reaches past position t is summarised by the mean of
+ * its keys at positions <= t, computed here from the raw keys into buf (d
+ * doubles); a span with no such key reads as zeros. */
+static const double* po_summary(const po_query* Q, int level, int64_t j, double* buf) {
+  if (Q->p->prefix) {
+    const int64_t span = (int64_t)Q->p->C << (level - 1);
+    const int64_t lo = j * span;
+    int64_t hi = lo + span;
+    if (hi > Q->len) hi = Q->len;
+    if (hi > Q->t + 1) {
+      const int d = Q->p->d;
+      const double* kh = Q->k + ((Q->b * Q->p->Hkv + Q->h) * Q->p->N) * d;
+      const int64_t end = Q->t + 1;
+      for (int c = 0; c < d; ++c) buf[c] = 0.0;
+      if (end <= lo) return buf;
+      for (int64_t i = lo; i < end; ++i)
+        for (int c = 0; c < d; ++c) buf[c] += kh[i * d + c];
+      for (int c = 0; c < d; ++c) buf[c] /= (double)(end - lo);
+      return buf;
+    }
+  }
+  return po_node(Q, level, j);
+}
+
 /* Score of candidate j at `level`, summed over the G query heads of the group
  * [AGI kernel paragraph: heads of one GQA group share the selection].
  *  level >= 2: log-sum-exp over the eligible children's summaries
@@ -222,11 +256,13 @@ static double po_score(const po_query* Q, int level, int64_t j,
   double total = 0.0;
   if (level >= 2) {
     const double* kids[2];
+    double* bufs = (double*)malloc(sizeof(double) * 2 * (size_t)d);
     int nk = 0;
     for (int64_t c = 2 * j; c <= 2 * j + 1; ++c) {
       if (c >= Q->sizes[level - 2]) continue;
       if (!po_eligible(Q, level - 1, c)) continue;
-      kids[nk++] = po_node(Q, level - 1, c);
+      kids[nk] = po_summary(Q, level - 1, c, bufs + (size_t)nk * d);
+      ++nk;
     }
     if (counters) counters[1] += nk;
     for (int g = 0; g < Q->G; ++g) {
@@ -234,6 +270,7 @@ static double po_score(const po_query* Q, int level, int64_t j,
       for (int i = 0; i < nk; ++i) x[i] = Q->s * po_dot(Q->qrow[g], kids[i], d);
       total += po_reduce(x, nk, Q->p->scorer);
     }
+    free(bufs);
     return total;
   }
   /* leaf: keys [j*C, min((j+1)*C, len)) of key head h */

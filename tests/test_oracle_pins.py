@@ -54,8 +54,9 @@ class RecursiveRef:
     """An independent, recursive restatement of the walk (numpy means taken
     directly from the raw keys, scipy logsumexp).  Tiny inputs only."""
 
-    def __init__(self, q, k, C, K, scale=None):
+    def __init__(self, q, k, C, K, scale=None, prefix=False):
         self.q, self.k, self.C, self.K = q, k, C, K
+        self.prefix = prefix  # summaries of the keys at positions <= t only
         self.d = q.shape[-1]
         self.s = scale if scale else 1.0 / math.sqrt(self.d)
         self.G = q.shape[1] // k.shape[1]
@@ -81,6 +82,8 @@ class RecursiveRef:
 
         def mean(level, j):
             lo, hi = span_keys(level, j, C, N)
+            if self.prefix:
+                hi = min(hi, t + 1)
             return keys[lo:hi].mean(axis=0)
 
         def score(level, j):
