@@ -225,7 +225,7 @@ def algorithmic_work(s, kept2):
                 leaf_bytes=q_bytes + k_bytes + kept_bytes + out_bytes)
 
 
-ROUTE_KERNEL = "route_mma_kernel"
+ROUTE_KERNEL = "route_haar_kernel"
 
 
 def load_traffic(name):

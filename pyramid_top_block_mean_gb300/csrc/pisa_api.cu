@@ -54,9 +54,8 @@ PrefillWs prefill_ws_layout(const Prob& pr, const Pyr& s) {
   w.tile_off = o; o = align_up(o + (size_t)(w.nbuckets + 1) * 4, 256);
   w.pairs = o; o = align_up(o + (size_t)nq * pr.K * 4, 256);
   w.tile_info = o; o = align_up(o + (size_t)w.max_tiles * 16, 256);
-  const size_t pyr_elems = (size_t)pr.B * pr.Hkv * s.P * pr.d;
-  w.pyr_hi = o; o = align_up(o + pyr_elems * 2, 256);
-  w.pyr_lo = o; o = align_up(o + pyr_elems * 2, 256);
+  w.haar_rows = o; o = align_up(o + 4 * haar_rows_bytes(pr, s), 256);
+  w.haar_meta = o; o = align_up(o + haar_meta_bytes(pr, s), 256);
   w.total = o;
   return w;
 }
@@ -254,9 +253,9 @@ static pisa_status run_route(const Prob& pr, const Pyr& s, const PrefillWs& w, c
                              char* base, int32_t* trace, cudaStream_t st) {
   int32_t* status = (int32_t*)(base + w.status);
   if (cudaMemsetAsync(status, 0, 256, st) != cudaSuccess) return PISA_ERR_CUDA;
-  if (route_mma_supported(pr))
-    return cuda_status(launch_route_mma(pr, s, q, pyramid, (uint16_t*)(base + w.pyr_hi), (uint16_t*)(base + w.pyr_lo),
-                                        (int32_t*)(base + w.kept2), trace, st));
+  if (route_haar_supported(pr))
+    return cuda_status(launch_route_haar(pr, s, q, pyramid, base + w.haar_rows, (float4*)(base + w.haar_meta),
+                                         (int32_t*)(base + w.kept2), trace, st));
   return cuda_status(launch_route(pr, s, q, pyramid, (int32_t*)(base + w.kept2), trace, status, st));
 }
 

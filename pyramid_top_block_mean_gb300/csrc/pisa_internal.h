@@ -25,8 +25,8 @@ struct PrefillWs {
   size_t tile_off;    // int32 [nbuckets + 1] exclusive scan of tiles per bucket
   size_t pairs;       // int32 [B * Hkv * N * K] (t << 5 | slot) grouped by bucket
   size_t tile_info;   // int4  [max_tiles] {bucket, first pair, pairs, 0}
-  size_t pyr_hi;      // bf16 [B, Hkv, P, d] pyramid rounded (tensor-core routing)
-  size_t pyr_lo;      // bf16 [B, Hkv, P, d] rounding residual
+  size_t haar_rows;   // fp16 4 x [B, Hkv, P2, d]: summary and child-difference rows, hi and lo (P2 = P - n_1)
+  size_t haar_meta;   // fp32 [B, Hkv, P2, 4]: row scales and residual norms
   size_t total;
   int64_t nbuckets;   // B * Hkv * nchunk * n_2
   int64_t nchunk;     // ceil(N / 2^kChunkShift)
@@ -85,9 +85,11 @@ cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, co
                                  const int32_t* seq_lens, float* pyr, int32_t* status, cudaStream_t st);
 cudaError_t launch_route(const Prob& pr, const Pyr& s, const void* q, const float* pyr, int32_t* kept2,
                          int32_t* trace, int32_t* status, cudaStream_t st);
-bool route_mma_supported(const Prob& pr);
-cudaError_t launch_route_mma(const Prob& pr, const Pyr& s, const void* q, const float* pyr, uint16_t* phi,
-                             uint16_t* plo, int32_t* kept2, int32_t* trace, cudaStream_t st);
+bool route_haar_supported(const Prob& pr);
+size_t haar_rows_bytes(const Prob& pr, const Pyr& s);  // one of the four fp16 row arrays
+size_t haar_meta_bytes(const Prob& pr, const Pyr& s);
+cudaError_t launch_route_haar(const Prob& pr, const Pyr& s, const void* q, const float* pyr, char* rows,
+                              float4* meta, int32_t* kept2, int32_t* trace, cudaStream_t st);
 cudaError_t launch_leaf_simt(const Prob& pr, const Pyr& s, const void* q, const void* k, const int32_t* kept2,
                              int32_t* out_idx, float* out_score, cudaStream_t st);
 cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, char* ws, const void* q,

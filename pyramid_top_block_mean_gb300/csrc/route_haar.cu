@@ -1,0 +1,618 @@
+// route_haar.cu -- top-down pyramid routing over a difference ("Haar")
+// form of the pyramid, with the dot products on the tensor cores (bf16
+// queries, GQA groups of 4 query heads).  Same walk and scores as route.cu
+// (rcap.io post on "Block Sparse Attention with Log-Linear Complexity":
+// "Selection walks the tree top-down", "The scoring rule matters";
+// agihunt.info summary, kernel paragraph: one selection per GQA group, the
+// heads' scores summed).
+//
+// Summary rows.  For every node (l, j) of level l >= 2 the preparation
+// kernel stores two rows, each as fp16 with a power-of-two scale of its own
+// (so that the row's largest element lands in [2^14, 2^15)):
+//   MU  = mu(l, j) - mu(root)            (the summary relative to the root's)
+//   DD  = mu(l-1, 2j) - mu(l-1, 2j+1)    (the difference of its two children;
+//                                         zero when the node has one child)
+// plus the fp16 rounding residual of each (lo) and its 2-norm.  Because the
+// parent is the count-weighted mean of its children,
+//   q.mu(child 0) = q.mu(node) + n1/(n0+n1) q.DD,
+//   q.mu(child 1) = q.mu(node) - n0/(n0+n1) q.DD,
+// so one DD row per candidate gives both of its children's dots from the
+// candidate's own dot, and the rounding errors of the levels only add up
+// (no factor grows along the path).  Dots relative to the root differ from
+// the true ones by one constant per head, which shifts every candidate's
+// group score by the same amount and leaves each Top-K unchanged.
+//
+// Precision.  An fp16 row moves half the bytes of the bf16 hi + lo pair that
+// an fp32-faithful dot needs.  Its rounding error in a dot is at most
+// s |q_h| |residual| (Cauchy-Schwarz); when that bound, summed over the
+// group's heads, exceeds kLoTau (log2 units) the residual row is fetched too
+// and multiplied in the same accumulators (rows with unusually large
+// summaries, such as the ancestors of a block of planted keys).  Otherwise the
+// error stays a few 1e-5 in the group score, two orders of magnitude below
+// the 1e-3 margin within which two candidates count as tied.
+//
+// A warp walks two queries (16 lanes of bookkeeping each).  Per level and
+// query, every candidate needs one DD row (and, at the start level, its MU
+// row); eight rows at a time are multiplied against the query's four head
+// vectors as m16n8k16 MMAs with A = 8 nodes x the two halves of the d dims
+// and B = the 4 heads x the two halves, of which the two half-diagonal
+// blocks are used.  Rows are stored half-interleaved so the eight lanes of a
+// node read one whole 128-byte line per load.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "pisa_common.cuh"
+#include "pisa_internal.h"
+
+namespace pisa {
+
+namespace {
+
+// Residual fetch threshold: the bound on a row's fp16 rounding error in the
+// group score, in log2 units (2e-3 in natural-log units).
+constexpr float kLoTau = 2.0e-3f * kLog2e;
+
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }
+
+// Exponent e such that max * 2^e lies in [2^14, 2^15) (0 for zero or
+// non-finite max), clamped so that 2^e and 2^-e are normal floats.
+__device__ __forceinline__ int row_exponent(float mx) {
+  if (!(mx > 0.0f) || !(mx < INFINITY)) return 0;
+  const int E = (int)((__float_as_uint(mx) >> 23) & 0xffu) - 127;
+  return min(126, max(-126, 14 - E));
+}
+
+// Position of dim c within a stored row of D elements: 128-byte line bb holds
+// dims [32 bb, 32 bb + 32) of the first half, then the same dims of the second.
+__device__ __forceinline__ int row_pos(int c, int D) {
+  const int hd = D / 2;
+  return ((c % hd) / 32) * 64 + (c / hd) * 32 + (c & 31);
+}
+
+__device__ __forceinline__ uint32_t orderable_key_h(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Exclusive prefix sum of v in {0, 1, 2} over the 16 lanes of this lane's
+// half of the warp (two ballots); *tot receives the half's total.
+__device__ __forceinline__ int prefix16h(int v, int lane, int* tot) {
+  const unsigned b0 = __ballot_sync(0xffffffffu, v & 1);
+  const unsigned b1 = __ballot_sync(0xffffffffu, v & 2);
+  const unsigned hm = (lane & 16) ? 0xffff0000u : 0x0000ffffu;
+  const unsigned lt = hm & ((1u << lane) - 1u);
+  *tot = __popc(b0 & hm) + 2 * __popc(b1 & hm);
+  return __popc(b0 & lt) + 2 * __popc(b1 & lt);
+}
+
+__device__ __forceinline__ bool elig_node_h(int level, int j, int e_hi) {
+  return (j << (level - 1)) <= e_hi && (((j + 1) << (level - 1)) - 1) >= 1;
+}
+
+__device__ __forceinline__ int count_node_h(int C, int level, int j, int64_t N) {
+  const int64_t w = (int64_t)C << (level - 1);
+  const int64_t c = N - (int64_t)j * w;
+  return (int)(c < 0 ? 0 : (c > w ? w : c));
+}
+
+__device__ __forceinline__ float comp4(const float4& v, int g) {
+  return g == 0 ? v.x : (g == 1 ? v.y : (g == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+}  // namespace
+
+// One warp per stored row: row w of [BH, P2, 2] is (node r = w / 2 of the
+// levels >= 2, kind w % 2: MU or DD).  P2 = P - n_1 rows per (sequence, key
+// head); node (l, j) is row off_l - n_1 + j.  meta[r] = {2^-e of MU, norm of
+// the MU residual, 2^-e of DD, norm of the DD residual} (residual norms in
+// the pyramid's units).
+__global__ void haar_prep_kernel(int64_t BH, Pyr s, int D, const float* __restrict__ pyr, __half* __restrict__ mu_hi,
+                                 __half* __restrict__ mu_lo, __half* __restrict__ dd_hi, __half* __restrict__ dd_lo,
+                                 float2* __restrict__ meta) {
+  const int64_t n1 = s.size[0];
+  const int64_t P2 = s.P - n1;
+  const int64_t nrow = BH * P2 * 2;
+  const int lane = threadIdx.x & 31;
+  const int per = D / 32;  // elements per lane (2 or 4)
+  for (int64_t w = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / 32; w < nrow;
+       w += (int64_t)gridDim.x * blockDim.x / 32) {
+    const int kind = (int)(w & 1);
+    const int64_t r = w >> 1;
+    const int64_t bh = r / P2, r2 = r % P2;
+    int l = 2;
+    while (l < s.L && r2 >= s.off[l] - n1) ++l;  // s.off[l] is the first row of level l + 1
+    const int64_t j = r2 - (s.off[l - 1] - n1);
+    const float* pb = pyr + bh * s.P * D;
+    float v[4];
+    float mx = 0.0f;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      if (m >= per) break;
+      const int c = lane + 32 * m;
+      float x;
+      if (kind == 0) {
+        const float ref = pb[(s.P - 1) * D + c];
+        x = pb[(s.off[l - 1] + j) * D + c] - (isfinite(ref) ? ref : 0.0f);
+      } else {
+        const int64_t c0 = 2 * j, c1 = 2 * j + 1;
+        x = c1 < s.size[l - 2] ? pb[(s.off[l - 2] + c0) * D + c] - pb[(s.off[l - 2] + c1) * D + c] : 0.0f;
+      }
+      v[m] = x;
+      mx = fmaxf(mx, fabsf(x));
+    }
+    mx = warp_max(mx);
+    const int e = row_exponent(mx);
+    const float sc = pow2f(e);
+    float ss = 0.0f;
+    __half* hi = (kind == 0 ? mu_hi : dd_hi) + r * D;
+    __half* lo = (kind == 0 ? mu_lo : dd_lo) + r * D;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      if (m >= per) break;
+      const int c = lane + 32 * m;
+      const float xs = v[m] * sc;
+      const __half h = __float2half_rn(xs);
+      const __half lw = __float2half_rn(xs - __half2float(h));
+      const float lf = __half2float(lw);
+      ss = fmaf(lf, lf, ss);
+      const int p = row_pos(c, D);
+      hi[p] = h;
+      lo[p] = lw;
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) meta[r * 2 + kind] = make_float2(pow2f(-e), sqrtf(ss) * pow2f(-e));
+  }
+}
+
+template <int NC>
+struct HaarQ {
+  float4 x[2][NC];  // own dots per head of the candidate lists (log2 units, root-relative)
+  float4 y[NC];     // raw MMA dots of the current pass, by slot
+  int32_t cand[2][NC];
+};
+
+template <int NC>
+struct HaarQPad : HaarQ<NC> {
+  // the two queries of a warp start 16 banks apart
+  static constexpr int kWords = (int)(sizeof(HaarQ<NC>) / 4);
+  static constexpr int kPad = (16 - kWords % 32 + 64) % 32;
+  int32_t pad[kPad > 0 ? kPad : 4];
+};
+
+struct HaarView {
+  const uint16_t* mu_hi;
+  const uint16_t* mu_lo;
+  const uint16_t* dd_hi;
+  const uint16_t* dd_lo;
+  const float4* meta;
+  int64_t P2;
+};
+
+// Dots of the rows (hi, plus lo where lomask says so) of the candidates of
+// both queries of the warp, raw MMA results (row and query scales not yet
+// applied) into sm[u].y[slot].  Query u's candidates are
+// smw[u].cand[cur[u]][0, nw[u]); lomask[u]: bit i set when slot i of query u
+// needs its residual row.
+template <int D, int NC>
+__device__ __forceinline__ void haar_dots(HaarQPad<NC>* smw, const int (&cur)[2], const uint16_t* __restrict__ hi,
+                                          const uint16_t* __restrict__ lo, const int64_t (&pbase)[2], int64_t rowoff,
+                                          const int (&nw)[2], const uint64_t (&lomask)[2],
+                                          const uint32_t (&bq)[2][D / 64][4], int lane) {
+  constexpr int NB = D / 64;
+  const int grp = lane >> 2, tig = lane & 3;
+  const int nmax = max(nw[0], nw[1]);
+  const int64_t loff = rowoff * D + (grp & 1) * 32 + 8 * tig;
+  const bool roleA = !(grp & 1) && tig < 2, roleB = (grp & 1) && tig >= 2;
+#pragma unroll
+  for (int r0 = 0; r0 < NC; r0 += 8) {
+    if (r0 >= nmax) break;
+    uint32_t ro[2][2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int w = r0 + 4 * rr + (grp >> 1);
+        ro[u][rr] = (uint32_t)(w < nw[u] ? smw[u].cand[cur[u]][w] : 0) * (uint32_t)D;
+      }
+    float d[2][4];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) d[u][e] = 0.0f;
+    {
+      uint4 hv[2][2][NB];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+          for (int bb = 0; bb < NB; ++bb)
+            hv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(hi + pbase[u] + loff + ro[u][rr] + 64 * bb));
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint4 h0 = hv[u][0][bb], h1 = hv[u][1][bb];
+          mma_f16_16816(d[u], h0.x, h1.x, h0.y, h1.y, bq[u][bb][0], bq[u][bb][1]);
+          mma_f16_16816(d[u], h0.z, h1.z, h0.w, h1.w, bq[u][bb][2], bq[u][bb][3]);
+        }
+    }
+    if ((((lomask[0] | lomask[1]) >> r0) & 0xffull) != 0ull) {  // warp-uniform
+      uint4 lv[2][2][NB];
+#pragma unroll
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+          for (int bb = 0; bb < NB; ++bb)
+            lv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(lo + pbase[u] + loff + ro[u][rr] + 64 * bb));
+#pragma unroll
+      for (int bb = 0; bb < NB; ++bb)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const uint4 l0 = lv[u][0][bb], l1 = lv[u][1][bb];
+          mma_f16_16816(d[u], l0.x, l1.x, l0.y, l1.y, bq[u][bb][0], bq[u][bb][1]);
+          mma_f16_16816(d[u], l0.z, l1.z, l0.w, l1.w, bq[u][bb][2], bq[u][bb][3]);
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      // add the two halves: partner lane = lane ^ 6 (group ^ 1, t ^ 2)
+      const float x0 = __shfl_xor_sync(0xffffffffu, roleA ? d[u][2] : d[u][0], 6);
+      const float x1 = __shfl_xor_sync(0xffffffffu, roleA ? d[u][3] : d[u][1], 6);
+      const int w = r0 + (roleA ? 0 : 4) + (grp >> 1);
+      if ((roleA || roleB) && w < nw[u]) {
+        const float2 v = roleA ? make_float2(d[u][0] + x0, d[u][1] + x1) : make_float2(d[u][2] + x0, d[u][3] + x1);
+        *reinterpret_cast<float2*>(reinterpret_cast<float*>(&smw[u].y[w]) + 2 * (tig & 1)) = v;
+      }
+    }
+  }
+}
+
+template <int D, int KM, int WARPS, bool kLse>
+__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
+    route_haar_kernel(Prob pr, Pyr s, const uint16_t* __restrict__ q, HaarView hv, int32_t* __restrict__ kept2,
+                      int32_t* __restrict__ trace) {
+  constexpr int G = 4;
+  constexpr int NC = 2 * KM;
+  constexpr int CPL = NC / 16;
+  constexpr int NB = D / 64;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  HaarQPad<NC>& sm = reinterpret_cast<HaarQPad<NC>*>(smem_raw)[threadIdx.x / 16];
+  HaarQPad<NC>* smw = reinterpret_cast<HaarQPad<NC>*>(smem_raw) + (threadIdx.x / 32) * 2;
+  const int lane = threadIdx.x & 31, ll = lane & 15, half = lane >> 4;
+  const int grp = lane >> 2, tig = lane & 3;
+  // query counts are below 2^31 (the prefill size limit), so 32-bit index math
+  const uint32_t nq = (uint32_t)(pr.B * pr.Hkv * pr.N), N32 = (uint32_t)pr.N;
+  const uint32_t qi = (blockIdx.x * WARPS + threadIdx.x / 32) * 2 + half;
+  const bool live = qi < nq;
+  const uint32_t qc = live ? qi : nq - 1;
+  const int64_t t = qc % N32;
+  const int K = pr.K;
+  const int64_t qb = t / s.C;
+  int32_t* kout = kept2 + (int64_t)qc * K;
+  int32_t* trow = (trace && live) ? trace + (int64_t)qc * s.L * K : nullptr;
+  if (trow)
+    for (int i = ll; i < s.L * K; i += 16) trow[i] = -1;
+
+  int l0 = 0;
+  if (live && qb - 2 >= 1) {
+    // start level: the highest level with more than K eligible nodes, i.e.
+    // the largest l <= L with (qb - 2) >> (l - 1) >= K
+    const uint32_t xk = (uint32_t)(qb - 2) / (uint32_t)K;
+    if (xk >= 2) l0 = min((int)s.L, 32 - __clz(xk));
+    if (l0 < 2) l0 = 0;
+    if (trow)
+      for (int level = s.L; level >= 2 && level > l0; --level) {
+        const int64_t n = eligible_count(level, qb);
+        for (int i = ll; i < n; i += 16) trow[(level - 1) * K + i] = i;
+      }
+    if (l0 == 0) {
+      const int64_t n2 = eligible_count(2, qb);
+      for (int i = ll; i < K; i += 16) kout[i] = i < n2 ? i : -1;
+    }
+  } else if (live) {
+    for (int i = ll; i < K; i += 16) kout[i] = -1;
+  }
+  const int l0o = __shfl_xor_sync(0xffffffffu, l0, 16);
+  const int l0w = max(l0, l0o);
+  if (l0w == 0) return;  // warp-uniform
+
+  // B fragments of both queries: column grp = (head grp % 4, half grp / 4),
+  // converted to fp16 with a power-of-two scale per query (exact for bf16
+  // inputs in range); per-query head norms for the residual bound.
+  const uint32_t qw = (blockIdx.x * WARPS + threadIdx.x / 32) * 2;
+  uint32_t bq[2][NB][4];
+  int64_t pbase[2], mbase[2];
+  float qfac[2], bfac[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const uint32_t qu = min(qw + u, nq - 1);
+    const uint32_t tu = qu % N32, bhu = qu / N32;
+    const uint32_t Hkv = (uint32_t)pr.Hkv;
+    const int64_t qrow = ((int64_t)((bhu / Hkv) * (uint32_t)pr.Hq + (bhu % Hkv) * G + (grp & 3)) * pr.N + tu) * D +
+                         (grp >> 2) * (D / 2) + 8 * tig;
+    float f[NB][8];
+    float mx = 0.0f, ss = 0.0f;
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(q + qrow + 32 * bb));
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        f[bb][2 * e] = __uint_as_float(wv[e] << 16);
+        f[bb][2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        mx = fmaxf(mx, fabsf(f[bb][e]));
+        ss = fmaf(f[bb][e], f[bb][e], ss);
+      }
+    }
+    mx = warp_max(mx);
+    const int e = row_exponent(mx);
+    const float sc = pow2f(e);
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) bq[u][bb][w] = pack_f16x2(f[bb][2 * w] * sc, f[bb][2 * w + 1] * sc);
+    qfac[u] = pow2f(-e) * pr.scale2;
+    // |q_h|^2: lanes of head h are grp in {h, h + 4}, any tig
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+    float hn = sqrtf(ss);
+    hn += __shfl_xor_sync(0xffffffffu, hn, 4);
+    hn += __shfl_xor_sync(0xffffffffu, hn, 8);
+    bfac[u] = hn * pr.scale2;  // bound per unit of residual norm: sum over heads of s |q_h| (log2 units)
+    pbase[u] = (int64_t)bhu * hv.P2 * D;
+    mbase[u] = (int64_t)bhu * hv.P2;
+  }
+  const float myq = half ? qfac[1] : qfac[0], mybf = half ? bfac[1] : bfac[0];
+  const int64_t mymb = half ? mbase[1] : mbase[0];
+
+  int cur = 0;
+  int nc = l0 > 0 ? (int)eligible_count(l0, qb) : 0;
+  for (int i = ll; i < nc; i += 16) sm.cand[0][i] = i;
+  const int e_hi = (int)(qb - 2);
+  const int64_t n1 = s.size[0];
+  __syncwarp();
+
+  for (int level = l0w; level >= 2; --level) {
+    const bool act = level <= l0;
+    const int ncur = act ? nc : 0;
+    const bool start = act && level == l0;
+    const int ncap = (int)s.size[level - 2];
+    const int64_t rowoff = s.off[level - 1] - n1;
+
+    int cv[CPL];
+    float4 mt[CPL];
+    float4 xv[CPL];
+#pragma unroll
+    for (int sl = 0; sl < CPL; ++sl) {
+      const int i = sl * 16 + ll;
+      const bool valid = i < ncur;
+      cv[sl] = valid ? sm.cand[cur][i] : 0;
+      mt[sl] = valid ? __ldg(hv.meta + mymb + rowoff + cv[sl]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      xv[sl] = (valid && !start) ? sm.x[cur][i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const int nwu[2] = {__shfl_sync(0xffffffffu, ncur, 0), __shfl_sync(0xffffffffu, ncur, 16)};
+    const int curu[2] = {__shfl_sync(0xffffffffu, cur, 0), __shfl_sync(0xffffffffu, cur, 16)};
+
+    // start level: the candidates' own dots from their MU rows
+    const unsigned st_b = __ballot_sync(0xffffffffu, start);
+    if (st_b) {
+      uint64_t lm[2] = {0ull, 0ull};
+#pragma unroll
+      for (int sl = 0; sl < CPL; ++sl) {
+        const bool need = start && sl * 16 + ll < ncur && mybf * mt[sl].y > kLoTau;
+        const unsigned b = __ballot_sync(0xffffffffu, need);
+        lm[0] |= (uint64_t)(b & 0xffffu) << (16 * sl);
+        lm[1] |= (uint64_t)(b >> 16) << (16 * sl);
+      }
+      const int ns[2] = {(st_b & 1u) ? nwu[0] : 0, (st_b >> 16) ? nwu[1] : 0};
+      haar_dots<D, NC>(smw, curu, hv.mu_hi, hv.mu_lo, pbase, rowoff, ns, lm, bq, lane);
+      __syncwarp();
+#pragma unroll
+      for (int sl = 0; sl < CPL; ++sl) {
+        const int i = sl * 16 + ll;
+        if (start && i < ncur) {
+          const float4 r = sm.y[i];
+          const float f = mt[sl].x * myq;
+          xv[sl] = make_float4(r.x * f, r.y * f, r.z * f, r.w * f);
+        }
+      }
+      __syncwarp();
+    }
+
+    // every level: the candidates' DD rows give both children's dots
+    {
+      uint64_t lm[2] = {0ull, 0ull};
+#pragma unroll
+      for (int sl = 0; sl < CPL; ++sl) {
+        const bool need = sl * 16 + ll < ncur && mybf * mt[sl].w > kLoTau;
+        const unsigned b = __ballot_sync(0xffffffffu, need);
+        lm[0] |= (uint64_t)(b & 0xffffu) << (16 * sl);
+        lm[1] |= (uint64_t)(b >> 16) << (16 * sl);
+      }
+      haar_dots<D, NC>(smw, curu, hv.dd_hi, hv.dd_lo, pbase, rowoff, nwu, lm, bq, lane);
+    }
+    __syncwarp();
+
+    // scores and rank keys (higher score first, then lower index)
+    uint32_t key[CPL];
+    float4 ya[CPL], yb[CPL];
+    int e0v[CPL], e1v[CPL];
+#pragma unroll
+    for (int sl = 0; sl < CPL; ++sl) {
+      const int i = sl * 16 + ll;
+      key[sl] = 0;
+      e0v[sl] = e1v[sl] = 0;
+      ya[sl] = yb[sl] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < ncur) {
+        const int c0 = 2 * cv[sl];
+        const bool has1 = c0 + 1 < ncap;
+        e0v[sl] = elig_node_h(level - 1, c0, e_hi);
+        e1v[sl] = has1 && elig_node_h(level - 1, c0 + 1, e_hi);
+        // child weights: only the last node of a level can hold fewer keys
+        float w0 = 0.5f, w1 = 0.5f;
+        if (c0 + 2 >= ncap) {
+          const float n0 = (float)count_node_h(s.C, level - 1, c0, s.N);
+          const float nn1 = has1 ? (float)count_node_h(s.C, level - 1, c0 + 1, s.N) : 0.0f;
+          w0 = nn1 / (n0 + nn1);
+          w1 = n0 / (n0 + nn1);
+        }
+        const float4 r = sm.y[i];
+        const float f = mt[sl].z * myq;
+        const float4 x = xv[sl];
+        const float yv[4] = {r.x * f, r.y * f, r.z * f, r.w * f};
+        ya[sl] = make_float4(fmaf(w0, yv[0], x.x), fmaf(w0, yv[1], x.y), fmaf(w0, yv[2], x.z), fmaf(w0, yv[3], x.w));
+        yb[sl] = make_float4(fmaf(-w1, yv[0], x.x), fmaf(-w1, yv[1], x.y), fmaf(-w1, yv[2], x.z),
+                             fmaf(-w1, yv[3], x.w));
+        const bool both = e0v[sl] && e1v[sl];
+        float scv = 0.0f;
+        if constexpr (kLse) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float a = comp4(ya[sl], g), bb = comp4(yb[sl], g);
+            scv += both ? lse2_pair(a, bb) : (e0v[sl] ? a : bb);
+          }
+        } else {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float a = comp4(ya[sl], g), bb = comp4(yb[sl], g);
+            scv += both ? pair_score(pr.scorer, a, bb) : (e0v[sl] ? a : bb);
+          }
+        }
+        if (scv == 0.0f) scv = 0.0f;     // -0 ranks like +0
+        if (scv != scv) scv = -INFINITY;  // NaN ranks last (keys stay <= 0xff800000)
+        key[sl] = orderable_key_h(scv);
+      }
+    }
+    int rank[CPL];
+#pragma unroll
+    for (int sl = 0; sl < CPL; ++sl) rank[sl] = 0;
+#pragma unroll
+    for (int sj = 0; sj < CPL; ++sj) {
+#pragma unroll
+      for (int l = 0; l < 16; ++l) {
+        const uint32_t kj = __shfl_sync(0xffffffffu, key[sj], l, 16);
+#pragma unroll
+        for (int sl = 0; sl < CPL; ++sl) {
+          // equal scores: the lower slot (the lower node index) ranks first.
+          // Keys of real scores are at most 0xff800000, so kj + 1 cannot wrap.
+          const uint32_t before = (sj < sl || (sj == sl && l < ll)) ? 1u : 0u;
+          rank[sl] += (kj + before > key[sl]) ? 1 : 0;
+        }
+      }
+    }
+
+    // kept set (index order), next candidates (ascending) or the kept level-2 nodes
+    const int nxt = cur ^ 1;
+    int nkept = 0, nchild = 0;
+#pragma unroll
+    for (int sl = 0; sl < CPL; ++sl) {
+      const int i = sl * 16 + ll;
+      const int keep = (i < ncur && rank[sl] < K) ? 1 : 0;
+      const int nch = keep && level > 2 ? e0v[sl] + e1v[sl] : 0;
+      int ktot, ctot;
+      const int kp = nkept + prefix16h(keep, lane, &ktot);
+      int cp = nchild + prefix16h(nch, lane, &ctot);
+      if (keep) {
+        const int32_t ci = cv[sl];
+        if (trow) trow[(level - 1) * K + kp] = ci;
+        if (level == 2) kout[kp] = ci;
+        if (e0v[sl] && nch) {
+          sm.cand[nxt][cp] = 2 * ci;
+          sm.x[nxt][cp] = ya[sl];
+          ++cp;
+        }
+        if (e1v[sl] && nch) {
+          sm.cand[nxt][cp] = 2 * ci + 1;
+          sm.x[nxt][cp] = yb[sl];
+        }
+      }
+      nkept += ktot;
+      nchild += ctot;
+    }
+    if (level == 2 && act)
+      for (int i = nkept + ll; i < K; i += 16) kout[i] = -1;
+    if (act) {
+      nc = nchild;
+      cur = nxt;
+    }
+    __syncwarp();
+  }
+}
+
+template <int D, int KM, int WARPS, bool kLse>
+static cudaError_t launch_route_haar_t(const Prob& pr, const Pyr& s, const void* q, const HaarView& hv, int32_t* kept2,
+                                       int32_t* trace, cudaStream_t st) {
+  const size_t smem = sizeof(HaarQPad<2 * KM>) * 2 * WARPS;
+  auto kern = route_haar_kernel<D, KM, WARPS, kLse>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int64_t nq = pr.B * pr.Hkv * pr.N;
+  note_launch();
+  kern<<<(unsigned)ceil_div64(nq, 2 * WARPS), WARPS * 32, smem, st>>>(pr, s, (const uint16_t*)q, hv, kept2, trace);
+  return cudaGetLastError();
+}
+
+bool route_haar_supported(const Prob& pr) {
+  return pr.dtype == PISA_BF16 && pr.G == 4 && (pr.d == 64 || pr.d == 128);
+}
+
+size_t haar_rows_bytes(const Prob& pr, const Pyr& s) {
+  const int64_t P2 = s.L >= 2 ? s.P - s.size[0] : 0;
+  return (size_t)pr.B * pr.Hkv * P2 * pr.d * 2;  // one fp16 array (of four)
+}
+
+size_t haar_meta_bytes(const Prob& pr, const Pyr& s) {
+  const int64_t P2 = s.L >= 2 ? s.P - s.size[0] : 0;
+  return (size_t)pr.B * pr.Hkv * P2 * 16;
+}
+
+cudaError_t launch_route_haar(const Prob& pr, const Pyr& s, const void* q, const float* pyr, char* rows,
+                              float4* meta, int32_t* kept2, int32_t* trace, cudaStream_t st) {
+  const int64_t BH = pr.B * pr.Hkv;
+  const int64_t P2 = s.L >= 2 ? s.P - s.size[0] : 0;
+  const size_t arr = haar_rows_bytes(pr, s);
+  HaarView hv{(const uint16_t*)rows, (const uint16_t*)(rows + arr), (const uint16_t*)(rows + 2 * arr),
+              (const uint16_t*)(rows + 3 * arr), meta, P2};
+  if (P2 > 0) {
+    const int64_t warps = BH * P2 * 2;
+    note_launch();
+    haar_prep_kernel<<<(unsigned)std::min<int64_t>(ceil_div64(warps, 8), 16384), 256, 0, st>>>(
+        BH, s, pr.d, pyr, (__half*)rows, (__half*)(rows + arr), (__half*)(rows + 2 * arr), (__half*)(rows + 3 * arr),
+        reinterpret_cast<float2*>(meta));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+#define PISA_RH_CASE(DD, LSE)                                                                            \
+  if (pr.d == DD && (pr.scorer == PISA_SCORER_LSE) == LSE) {                                             \
+    if (pr.K <= 8) return launch_route_haar_t<DD, 8, 8, LSE>(pr, s, q, hv, kept2, trace, st);            \
+    if (pr.K <= 16) return launch_route_haar_t<DD, 16, 8, LSE>(pr, s, q, hv, kept2, trace, st);          \
+    return launch_route_haar_t<DD, 32, 4, LSE>(pr, s, q, hv, kept2, trace, st);                          \
+  }
+  PISA_RH_CASE(128, true) PISA_RH_CASE(64, true) PISA_RH_CASE(128, false) PISA_RH_CASE(64, false)
+#undef PISA_RH_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pisa

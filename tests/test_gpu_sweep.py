@@ -11,7 +11,7 @@ sweep from 4K to 256K tokens at C = 64, K = 8):
   * 128K: the whole second chunk plus the last 2,048 positions of the first,
     for every key head, so both chunk boundaries are crossed;
   * 256K: the 128 positions on each side of every chunk boundary, the last
-    two leaf blocks and 25,000 random positions, for every key head
+    two leaf blocks and 26,500 random draws of a position, for every key head
     (over 100,000 pairs).
 The rule is the selector's tolerance (tests/parity.py): identical index sets
 except where the oracle's K-th and (K+1)-th scores differ by < 1e-3 on some
@@ -45,7 +45,7 @@ def positions(N):
     if N == 2 * CHUNK:
         return np.arange(CHUNK - 2048, N)
     gen = np.random.default_rng(17)
-    ts = set(gen.integers(0, N, 25000).tolist()) | set(range(N - 128, N))
+    ts = set(gen.integers(0, N, 26500).tolist()) | set(range(N - 128, N))
     for c in range(1, N // CHUNK):
         ts |= set(range(c * CHUNK - 128, c * CHUNK + 128))
     return np.array(sorted(ts))
