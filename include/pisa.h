@@ -19,7 +19,7 @@
  * at the root and keeps all candidates while a level has at most K; a node is
  * eligible when its leaf range meets E = [1, qb-2] (qb = t / C); summaries are
  * plain means of the keys present in a node's span (not masked by the query
- * position); the group score is the sum of the heads' natural-log LSEs; the
+ * position, unless PISA_SUMMARIES_PREFIX is asked for); the group score is the sum of the heads' natural-log LSEs; the
  * scale is 1/sqrt(d) unless given; Top-K ties go to the lower node index;
  * the forced blocks F = {0, qb-1, qb} are added to the Top-K of E.
  *
@@ -66,7 +66,7 @@
 extern "C" {
 #endif
 
-#define PISA_ABI_VERSION 2
+#define PISA_ABI_VERSION 3
 
 typedef enum {
   PISA_OK = 0,
@@ -96,6 +96,23 @@ typedef enum {
   PISA_SCORER_MEAN_VAR = 2
 } pisa_scorer;
 
+/* Which keys a prefill query's node summaries cover (agihunt.info summary,
+ * pyramid paragraph: decode routing walks the pyramid of the keys seen so
+ * far; rcap.io, the pisa_select sketch walks summaries without a mask).
+ *   PISA_SUMMARIES_ALL     every key of the node's span (the pyramid of the
+ *                          whole sequence; a summary straddling position t
+ *                          includes keys after t)
+ *   PISA_SUMMARIES_PREFIX  the span's keys at positions <= t only, i.e. the
+ *                          pyramid of the first t + 1 keys, which is what the
+ *                          decode step at length t + 1 walks (prefix-
+ *                          consistent, leak-free)
+ * Leaf scores read complete past blocks under both, and the decode, flat and
+ * attention calls ignore the field. */
+typedef enum {
+  PISA_SUMMARIES_ALL = 0,
+  PISA_SUMMARIES_PREFIX = 1
+} pisa_summaries;
+
 typedef enum {
   PISA_MODE_PREFILL = 0,
   PISA_MODE_DECODE = 1,
@@ -123,6 +140,7 @@ typedef struct {
   int32_t qtile;        /* queries sharing one leaf tile (reuse only) */
   float scale;          /* score scale inside exp(); 0 means 1/sqrt(d) */
   int32_t scorer;       /* pisa_scorer (0: the log-sum-exp of PISA) */
+  int32_t summaries;    /* pisa_summaries of prefill walks (0: all keys) */
 } pisa_params;
 
 /* ABI version of the loaded library (PISA_ABI_VERSION). */
@@ -183,6 +201,8 @@ pisa_status pisa_select_prefill(const pisa_params* p, const void* q,
  *   pisa_prefill_route: clears the status word and walks levels L..2 for
  *     every query (rcap.io, "Selection walks the tree top-down"), leaving the
  *     kept level-2 nodes of each query in the workspace; writes `trace`.
+ *     With PISA_SUMMARIES_PREFIX it returns PISA_ERR_UNSUPPORTED (that walk
+ *     reads the raw keys of each query's own leaf): use pisa_select_prefill.
  *   pisa_prefill_leaves: scores the leaf candidates (the two children of each
  *     kept level-2 node) by LSE over their raw keys and writes out_idx and
  *     out_score.  It must follow pisa_prefill_route on the same workspace
@@ -337,6 +357,18 @@ pisa_status pisa_attend_decode(const pisa_params* p, const void* q,
                                const int32_t* seq_lens, const int32_t* idx,
                                void* ws, size_t ws_bytes, void* out,
                                void* stream);
+
+/* TEST ONLY: fault injection for the bounded device waits of the tcgen05
+ * leaf stage (the leaf kernel of pisa_select_prefill and
+ * pisa_prefill_leaves with bf16 inputs).  wait_limit_ns replaces the 4 s
+ * limit of every wait in later launches (0 restores it); with
+ * drop_first_key_tile != 0 the first CTA announces its first key tile on the
+ * stage barrier but never issues the copy, so its first MMA wait can only run
+ * out.  The kernel then sets PISA_DEV_TIMEOUT in the status word, lets every
+ * copy and MMA it issued complete, frees its tensor memory and returns; the
+ * call's outputs are then undefined.  Process-wide, not synchronised with
+ * launches in flight; never needed outside tests. */
+void pisa_test_inject_leaf_timeout(uint64_t wait_limit_ns, int32_t drop_first_key_tile);
 
 /* Synchronises `stream`, then copies the workspace status word into
  * *device_code (PISA_DEV_*).  Returns PISA_ERR_DEVICE when it is non-zero. */

@@ -232,6 +232,40 @@ class Oracle:
         return out
 
 
+def attention_mass(q, k, idx, sel, C: int, scale: float = 0.0, qrows: bool = False) -> np.ndarray:
+    """Attention-mass ratio of a selection (agihunt.info summary, quality
+    paragraph: the share of full attention's softmax mass that falls on the
+    selected blocks).  For query (b, h, t) and each head g of its GQA group,
+    the causal softmax over keys 0..t of s q_g . k_i is summed over the keys
+    of the distinct blocks listed in its row of idx (entries outside
+    [0, t // C] add nothing), then averaged over the group's heads.
+    q [B, Hq, N, d] (or, with qrows, [nsel, G, d]), k [B, Hkv, N, d],
+    idx [nsel, W] the selection rows of the sel triples (b, h, t).
+    Plain fp64 numpy, one query at a time; returns [nsel]."""
+    q = _f64(q)
+    k = _f64(k)
+    idx = np.asarray(idx)
+    Hkv, d = k.shape[1], k.shape[3]
+    G = q.shape[1] // Hkv if not qrows else q.shape[1]
+    s = scale if scale > 0 else 1.0 / np.sqrt(d)
+    out = np.empty(len(sel), np.float64)
+    for n, (b, h, t) in enumerate(sel):
+        keys = k[b, h, :t + 1]
+        blocks = {int(j) for j in idx[n] if 0 <= j <= t // C}
+        mask = np.zeros(t + 1, bool)
+        for j in blocks:
+            mask[j * C:min((j + 1) * C, t + 1)] = True
+        r = 0.0
+        for g in range(G):
+            qg = q[n, g] if qrows else q[b, h * G + g, t]
+            x = s * (keys @ qg)
+            m = x.max()
+            w = np.exp(x - m)
+            r += w[mask].sum() / w.sum()
+        out[n] = r / G
+    return out
+
+
 def num_threads() -> int:
     return lib().po_num_threads()
 

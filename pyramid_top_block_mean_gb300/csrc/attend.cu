@@ -226,11 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         last_bh = info.x;
         last_j = info.w;
       }
-      if (!ok) {
-        *abort = 1;
-        for (int k = bcount > SB ? bcount - SB : 0; k < bcount; ++k)
-          ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k % SB]), (k / SB) & 1, &sm.zero, kWaitLimitNs);
-      }
+      if (!ok) *abort = 1;
+      // every issued load lands before the CTA can exit, whoever gave up
+      for (int k = bcount > SB ? bcount - SB : 0; k < bcount; ++k)
+        ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k % SB]), (k / SB) & 1, &sm.zero, kWaitLimitNs);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {

@@ -166,13 +166,12 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
           ++ib;
         }
     }
-    if (!ok) {
-      *abort = 1;
-      if (lane == 0)
-        for (int k = ib > kFStagesB ? ib - kFStagesB : 0; k < ib; ++k)
-          ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k % kFStagesB]), (k / kFStagesB) & 1, &sm.zero,
-                                 kFWaitNs);
-    }
+    if (!ok) *abort = 1;
+    // every issued load lands before the CTA can exit, whoever gave up
+    if (lane == 0)
+      for (int k = ib > kFStagesB ? ib - kFStagesB : 0; k < ib; ++k)
+        ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k % kFStagesB]), (k / kFStagesB) & 1, &sm.zero,
+                               kFWaitNs);
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {

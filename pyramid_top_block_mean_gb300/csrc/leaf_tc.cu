@@ -28,6 +28,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "pisa_common.cuh"
@@ -50,6 +51,18 @@ constexpr int kEpiWarps = 8;             // the next 8 warps: (TMEM lane quadran
 constexpr int kLeafTcThreads = 32 * (kMmaWarp + 1 + kEpiWarps);
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
+
+// Host-side fault injection for tests of the bounded waits
+// (pisa_test_inject_leaf_timeout): a shorter wait limit, and whether CTA 0
+// announces its first key tile on the stage barrier without issuing the copy,
+// so that the first MMA wait can only run out.  Zero means the defaults.
+std::atomic<uint64_t> g_test_wait_ns{0};
+std::atomic<int32_t> g_test_drop_tile{0};
+
+struct LeafWaits {
+  uint64_t limit_ns;
+  int32_t drop_first_tile;
+};
 
 template <int D>
 struct LeafTcSmem {
@@ -276,7 +289,8 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
     leaf_tc_kernel(Prob pr, const __grid_constant__ CUtensorMap kmap,
                    const uint16_t* __restrict__ q, const int4* __restrict__ tile_info,
                    const int32_t* __restrict__ tile_total, const int32_t* __restrict__ pairs,
-                   float* __restrict__ leaf_score, int32_t* __restrict__ status) {
+                   float* __restrict__ leaf_score, int32_t* __restrict__ status, LeafWaits waits) {
+  const uint64_t kWaitLimitNs = waits.limit_ns;  // shadows the default: every wait below is bounded by it
   extern __shared__ unsigned char smem_raw[];
   LeafTcSmem<D>& sm = *reinterpret_cast<LeafTcSmem<D>*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -425,9 +439,12 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
           const uint32_t fb = ptx::smem_u32(&sm.full_b[sb]);
           ptx::mbar_arrive_expect_tx(fb, kBBytes);
           const int32_t y = (int32_t)(bh * pr.N + 128 * (int64_t)p);
+          // injected fault (tests only): the first tile is announced, never copied
+          const bool drop = waits.drop_first_tile && blockIdx.x == 0 && bcount == 0;
+          if (!drop)
 #pragma unroll
-          for (int hh = 0; hh < D / 64; ++hh)
-            ptx::tma_load_2d(ptx::smem_u32(sm.b[sb]) + hh * kHalf, &kmap, 64 * hh, y, fb);
+            for (int hh = 0; hh < D / 64; ++hh)
+              ptx::tma_load_2d(ptx::smem_u32(sm.b[sb]) + hh * kHalf, &kmap, 64 * hh, y, fb);
           ++bcount;
           last_bh = bh;
           last_p = p;
@@ -435,13 +452,13 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
         info = info1;
         info1 = info2;
       }
-      if (!ok) {
-        *abort = 1;
-        // let TMA loads already issued land before the CTA can exit
-        for (int k = bcount > kStagesB ? bcount - kStagesB : 0; k < bcount; ++k)
-          ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k % kStagesB]), (k / kStagesB) & 1, &sm.zero,
-                                 kWaitLimitNs);
-      }
+      if (!ok) *abort = 1;
+      // let every TMA load issued land before the CTA can exit, whoever gave
+      // up (the MMA thread may abort while loads it will never consume are in
+      // flight); after a normal run these phases have completed already
+      for (int k = bcount > kStagesB ? bcount - kStagesB : 0; k < bcount; ++k)
+        ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k % kStagesB]), (k / kStagesB) & 1, &sm.zero,
+                               kWaitLimitNs);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -740,6 +757,8 @@ template <int D, int G>
 static cudaError_t launch_leaf_tc_t(const Prob& pr, const PrefillWs& w, char* ws, const CUtensorMap& kmap,
                                     const void* q, int grid, cudaStream_t st) {
   const size_t smem = sizeof(LeafTcSmem<D>) + 1024;
+  const uint64_t tw = g_test_wait_ns.load(std::memory_order_relaxed);
+  const LeafWaits waits{tw ? tw : kWaitLimitNs, g_test_drop_tile.load(std::memory_order_relaxed)};
   auto kern = leaf_tc_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -748,7 +767,7 @@ static cudaError_t launch_leaf_tc_t(const Prob& pr, const PrefillWs& w, char* ws
                                            (const int4*)(ws + w.tile_info),
                                            (const int32_t*)(ws + w.tile_off) + w.nbuckets,
                                            (const int32_t*)(ws + w.pairs), (float*)(ws + w.leaf_score),
-                                           (int32_t*)(ws + w.status));
+                                           (int32_t*)(ws + w.status), waits);
   return cudaGetLastError();
 }
 
@@ -825,3 +844,8 @@ cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, cha
 }
 
 }  // namespace pisa
+
+extern "C" void pisa_test_inject_leaf_timeout(uint64_t wait_limit_ns, int32_t drop_first_key_tile) {
+  pisa::g_test_wait_ns.store(wait_limit_ns, std::memory_order_relaxed);
+  pisa::g_test_drop_tile.store(drop_first_key_tile ? 1 : 0, std::memory_order_relaxed);
+}

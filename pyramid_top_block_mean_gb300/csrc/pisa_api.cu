@@ -56,6 +56,7 @@ PrefillWs prefill_ws_layout(const Prob& pr, const Pyr& s) {
   w.tile_info = o; o = align_up(o + (size_t)w.max_tiles * 16, 256);
   w.haar_rows = o; o = align_up(o + 4 * haar_rows_bytes(pr, s), 256);
   w.haar_meta = o; o = align_up(o + haar_meta_bytes(pr, s), 256);
+  w.path = o; o = align_up(o + path_dots_bytes(pr, s), 256);
   w.total = o;
   return w;
 }
@@ -109,6 +110,7 @@ static pisa_status check_params(const pisa_params* p, Prob* pr, Pyr* s) {
   if (p->H_q % p->H_kv != 0) return PISA_ERR_INVALID_ARG;
   if (!(p->scale >= 0.0f) || isinf(p->scale)) return PISA_ERR_INVALID_ARG;
   if (p->scorer < PISA_SCORER_LSE || p->scorer > PISA_SCORER_MEAN_VAR) return PISA_ERR_INVALID_ARG;
+  if (p->summaries != PISA_SUMMARIES_ALL && p->summaries != PISA_SUMMARIES_PREFIX) return PISA_ERR_INVALID_ARG;
   if (p->dtype != PISA_BF16 && p->dtype != PISA_FP32) return PISA_ERR_UNSUPPORTED;
   const int G = p->H_q / p->H_kv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return PISA_ERR_UNSUPPORTED;
@@ -118,6 +120,7 @@ static pisa_status check_params(const pisa_params* p, Prob* pr, Pyr* s) {
   if (!make_pyr(p->N, p->C, s)) return PISA_ERR_INVALID_ARG;
   pr->B = p->B; pr->N = p->N; pr->Hq = p->H_q; pr->Hkv = p->H_kv; pr->G = G;
   pr->d = p->d; pr->C = p->C; pr->K = p->K; pr->dtype = p->dtype; pr->scorer = p->scorer;
+  pr->prefix = p->summaries == PISA_SUMMARIES_PREFIX ? 1 : 0;
   const float sc = p->scale > 0.0f ? p->scale : 1.0f / sqrtf((float)p->d);
   pr->scale2 = sc * kLog2e;
   return PISA_OK;
@@ -249,14 +252,23 @@ static pisa_status prefill_checks(const pisa_params* p, Prob* pr, Pyr* s, Prefil
   return PISA_OK;
 }
 
-static pisa_status run_route(const Prob& pr, const Pyr& s, const PrefillWs& w, const void* q, const float* pyramid,
-                             char* base, int32_t* trace, cudaStream_t st) {
+// k is needed only for prefix-consistent summaries (the partial leaf of each
+// query's path).
+static pisa_status run_route(const Prob& pr, const Pyr& s, const PrefillWs& w, const void* q, const void* k,
+                             const float* pyramid, char* base, int32_t* trace, cudaStream_t st) {
   int32_t* status = (int32_t*)(base + w.status);
   if (cudaMemsetAsync(status, 0, 256, st) != cudaSuccess) return PISA_ERR_CUDA;
-  if (route_haar_supported(pr))
-    return cuda_status(launch_route_haar(pr, s, q, pyramid, base + w.haar_rows, (float4*)(base + w.haar_meta),
+  const bool haar = route_haar_supported(pr);
+  float* path = nullptr;
+  if (pr.prefix) {
+    path = (float*)(base + w.path);
+    const cudaError_t e = launch_path_dots(pr, s, q, k, pyramid, haar ? 1 : 0, path, st);
+    if (e != cudaSuccess) return PISA_ERR_CUDA;
+  }
+  if (haar)
+    return cuda_status(launch_route_haar(pr, s, q, pyramid, base + w.haar_rows, (float4*)(base + w.haar_meta), path,
                                          (int32_t*)(base + w.kept2), trace, st));
-  return cuda_status(launch_route(pr, s, q, pyramid, (int32_t*)(base + w.kept2), trace, status, st));
+  return cuda_status(launch_route(pr, s, q, pyramid, path, (int32_t*)(base + w.kept2), trace, status, st));
 }
 
 static pisa_status run_leaves(const Prob& pr, const Pyr& s, const PrefillWs& w, const void* q, const void* k,
@@ -279,7 +291,7 @@ pisa_status pisa_select_prefill(const pisa_params* p, const void* q, const void*
                                   trace);
   if (rc != PISA_OK || pr.B * pr.Hkv * pr.N == 0) return rc;
   cudaStream_t st = (cudaStream_t)stream;
-  rc = run_route(pr, s, w, q, pyramid, (char*)ws, trace, st);
+  rc = run_route(pr, s, w, q, k, pyramid, (char*)ws, trace, st);
   if (rc != PISA_OK) return rc;
   return run_leaves(pr, s, w, q, k, (char*)ws, out_idx, out_score, st);
 }
@@ -290,7 +302,8 @@ pisa_status pisa_prefill_route(const pisa_params* p, const void* q, const float*
   pisa_status rc = prefill_checks(p, &pr, &s, &w, q, nullptr, pyramid, ws, ws_bytes, false, true, nullptr, false,
                                   nullptr, trace);
   if (rc != PISA_OK || pr.B * pr.Hkv * pr.N == 0) return rc;
-  return run_route(pr, s, w, q, pyramid, (char*)ws, trace, (cudaStream_t)stream);
+  if (pr.prefix) return PISA_ERR_UNSUPPORTED;  // prefix-consistent walks need the keys: pisa_select_prefill
+  return run_route(pr, s, w, q, nullptr, pyramid, (char*)ws, trace, (cudaStream_t)stream);
 }
 
 pisa_status pisa_prefill_leaves(const pisa_params* p, const void* q, const void* k, void* ws, size_t ws_bytes,

@@ -33,6 +33,7 @@ struct Prob {
   float scale2;     // score scale times log2(e): exponents are taken base 2
   int32_t dtype;    // PISA_BF16 / PISA_FP32
   int32_t scorer;   // pisa_scorer
+  int32_t prefix;   // prefill walks read prefix-consistent summaries (PISA_SUMMARIES_PREFIX)
 };
 
 __host__ __device__ inline int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }

@@ -27,6 +27,7 @@ struct PrefillWs {
   size_t tile_info;   // int4  [max_tiles] {bucket, first pair, pairs, 0}
   size_t haar_rows;   // fp16 4 x [B, Hkv, P2, d]: summary and child-difference rows, hi and lo (P2 = P - n_1)
   size_t haar_meta;   // fp32 [B, Hkv, P2, 4]: row scales and residual norms
+  size_t path;        // fp32 [B, Hkv, N, L, 2, G] prefix-consistent path dots (only with PISA_SUMMARIES_PREFIX)
   size_t total;
   int64_t nbuckets;   // B * Hkv * nchunk * n_2
   int64_t nchunk;     // ceil(N / 2^kChunkShift)
@@ -83,13 +84,20 @@ bool make_tmap_rows(CUtensorMap* m, const void* base, int64_t rows, int d, int b
 
 cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, const KeyPages& kp,
                                  const int32_t* seq_lens, float* pyr, int32_t* status, cudaStream_t st);
-cudaError_t launch_route(const Prob& pr, const Pyr& s, const void* q, const float* pyr, int32_t* kept2,
-                         int32_t* trace, int32_t* status, cudaStream_t st);
+// path: the prefix-consistent path dots of every query (launch_path_dots) or
+// null for summaries over all keys.
+cudaError_t launch_route(const Prob& pr, const Pyr& s, const void* q, const float* pyr, const float* path,
+                         int32_t* kept2, int32_t* trace, int32_t* status, cudaStream_t st);
+size_t path_dots_bytes(const Prob& pr, const Pyr& s);
+// ref_root: dots relative to the finite-masked root summary (the difference-row
+// routing) rather than absolute (the fp32 routing).
+cudaError_t launch_path_dots(const Prob& pr, const Pyr& s, const void* q, const void* k, const float* pyr,
+                             int ref_root, float* out, cudaStream_t st);
 bool route_haar_supported(const Prob& pr);
 size_t haar_rows_bytes(const Prob& pr, const Pyr& s);  // one of the four fp16 row arrays
 size_t haar_meta_bytes(const Prob& pr, const Pyr& s);
 cudaError_t launch_route_haar(const Prob& pr, const Pyr& s, const void* q, const float* pyr, char* rows,
-                              float4* meta, int32_t* kept2, int32_t* trace, cudaStream_t st);
+                              float4* meta, const float* path, int32_t* kept2, int32_t* trace, cudaStream_t st);
 cudaError_t launch_leaf_simt(const Prob& pr, const Pyr& s, const void* q, const void* k, const int32_t* kept2,
                              int32_t* out_idx, float* out_score, cudaStream_t st);
 cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, char* ws, const void* q,

@@ -90,9 +90,27 @@ __device__ __forceinline__ bool elig32(int level, int j, int e_hi) {
   return (j << (level - 1)) <= e_hi && (((j + 1) << (level - 1)) - 1) >= 1;
 }
 
+// Dots (s2 units) of the two children of a query's path node at `level`
+// under prefix-consistent summaries: a complete left child and the path
+// child's prefix summary (see prefix_path.cu).  path: [nq, L, 2, G].
+template <int G>
+__device__ __forceinline__ void path_children(const float* __restrict__ path, int64_t qc, int L, int64_t qb,
+                                              int level, int g, float* a, float* bb) {
+  const float* pp = path + qc * L * 2 * G;
+  const float pc = pp[(level - 2) * 2 * G + g];
+  if ((qb >> (level - 2)) & 1) {
+    *a = pp[(level - 1) * 2 * G + G + g];
+    *bb = pc;
+  } else {
+    *a = pc;
+    *bb = pc;
+  }
+}
+
 template <int D, int G, int KM, int WARPS, int LQ>
 __global__ void __launch_bounds__(WARPS * 32) route_kernel(Prob pr, Pyr s, const void* __restrict__ q,
                                                            const float* __restrict__ pyr,
+                                                           const float* __restrict__ path,
                                                            int32_t* __restrict__ kept2,
                                                            int32_t* __restrict__ trace) {
   constexpr int NC = 2 * KM;
@@ -259,13 +277,15 @@ __global__ void __launch_bounds__(WARPS * 32) route_kernel(Prob pr, Pyr s, const
           n0 = node_count32(s.C, level - 1, c0v[sl], s.N);
           n1 = node_count32(s.C, level - 1, c0v[sl] + 1, s.N);
         }
+        const bool onpath = path && sm.cand[cur][i] == (int)(qb >> (level - 1));
         float sc = 0.0f;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float a = s0 >= 0 ? sm.y[s0][g] : 0.0f;
+          float a = s0 >= 0 ? sm.y[s0][g] : 0.0f;
           float bb = 0.0f;
           if (s1 >= 0) bb = sm.y[s1][g];
           else if (s1 == -2) bb = sibling_dot(sm.x[cur][i][g], a, n0, n1);
+          if (onpath) path_children<G>(path, qc, s.L, qb, level, g, &a, &bb);
           sc += (s0 >= 0 && s1 != -1) ? pair_score(pr.scorer, a, bb) : (s0 >= 0 ? a : bb);
         }
         if (sc != sc) sc = -INFINITY;  // NaN ranks last
@@ -309,10 +329,15 @@ __global__ void __launch_bounds__(WARPS * 32) route_kernel(Prob pr, Pyr s, const
             n0 = node_count32(s.C, level - 1, c0v[sl], s.N);
             n1 = node_count32(s.C, level - 1, c0v[sl] + 1, s.N);
           }
+          const bool onpath = path && ci == (int)(qb >> (level - 1));
           if (e0v[sl]) {
             sm.cand[nxt][cp] = c0v[sl];
 #pragma unroll
-            for (int g = 0; g < G; ++g) sm.x[nxt][cp][g] = sm.y[s0][g];
+            for (int g = 0; g < G; ++g) {
+              float a = sm.y[s0][g], bb = 0.0f;
+              if (onpath) path_children<G>(path, qc, s.L, qb, level, g, &a, &bb);
+              sm.x[nxt][cp][g] = a;
+            }
             sm.hasx[nxt][cp] = 1;
             ++cp;
           }
@@ -320,8 +345,10 @@ __global__ void __launch_bounds__(WARPS * 32) route_kernel(Prob pr, Pyr s, const
             sm.cand[nxt][cp] = c0v[sl] + 1;
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-              const float a = e0v[sl] ? sm.y[s0][g] : 0.0f;
-              sm.x[nxt][cp][g] = s1 >= 0 ? sm.y[s1][g] : sibling_dot(sm.x[cur][i][g], a, n0, n1);
+              float a = e0v[sl] ? sm.y[s0][g] : 0.0f;
+              float bb = s1 >= 0 ? sm.y[s1][g] : sibling_dot(sm.x[cur][i][g], a, n0, n1);
+              if (onpath) path_children<G>(path, qc, s.L, qb, level, g, &a, &bb);
+              sm.x[nxt][cp][g] = bb;
             }
             sm.hasx[nxt][cp] = 1;
           }
@@ -341,8 +368,8 @@ __global__ void __launch_bounds__(WARPS * 32) route_kernel(Prob pr, Pyr s, const
 }
 
 template <int D, int G, int KM, int WARPS>
-static cudaError_t launch_route_t(const Prob& pr, const Pyr& s, const void* q, const float* pyr, int32_t* kept2,
-                                  int32_t* trace, cudaStream_t st) {
+static cudaError_t launch_route_t(const Prob& pr, const Pyr& s, const void* q, const float* pyr, const float* path,
+                                  int32_t* kept2, int32_t* trace, cudaStream_t st) {
   constexpr int DQ = (64 / G) < D ? 64 / G : D;
   constexpr int LQ = (D / DQ) > 8 ? 16 : 8;  // lanes per query
   const size_t smem = sizeof(RouteQ<G, 2 * KM, 32 / LQ>) * (32 / LQ) * WARPS;
@@ -352,23 +379,23 @@ static cudaError_t launch_route_t(const Prob& pr, const Pyr& s, const void* q, c
   const int64_t nq = pr.B * pr.Hkv * pr.N;
   const int64_t grid = ceil_div64(nq, (32 / LQ) * WARPS);
   note_launch();
-  kern<<<(unsigned)grid, WARPS * 32, smem, st>>>(pr, s, q, pyr, kept2, trace);
+  kern<<<(unsigned)grid, WARPS * 32, smem, st>>>(pr, s, q, pyr, path, kept2, trace);
   return cudaGetLastError();
 }
 
 template <int D, int G>
-static cudaError_t launch_route_k(const Prob& pr, const Pyr& s, const void* q, const float* pyr, int32_t* kept2,
-                                  int32_t* trace, cudaStream_t st) {
-  if (pr.K <= 8) return launch_route_t<D, G, 8, 8>(pr, s, q, pyr, kept2, trace, st);
-  if (pr.K <= 16) return launch_route_t<D, G, 16, 8>(pr, s, q, pyr, kept2, trace, st);
-  return launch_route_t<D, G, 32, 4>(pr, s, q, pyr, kept2, trace, st);
+static cudaError_t launch_route_k(const Prob& pr, const Pyr& s, const void* q, const float* pyr, const float* path,
+                                  int32_t* kept2, int32_t* trace, cudaStream_t st) {
+  if (pr.K <= 8) return launch_route_t<D, G, 8, 8>(pr, s, q, pyr, path, kept2, trace, st);
+  if (pr.K <= 16) return launch_route_t<D, G, 16, 8>(pr, s, q, pyr, path, kept2, trace, st);
+  return launch_route_t<D, G, 32, 4>(pr, s, q, pyr, path, kept2, trace, st);
 }
 
-cudaError_t launch_route(const Prob& pr, const Pyr& s, const void* q, const float* pyr, int32_t* kept2,
-                         int32_t* trace, int32_t* /*status*/, cudaStream_t st) {
+cudaError_t launch_route(const Prob& pr, const Pyr& s, const void* q, const float* pyr, const float* path,
+                         int32_t* kept2, int32_t* trace, int32_t* /*status*/, cudaStream_t st) {
   if (pr.B * pr.Hkv * pr.N == 0) return cudaSuccess;
 #define PISA_ROUTE_CASE(DD, GG) \
-  if (pr.d == DD && pr.G == GG) return launch_route_k<DD, GG>(pr, s, q, pyr, kept2, trace, st);
+  if (pr.d == DD && pr.G == GG) return launch_route_k<DD, GG>(pr, s, q, pyr, path, kept2, trace, st);
   PISA_ROUTE_CASE(128, 1) PISA_ROUTE_CASE(128, 2) PISA_ROUTE_CASE(128, 4) PISA_ROUTE_CASE(128, 8)
   PISA_ROUTE_CASE(64, 1) PISA_ROUTE_CASE(64, 2) PISA_ROUTE_CASE(64, 4) PISA_ROUTE_CASE(64, 8)
 #undef PISA_ROUTE_CASE

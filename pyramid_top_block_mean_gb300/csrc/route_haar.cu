@@ -109,6 +109,18 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2_fast(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -204,16 +216,15 @@ struct HaarView {
   int64_t P2;
 };
 
-// Dots of the rows (hi, plus lo where lomask says so) of the candidates of
-// both queries of the warp, raw MMA results (row and query scales not yet
-// applied) into sm[u].y[slot].  Query u's candidates are
-// smw[u].cand[cur[u]][0, nw[u]); lomask[u]: bit i set when slot i of query u
-// needs its residual row.
-template <int D, int NC>
-__device__ __forceinline__ void haar_dots(HaarQPad<NC>* smw, const int (&cur)[2], const uint16_t* __restrict__ hi,
-                                          const uint16_t* __restrict__ lo, const int64_t (&pbase)[2], int64_t rowoff,
-                                          const int (&nw)[2], const uint64_t (&lomask)[2],
-                                          const uint32_t (&bq)[2][D / 64][4], int lane) {
+// Dots of fp16 rows of the candidates of both queries of the warp: query
+// u's candidates are smw[u].cand[cur[u]][0, nw[u]).  The raw MMA results (row
+// and query scales not yet applied) go to sm[u].y[slot]; with kAdd they are
+// added to it instead, and only the groups of eight slots whose bit is set in
+// gmask (one bit per group, both queries) are done: the residual pass.
+template <int D, int NC, bool kAdd>
+__device__ __forceinline__ void haar_pass(HaarQPad<NC>* smw, const int (&cur)[2], const uint16_t* __restrict__ rows,
+                                          const int64_t (&pbase)[2], int64_t rowoff, const int (&nw)[2],
+                                          uint32_t gmask, const uint32_t (&bq)[2][D / 64][4], int lane) {
   constexpr int NB = D / 64;
   const int grp = lane >> 2, tig = lane & 3;
   const int nmax = max(nw[0], nw[1]);
@@ -222,6 +233,7 @@ __device__ __forceinline__ void haar_dots(HaarQPad<NC>* smw, const int (&cur)[2]
 #pragma unroll
   for (int r0 = 0; r0 < NC; r0 += 8) {
     if (r0 >= nmax) break;
+    if (kAdd && !((gmask >> (r0 / 8)) & 1u)) continue;  // warp-uniform
     uint32_t ro[2][2];
 #pragma unroll
     for (int u = 0; u < 2; ++u)
@@ -230,47 +242,27 @@ __device__ __forceinline__ void haar_dots(HaarQPad<NC>* smw, const int (&cur)[2]
         const int w = r0 + 4 * rr + (grp >> 1);
         ro[u][rr] = (uint32_t)(w < nw[u] ? smw[u].cand[cur[u]][w] : 0) * (uint32_t)D;
       }
+    uint4 hv[2][2][NB];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb)
+          hv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(rows + pbase[u] + loff + ro[u][rr] + 64 * bb));
     float d[2][4];
 #pragma unroll
     for (int u = 0; u < 2; ++u)
 #pragma unroll
       for (int e = 0; e < 4; ++e) d[u][e] = 0.0f;
-    {
-      uint4 hv[2][2][NB];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+    for (int bb = 0; bb < NB; ++bb)
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-          for (int bb = 0; bb < NB; ++bb)
-            hv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(hi + pbase[u] + loff + ro[u][rr] + 64 * bb));
-#pragma unroll
-      for (int bb = 0; bb < NB; ++bb)
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint4 h0 = hv[u][0][bb], h1 = hv[u][1][bb];
-          mma_f16_16816(d[u], h0.x, h1.x, h0.y, h1.y, bq[u][bb][0], bq[u][bb][1]);
-          mma_f16_16816(d[u], h0.z, h1.z, h0.w, h1.w, bq[u][bb][2], bq[u][bb][3]);
-        }
-    }
-    if ((((lomask[0] | lomask[1]) >> r0) & 0xffull) != 0ull) {  // warp-uniform
-      uint4 lv[2][2][NB];
-#pragma unroll
-      for (int u = 0; u < 2; ++u)
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-          for (int bb = 0; bb < NB; ++bb)
-            lv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(lo + pbase[u] + loff + ro[u][rr] + 64 * bb));
-#pragma unroll
-      for (int bb = 0; bb < NB; ++bb)
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint4 l0 = lv[u][0][bb], l1 = lv[u][1][bb];
-          mma_f16_16816(d[u], l0.x, l1.x, l0.y, l1.y, bq[u][bb][0], bq[u][bb][1]);
-          mma_f16_16816(d[u], l0.z, l1.z, l0.w, l1.w, bq[u][bb][2], bq[u][bb][3]);
-        }
-    }
+      for (int u = 0; u < 2; ++u) {
+        const uint4 h0 = hv[u][0][bb], h1 = hv[u][1][bb];
+        mma_f16_16816(d[u], h0.x, h1.x, h0.y, h1.y, bq[u][bb][0], bq[u][bb][1]);
+        mma_f16_16816(d[u], h0.z, h1.z, h0.w, h1.w, bq[u][bb][2], bq[u][bb][3]);
+      }
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       // add the two halves: partner lane = lane ^ 6 (group ^ 1, t ^ 2)
@@ -278,17 +270,37 @@ __device__ __forceinline__ void haar_dots(HaarQPad<NC>* smw, const int (&cur)[2]
       const float x1 = __shfl_xor_sync(0xffffffffu, roleA ? d[u][3] : d[u][1], 6);
       const int w = r0 + (roleA ? 0 : 4) + (grp >> 1);
       if ((roleA || roleB) && w < nw[u]) {
-        const float2 v = roleA ? make_float2(d[u][0] + x0, d[u][1] + x1) : make_float2(d[u][2] + x0, d[u][3] + x1);
-        *reinterpret_cast<float2*>(reinterpret_cast<float*>(&smw[u].y[w]) + 2 * (tig & 1)) = v;
+        float2 v = roleA ? make_float2(d[u][0] + x0, d[u][1] + x1) : make_float2(d[u][2] + x0, d[u][3] + x1);
+        float2* dst = reinterpret_cast<float2*>(reinterpret_cast<float*>(&smw[u].y[w]) + 2 * (tig & 1));
+        if (kAdd) {
+          const float2 o = *dst;
+          v = make_float2(o.x + v.x, o.y + v.y);
+        }
+        *dst = v;
       }
     }
   }
 }
 
+// Groups of eight slots (bit i: slots [8i, 8i + 8) of either query) in which
+// some candidate's residual bound bnd exceeds kLoTau.
+template <int CPL>
+__device__ __forceinline__ uint32_t lo_groups(const float (&bnd)[CPL], int ncur, int ll) {
+  uint32_t gm = 0;
+#pragma unroll
+  for (int sl = 0; sl < CPL; ++sl) {
+    const unsigned b = __ballot_sync(0xffffffffu, sl * 16 + ll < ncur && bnd[sl] > kLoTau);
+    const unsigned m = (b | (b >> 16)) & 0xffffu;  // slots of either query
+    gm |= ((m & 0xffu) ? 1u : 0u) << (2 * sl);
+    gm |= ((m >> 8) ? 1u : 0u) << (2 * sl + 1);
+  }
+  return gm;
+}
+
 template <int D, int KM, int WARPS, bool kLse>
 __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
-    route_haar_kernel(Prob pr, Pyr s, const uint16_t* __restrict__ q, HaarView hv, int32_t* __restrict__ kept2,
-                      int32_t* __restrict__ trace) {
+    route_haar_kernel(Prob pr, Pyr s, const uint16_t* __restrict__ q, HaarView hv, const float* __restrict__ path,
+                      int32_t* __restrict__ kept2, int32_t* __restrict__ trace) {
   constexpr int G = 4;
   constexpr int NC = 2 * KM;
   constexpr int CPL = NC / 16;
@@ -415,19 +427,18 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     const int nwu[2] = {__shfl_sync(0xffffffffu, ncur, 0), __shfl_sync(0xffffffffu, ncur, 16)};
     const int curu[2] = {__shfl_sync(0xffffffffu, cur, 0), __shfl_sync(0xffffffffu, cur, 16)};
 
-    // start level: the candidates' own dots from their MU rows
+    // start level: the candidates' own dots from their MU rows (hi pass,
+    // then the residual pass for the groups whose rounding bound is too wide)
     const unsigned st_b = __ballot_sync(0xffffffffu, start);
     if (st_b) {
-      uint64_t lm[2] = {0ull, 0ull};
-#pragma unroll
-      for (int sl = 0; sl < CPL; ++sl) {
-        const bool need = start && sl * 16 + ll < ncur && mybf * mt[sl].y > kLoTau;
-        const unsigned b = __ballot_sync(0xffffffffu, need);
-        lm[0] |= (uint64_t)(b & 0xffffu) << (16 * sl);
-        lm[1] |= (uint64_t)(b >> 16) << (16 * sl);
-      }
       const int ns[2] = {(st_b & 1u) ? nwu[0] : 0, (st_b >> 16) ? nwu[1] : 0};
-      haar_dots<D, NC>(smw, curu, hv.mu_hi, hv.mu_lo, pbase, rowoff, ns, lm, bq, lane);
+      haar_pass<D, NC, false>(smw, curu, hv.mu_hi, pbase, rowoff, ns, 0u, bq, lane);
+      float bnd[CPL];
+#pragma unroll
+      for (int sl = 0; sl < CPL; ++sl) bnd[sl] = start ? mybf * mt[sl].y : 0.0f;
+      const uint32_t gm = lo_groups<CPL>(bnd, ncur, ll);
+      __syncwarp();
+      if (gm) haar_pass<D, NC, true>(smw, curu, hv.mu_lo, pbase, rowoff, ns, gm, bq, lane);
       __syncwarp();
 #pragma unroll
       for (int sl = 0; sl < CPL; ++sl) {
@@ -442,16 +453,14 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     }
 
     // every level: the candidates' DD rows give both children's dots
+    haar_pass<D, NC, false>(smw, curu, hv.dd_hi, pbase, rowoff, nwu, 0u, bq, lane);
     {
-      uint64_t lm[2] = {0ull, 0ull};
+      float bnd[CPL];
 #pragma unroll
-      for (int sl = 0; sl < CPL; ++sl) {
-        const bool need = sl * 16 + ll < ncur && mybf * mt[sl].w > kLoTau;
-        const unsigned b = __ballot_sync(0xffffffffu, need);
-        lm[0] |= (uint64_t)(b & 0xffffu) << (16 * sl);
-        lm[1] |= (uint64_t)(b >> 16) << (16 * sl);
-      }
-      haar_dots<D, NC>(smw, curu, hv.dd_hi, hv.dd_lo, pbase, rowoff, nwu, lm, bq, lane);
+      for (int sl = 0; sl < CPL; ++sl) bnd[sl] = mybf * mt[sl].w;
+      const uint32_t gm = lo_groups<CPL>(bnd, ncur, ll);
+      __syncwarp();
+      if (gm) haar_pass<D, NC, true>(smw, curu, hv.dd_lo, pbase, rowoff, nwu, gm, bq, lane);
     }
     __syncwarp();
 
@@ -485,13 +494,37 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
         ya[sl] = make_float4(fmaf(w0, yv[0], x.x), fmaf(w0, yv[1], x.y), fmaf(w0, yv[2], x.z), fmaf(w0, yv[3], x.w));
         yb[sl] = make_float4(fmaf(-w1, yv[0], x.x), fmaf(-w1, yv[1], x.y), fmaf(-w1, yv[2], x.z),
                              fmaf(-w1, yv[3], x.w));
+        if (path && cv[sl] == (int)(qb >> (level - 1))) {
+          // the query's path node: its children read the prefix-consistent
+          // summaries (the path child's prefix dot; a complete left sibling)
+          const float4* pp = reinterpret_cast<const float4*>(path + (int64_t)qc * s.L * 2 * G);
+          const float4 pc = __ldg(pp + (level - 2) * 2);
+          if ((qb >> (level - 2)) & 1) {
+            ya[sl] = __ldg(pp + (level - 1) * 2 + 1);
+            yb[sl] = pc;
+          } else {
+            ya[sl] = pc;
+            yb[sl] = pc;
+          }
+        }
         const bool both = e0v[sl] && e1v[sl];
         float scv = 0.0f;
         if constexpr (kLse) {
+          // sum over heads of log2(2^a + 2^b) = sum of maxima + log2 of the
+          // product of (1 + 2^(min - max)), each factor in (1, 2]
+          if (both) {
+            float pr4 = 1.0f;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float a = comp4(ya[sl], g), bb = comp4(yb[sl], g);
-            scv += both ? lse2_pair(a, bb) : (e0v[sl] ? a : bb);
+            for (int g = 0; g < G; ++g) {
+              const float a = comp4(ya[sl], g), bb = comp4(yb[sl], g);
+              const float mx = fmaxf(a, bb);
+              scv += mx;
+              pr4 *= 1.0f + ex2_fast(fminf(a, bb) - mx);
+            }
+            scv += lg2_fast(pr4);
+          } else {
+#pragma unroll
+            for (int g = 0; g < G; ++g) scv += e0v[sl] ? comp4(ya[sl], g) : comp4(yb[sl], g);
           }
         } else {
 #pragma unroll
@@ -501,8 +534,12 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
           }
         }
         if (scv == 0.0f) scv = 0.0f;     // -0 ranks like +0
-        if (scv != scv) scv = -INFINITY;  // NaN ranks last (keys stay <= 0xff800000)
-        key[sl] = orderable_key_h(scv);
+        if (scv != scv) scv = -INFINITY;  // NaN ranks last
+        // rank key: the orderable score with its low 6 bits replaced by the
+        // reversed slot, so keys are distinct and, among scores equal to 2^-17
+        // relative (ties far inside the 1e-3 tie margin), the lower slot --
+        // the lower node index -- ranks first
+        key[sl] = (orderable_key_h(scv) & ~63u) | (uint32_t)(63 - i);
       }
     }
     int rank[CPL];
@@ -514,12 +551,7 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
       for (int l = 0; l < 16; ++l) {
         const uint32_t kj = __shfl_sync(0xffffffffu, key[sj], l, 16);
 #pragma unroll
-        for (int sl = 0; sl < CPL; ++sl) {
-          // equal scores: the lower slot (the lower node index) ranks first.
-          // Keys of real scores are at most 0xff800000, so kj + 1 cannot wrap.
-          const uint32_t before = (sj < sl || (sj == sl && l < ll)) ? 1u : 0u;
-          rank[sl] += (kj + before > key[sl]) ? 1 : 0;
-        }
+        for (int sl = 0; sl < CPL; ++sl) rank[sl] += kj > key[sl] ? 1 : 0;
       }
     }
 
@@ -562,15 +594,16 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
 }
 
 template <int D, int KM, int WARPS, bool kLse>
-static cudaError_t launch_route_haar_t(const Prob& pr, const Pyr& s, const void* q, const HaarView& hv, int32_t* kept2,
-                                       int32_t* trace, cudaStream_t st) {
+static cudaError_t launch_route_haar_t(const Prob& pr, const Pyr& s, const void* q, const HaarView& hv,
+                                       const float* path, int32_t* kept2, int32_t* trace, cudaStream_t st) {
   const size_t smem = sizeof(HaarQPad<2 * KM>) * 2 * WARPS;
   auto kern = route_haar_kernel<D, KM, WARPS, kLse>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t nq = pr.B * pr.Hkv * pr.N;
   note_launch();
-  kern<<<(unsigned)ceil_div64(nq, 2 * WARPS), WARPS * 32, smem, st>>>(pr, s, (const uint16_t*)q, hv, kept2, trace);
+  kern<<<(unsigned)ceil_div64(nq, 2 * WARPS), WARPS * 32, smem, st>>>(pr, s, (const uint16_t*)q, hv, path, kept2,
+                                                                        trace);
   return cudaGetLastError();
 }
 
@@ -589,7 +622,7 @@ size_t haar_meta_bytes(const Prob& pr, const Pyr& s) {
 }
 
 cudaError_t launch_route_haar(const Prob& pr, const Pyr& s, const void* q, const float* pyr, char* rows,
-                              float4* meta, int32_t* kept2, int32_t* trace, cudaStream_t st) {
+                              float4* meta, const float* path, int32_t* kept2, int32_t* trace, cudaStream_t st) {
   const int64_t BH = pr.B * pr.Hkv;
   const int64_t P2 = s.L >= 2 ? s.P - s.size[0] : 0;
   const size_t arr = haar_rows_bytes(pr, s);
@@ -606,9 +639,9 @@ cudaError_t launch_route_haar(const Prob& pr, const Pyr& s, const void* q, const
   }
 #define PISA_RH_CASE(DD, LSE)                                                                            \
   if (pr.d == DD && (pr.scorer == PISA_SCORER_LSE) == LSE) {                                             \
-    if (pr.K <= 8) return launch_route_haar_t<DD, 8, 8, LSE>(pr, s, q, hv, kept2, trace, st);            \
-    if (pr.K <= 16) return launch_route_haar_t<DD, 16, 8, LSE>(pr, s, q, hv, kept2, trace, st);          \
-    return launch_route_haar_t<DD, 32, 4, LSE>(pr, s, q, hv, kept2, trace, st);                          \
+    if (pr.K <= 8) return launch_route_haar_t<DD, 8, 8, LSE>(pr, s, q, hv, path, kept2, trace, st);            \
+    if (pr.K <= 16) return launch_route_haar_t<DD, 16, 8, LSE>(pr, s, q, hv, path, kept2, trace, st);          \
+    return launch_route_haar_t<DD, 32, 4, LSE>(pr, s, q, hv, path, kept2, trace, st);                          \
   }
   PISA_RH_CASE(128, true) PISA_RH_CASE(64, true) PISA_RH_CASE(128, false) PISA_RH_CASE(64, false)
 #undef PISA_RH_CASE

@@ -29,6 +29,7 @@ STATUS_NAMES = {0: "PISA_OK", -1: "PISA_ERR_INVALID_ARG", -2: "PISA_ERR_UNSUPPOR
                 -6: "PISA_ERR_DEVICE"}
 BF16, FP32 = 0, 1
 SCORER_LSE, SCORER_MEAN, SCORER_MEAN_VAR = 0, 1, 2
+SUMMARIES_ALL, SUMMARIES_PREFIX = 0, 1
 MODE_PREFILL, MODE_DECODE, MODE_FLAT, MODE_ATTEND = 0, 1, 2, 3
 DEV_OK, DEV_BAD_SEQ_LEN, DEV_TIMEOUT, DEV_BAD_INDEX = 0, 1, 2, 3
 
@@ -37,7 +38,7 @@ EXPORTED = ["pisa_abi_version", "pisa_status_string", "pisa_pyramid_levels", "pi
             "pisa_prefill_route", "pisa_prefill_leaves", "pisa_select_decode", "pisa_select_flat",
             "pisa_read_device_status", "pisa_select_prefill_static", "pisa_kernel_launches",
             "pisa_attend_prefill", "pisa_build_pyramid_paged", "pisa_select_decode_paged", "pisa_attend_decode",
-            "pisa_read_static_status"]
+            "pisa_read_static_status", "pisa_test_inject_leaf_timeout"]
 
 
 class Params(ctypes.Structure):
@@ -45,7 +46,8 @@ class Params(ctypes.Structure):
                 ("B", ctypes.c_int64), ("N", ctypes.c_int64),
                 ("H_q", ctypes.c_int32), ("H_kv", ctypes.c_int32), ("d", ctypes.c_int32),
                 ("C", ctypes.c_int32), ("g", ctypes.c_int32), ("K", ctypes.c_int32),
-                ("qtile", ctypes.c_int32), ("scale", ctypes.c_float), ("scorer", ctypes.c_int32)]
+                ("qtile", ctypes.c_int32), ("scale", ctypes.c_float), ("scorer", ctypes.c_int32),
+                ("summaries", ctypes.c_int32)]
 
 
 _P = ctypes.POINTER(Params)
@@ -89,6 +91,8 @@ _lib.pisa_select_prefill_static.argtypes = [_P, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.pisa_select_prefill_static.restype = ctypes.c_int
 _lib.pisa_read_static_status.argtypes = [ctypes.POINTER(ctypes.c_int32), _vp]
 _lib.pisa_read_static_status.restype = ctypes.c_int
+_lib.pisa_test_inject_leaf_timeout.argtypes = [ctypes.c_uint64, ctypes.c_int32]
+_lib.pisa_test_inject_leaf_timeout.restype = None
 
 
 class PisaError(RuntimeError):
@@ -115,15 +119,17 @@ def kernel_launches() -> int:
 
 
 def make_params(B: int, N: int, H_q: int, H_kv: int, d: int, C: int = 64, g: int = 2, K: int = 8,
-                qtile: int = 4, dtype: str = "bf16", scale: float = 0.0, scorer: int = 0) -> Params:
-    """scorer: SCORER_LSE (PISA), SCORER_MEAN (PISA-1) or SCORER_MEAN_VAR (PISA-2)."""
+                qtile: int = 4, dtype: str = "bf16", scale: float = 0.0, scorer: int = 0,
+                summaries: int = 0) -> Params:
+    """scorer: SCORER_LSE (PISA), SCORER_MEAN (PISA-1) or SCORER_MEAN_VAR (PISA-2);
+    summaries: SUMMARIES_ALL or SUMMARIES_PREFIX (prefix-consistent prefill)."""
     return Params(ctypes.sizeof(Params), BF16 if dtype == "bf16" else FP32, B, N, H_q, H_kv, d, C, g, K,
-                  qtile, scale, scorer)
+                  qtile, scale, scorer, summaries)
 
 
-def params_from_shape(s, N: Optional[int] = None, scorer: int = 0) -> Params:
+def params_from_shape(s, N: Optional[int] = None, scorer: int = 0, summaries: int = 0) -> Params:
     return make_params(s.B, s.N if N is None else N, s.Hq, s.Hkv, s.d, s.C, s.g, s.K, s.qtile, s.dtype,
-                       scorer=scorer)
+                       scorer=scorer, summaries=summaries)
 
 
 def pyramid_levels(p: Params) -> int:

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(pisa):
 
 
 def test_abi_version_and_status_strings(pisa):
-    assert pisa.abi_version() == 2
+    assert pisa.abi_version() == 3
     for code in range(-6, 1):
         assert pisa.status_string(code).startswith(pisa.STATUS_NAMES[code])
 
@@ -54,6 +54,7 @@ def test_size_queries_match_the_pyramid_shape(pisa):
     ("scale", -1.0, -1), ("d", 96, -2), ("C", 32, -2), ("g", 3, -2), ("K", 33, -2), ("dtype", 7, -2),
     ("H_q", 48, -2),  # G = 12
     ("N", (1 << 26) + 1, -2), ("struct_size", 8, -1), ("scorer", 3, -1), ("scorer", -1, -1),
+    ("summaries", 2, -1), ("summaries", -1, -1),
 ])
 def test_bad_params_are_rejected(pisa, field, value, code):
     p = pisa.make_params(1, 4096, 16, 4, 128, K=8)
@@ -91,6 +92,24 @@ def test_empty_problems_are_no_ops(pisa):
         p = pisa.make_params(B, N, 16, 4, 128, K=8)
         assert L.pisa_select_prefill(ctypes.byref(p), None, None, None, None, 0, None, None, None, None) == 0
         assert L.pisa_build_pyramid(ctypes.byref(p), None, None, None, None) == 0
+
+
+def test_params_without_the_summaries_field_are_rejected(pisa):
+    # a caller built against the second ABI passes the shorter struct
+    p = pisa.make_params(1, 4096, 16, 4, 128, K=8)
+    p.struct_size = pisa.Params.summaries.offset
+    assert pisa.workspace_bytes(p, 0) == 0
+    base = pisa.workspace_bytes(pisa.make_params(1, 4096, 16, 4, 128, K=8), 0)
+    pre = pisa.workspace_bytes(pisa.make_params(1, 4096, 16, 4, 128, K=8, summaries=pisa.SUMMARIES_PREFIX), 0)
+    assert 0 < base < pre  # the prefix-consistent walk keeps its path dots in the workspace
+
+
+def test_prefix_route_stage_alone_is_refused_before_launch(pisa):
+    # prefix-consistent walks read each query's own raw keys, which only
+    # pisa_select_prefill receives
+    p = pisa.make_params(1, 4096, 16, 4, 128, K=8, summaries=pisa.SUMMARIES_PREFIX)
+    a = ctypes.c_void_p(0x10000)
+    assert pisa.lib().pisa_prefill_route(ctypes.byref(p), a, a, a, 1 << 40, None, None) == -2
 
 
 def test_params_without_the_scorer_field_are_rejected(pisa):

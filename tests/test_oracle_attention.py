@@ -174,3 +174,49 @@ def test_selected_queries_match_full_run():
     G = Hq // Hkv
     rows = np.stack([q.numpy()[b, h * G:(h + 1) * G, t] for (b, h, t) in sel])
     np.testing.assert_array_equal(O.attend(rows, k, v, idx, sel, qrows=True), part)
+
+
+# ------------------------------------------------------- attention mass
+def _mass_case(seed=3):
+    s = W.Shape(B=1, N=64 * 12 + 9, Hq=4, Hkv=2, d=16, K=3, dtype="fp32")
+    q, k = W.iid(s, seed)
+    return s, q.double().numpy(), k.double().numpy()
+
+
+def test_attention_mass_of_every_causal_block_is_one():
+    s, q, k = _mass_case()
+    sel = [(0, h, t) for h in range(s.Hkv) for t in (0, 63, 64, 300, s.N - 1)]
+    idx = np.array([list(range(t // s.C + 1)) + [-1] * (20 - t // s.C - 1) for (_, _, t) in sel])
+    r = oracle.attention_mass(q, k, idx, sel, s.C)
+    np.testing.assert_allclose(r, 1.0, rtol=0, atol=1e-12)
+    none = oracle.attention_mass(q, k, np.full((len(sel), 4), -1), sel, s.C)
+    assert (none == 0.0).all()
+
+
+def test_attention_mass_is_additive_over_disjoint_blocks_and_ignores_repeats():
+    s, q, k = _mass_case(4)
+    t = s.N - 1
+    qb = t // s.C
+    sel = [(0, 1, t)]
+    parts = [oracle.attention_mass(q, k, np.array([[j]]), sel, s.C)[0] for j in range(qb + 1)]
+    assert abs(sum(parts) - 1.0) < 1e-12
+    both = oracle.attention_mass(q, k, np.array([[2, 5, 5, 2, qb + 3]]), sel, s.C)[0]
+    assert abs(both - (parts[2] + parts[5])) < 1e-12
+
+
+def test_attention_mass_of_one_block_is_the_exp_of_the_oracle_leaf_lse_gap():
+    """G = 1: the mass of block j is exp(LSE(block j) - LSE(all keys <= t)),
+    with LSE(block j) from the C oracle's leaf score (an independent
+    implementation of the leaf log-sum-exp)."""
+    s = W.Shape(B=1, N=64 * 10, Hq=1, Hkv=1, d=32, K=2, dtype="fp32")
+    qt, kt = W.iid(s, 9)
+    q, k = qt.double().numpy(), kt.double().numpy()
+    o = oracle.Oracle.from_shape(s)
+    pyr = o.pyramid(k)
+    t = s.N - 1
+    blocks = list(range(t // s.C + 1))
+    lse_blocks = o.score_nodes(q, k, pyr, 0, 0, t, 1, blocks)
+    total = np.logaddexp.reduce(lse_blocks)
+    for j in (0, 3, 7, 9):
+        m = oracle.attention_mass(q, k, np.array([[j]]), [(0, 0, t)], s.C)[0]
+        assert abs(m - np.exp(lse_blocks[j] - total)) < 1e-12

@@ -1,4 +1,7 @@
-"""Selection quality on synthetic workloads: Recall@K of the GPU selectors
+"""Selection quality on synthetic workloads: Recall@K and the attention-mass
+ratio (the share of the full causal softmax mass that falls on the selected
+blocks, forced ones included, averaged over the GQA group's heads;
+oracle.attention_mass) of the GPU selectors
 (PISA and the flat block-mean comparator) against the exhaustive ranking
 that PISA approximates, i.e. every eligible leaf block scored by the sum
 over the GQA group of the LogSumExp of its raw keys (agihunt.info summary,
@@ -42,11 +45,17 @@ def selections(pisa, s, q, k):
 
 
 def recall(pisa, s, q, k, positions):
+    """Mean Recall@K and mean attention-mass ratio per selector."""
     sel = selections(pisa, s, q, k)
     o = oracle.Oracle.from_shape(s)
     qn, kn = q.double().numpy(), k.double().numpy()
     pyr = o.pyramid(kn)
     rec = {"prefill": [], "flat": []}
+    mass = {}
+    keys = [(b, h, t) for b in range(s.B) for h in range(s.Hkv) for t in positions if t // s.C - 2 > s.K]
+    for mode in rec:
+        rows = sel[mode][[(b * s.Hkv + h) * s.N + t for (b, h, t) in keys]]
+        mass[mode] = float(np.mean(oracle.attention_mass(qn, kn, rows, keys, s.C)))
     for b in range(s.B):
         for h in range(s.Hkv):
             for t in positions:
@@ -61,28 +70,32 @@ def recall(pisa, s, q, k, positions):
                 for mode in rec:
                     got = {int(j) for j in sel[mode][row] if j >= 0 and j not in F}
                     rec[mode].append(len(got & best) / s.K)
-    return {m: float(np.mean(v)) for m, v in rec.items()}
+    out = {m: float(np.mean(v)) for m, v in rec.items()}
+    out.update({f"mass_{m}": v for m, v in mass.items()})
+    return out
 
 
 def test_recall_planted_pretrain(pisa):
     s = W.PRETRAIN
     q, k = W.planted(s, 1)
     r = recall(pisa, s, q, k, range(s.N - 640, s.N, 5))
-    print("planted pretrain Recall@8:", r)
+    print("planted pretrain Recall@8 and attention-mass ratio:", r)
     assert r["prefill"] >= 0.3 and r["prefill"] >= r["flat"]
+    assert 0.0 < r["mass_flat"] <= 1.0 and 0.0 < r["mass_prefill"] <= 1.0
 
 
 def test_recall_needles_cpt(pisa):
     s = W.CPT
     q, k, _ = W.needles(s, 2)
     r = recall(pisa, s, q, k, range(s.N - 256, s.N, 8))
-    print("needle CPT Recall@32:", r)
+    print("needle CPT Recall@32 and attention-mass ratio:", r)
     assert r["prefill"] >= 0.4 and r["prefill"] >= r["flat"]
+    assert 0.0 < r["mass_flat"] <= 1.0 and 0.0 < r["mass_prefill"] <= 1.0
 
 
 def test_recall_iid_16k(pisa):
     s = W.Shape(B=1, N=16384, Hq=16, Hkv=4, d=128, K=8)
     q, k = W.iid(s, 9)
     r = recall(pisa, s, q, k, range(s.N - 512, s.N, 16))
-    print("iid 16K Recall@8:", r)
+    print("iid 16K Recall@8 and attention-mass ratio:", r)
     assert 0.0 <= r["prefill"] <= 1.0 and 0.0 <= r["flat"] <= 1.0
