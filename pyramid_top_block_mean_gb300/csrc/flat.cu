@@ -29,6 +29,8 @@ constexpr int kFCap = kMaxK + 32;  // Top-K buffer per query: K kept + one 32-co
 constexpr int kFlatThreads = 192;
 constexpr uint32_t kFTmemCols = 256;
 constexpr uint64_t kFWaitNs = 4000000000ull;
+// log2(G) for the group sizes 1, 2, 4, 8
+__device__ constexpr float kFLog2G[9] = {0.0f, 0.0f, 1.0f, 0.0f, 2.0f, 0.0f, 0.0f, 0.0f, 3.0f};
 
 template <int D, int G>
 struct FlatSmem {
@@ -229,7 +231,9 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       const int64_t qb = t < pr.N ? t / pr.C : 0;  // valid columns: [0, qb)
       float m = -INFINITY, ssum = 0.0f, lse = 0.0f;
       int cnt = 0;              // entries in this query's buffer (g == 0 lane)
-      float theta = -INFINITY;  // K-th best so far, once cnt has reached K
+      float theta = -INFINITY;  // K-th best so far, once cnt has reached K (g == 0 lane)
+      float lthr = -INFINITY;   // log2(theta / G) less a margin: a column whose every head has
+                                // log2 p at or below it cannot enter the Top-K (all G lanes)
       for (int pass = 0; pass < 2 && ok; ++pass) {
         if (pass == 1) lse = m + ptx::lg2(ssum);
         for (int j = 0; j < nj; ++j) {
@@ -240,66 +244,106 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
           const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + acc * kFCols;
           const int64_t col0 = (int64_t)j * kFCols;
           if (pass == 0) {
-            float tm = -INFINITY;
-            float x[kFCols];
-#pragma unroll
+            // online log2-sum-exp2 per row over the complete past blocks
+            // [0, qb), 32 columns at a time
+#pragma unroll 1
             for (int c4 = 0; c4 < kFCols / 32; ++c4) {
               uint32_t v[32];
               ptx::tmem_ld32(taddr + c4 * 32, v);
               ptx::tmem_ld_wait();
+              const int64_t cb = col0 + c4 * 32;
+              if (cb + 32 <= qb) {
+                // every column valid: shift by the running maximum or the
+                // largest of 8 entries, packed exponent arguments and sums;
+                // an overflowed or NaN chunk is redone with its exact maximum
+                const float s8 = fmaxf(fmaxf(fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                                             fmaxf(__uint_as_float(v[2]), __uint_as_float(v[3]))),
+                                       fmaxf(fmaxf(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                                             fmaxf(__uint_as_float(v[6]), __uint_as_float(v[7]))));
+                float mn = fmaxf(m, s8 * sc);
+                const float2 sc2 = make_float2(sc, sc);
+                float2 nm2 = make_float2(-mn, -mn);
+                float2 a2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const int col = c4 * 32 + c;
-                x[col] = (col0 + col < qb) ? __uint_as_float(v[c]) * sc : -INFINITY;
-                tm = fmaxf(tm, x[col]);
+                for (int c = 0; c < 16; ++c) {
+                  const float2 e = __ffma2_rn(make_float2(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1])),
+                                              sc2, nm2);
+                  a2[c & 1] = __fadd2_rn(a2[c & 1], make_float2(ptx::ex2(e.x), ptx::ex2(e.y)));
+                }
+                const float2 s2 = __fadd2_rn(a2[0], a2[1]);
+                float cs = s2.x + s2.y;
+                if (!(cs <= 3.0e38f)) {
+                  float mx = m;
+#pragma unroll
+                  for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(v[c]) * sc);
+                  mn = mx;
+                  cs = 0.0f;
+#pragma unroll
+                  for (int c = 0; c < 32; ++c) cs += ptx::ex2(__uint_as_float(v[c]) * sc - mn);
+                }
+                ssum = (m > -INFINITY ? ssum * ptx::ex2(m - mn) : 0.0f) + cs;
+                m = mn;
+              } else if (cb < qb) {
+                float x[32];
+                float tm = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                  x[c] = (cb + c < qb) ? __uint_as_float(v[c]) * sc : -INFINITY;
+                  tm = fmaxf(tm, x[c]);
+                }
+                if (tm > -INFINITY) {
+                  const float mn = fmaxf(m, tm);
+                  float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                  for (int c = 0; c < 32; ++c) s4[c & 3] += ptx::ex2(x[c] - mn);
+                  ssum = ssum * ptx::ex2(m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+                  m = mn;
+                }
               }
             }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[acc]));
-            if (tm > -INFINITY) {
-              const float mn = fmaxf(m, tm);
-              float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-              for (int c = 0; c < kFCols; ++c) s4[c & 3] += ptx::ex2(x[c] - mn);
-              ssum = ssum * ptx::ex2(m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
-              m = mn;
-            }
           } else {
 #pragma unroll 1
             for (int c4 = 0; c4 < kFCols / 32; ++c4) {
               uint32_t v[32];
               ptx::tmem_ld32(taddr + c4 * 32, v);
               ptx::tmem_ld_wait();
-              float pv[32];
-              float bmax = -INFINITY;
+              const int64_t cb = col0 + c4 * 32;
+              // columns of E = [1, qb - 2] only; a column is looked at (its G
+              // probabilities summed) when some head's log2 p beats lthr
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
-                const int64_t col = col0 + c4 * 32 + c;
-                float p = (col < qb) ? ptx::ex2(__uint_as_float(v[c]) * sc - lse) : 0.0f;
+                const int64_t col = cb + c;
+                const bool inE = col >= 1 && col <= qb - 2;
+                const float y = __uint_as_float(v[c]) * sc - lse;
+                const unsigned bal = __ballot_sync(0xffffffffu, inE && y > lthr);
+                if (bal) {  // warp-uniform
+                  float p = inE ? ptx::ex2(y) : 0.0f;
 #pragma unroll
-                for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-                pv[c] = (col >= 1 && col <= qb - 2) ? p : -INFINITY;  // Top-K runs over E only
-                bmax = fmaxf(bmax, pv[c]);
-              }
-              // the group's first lane appends every column above the current
-              // K-th best to its buffer and compacts it back to K when a batch
-              // added anything (rare once the K-th best has settled)
-              if (g == 0 && bmax > theta) {
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                  if (pv[c] > theta) {
-                    ts[cnt] = pv[c];
-                    tix[cnt] = (int32_t)(col0 + c4 * 32 + c);
-                    ++cnt;
+                  for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                  const unsigned mine = (bal >> (lane & ~(G - 1))) & ((1u << G) - 1u);
+                  if (g == 0 && mine && p > theta) {
+                    ts[cnt] = p;
+                    tix[cnt] = (int32_t)col;
+                    if (++cnt == kFCap) {
+                      flat_select_topk(ts, tix, cnt, K);
+                      cnt = K;
+                      theta = ts[K - 1];
+                    }
                   }
                 }
-                if (cnt > K) {
-                  flat_select_topk(ts, tix, cnt, K);
-                  cnt = K;
-                  theta = ts[K - 1];
-                }
               }
+              // the group's first lane compacts its buffer back to K and
+              // tightens the threshold; the G lanes of the query share lthr
+              if (g == 0 && cnt > K) {
+                flat_select_topk(ts, tix, cnt, K);
+                cnt = K;
+                theta = ts[K - 1];
+              }
+              if (g == 0 && cnt == K) lthr = ptx::lg2(theta) - kFLog2G[G] - 1.0e-3f;
+              lthr = __shfl_sync(0xffffffffu, lthr, lane & ~(G - 1));
             }
             ptx::tc_fence_before();
             __syncwarp();
