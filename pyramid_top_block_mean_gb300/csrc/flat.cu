@@ -13,7 +13,7 @@
 // bf16 once and streamed as 128-leaf TMA tiles, tcgen05.mma accumulates
 // 128 x 128 fp32 scores in TMEM.  Pass 1 keeps a per-row online
 // log2-sum-exp2; pass 2 recomputes the scores, forms the probabilities, sums
-// the G head rows with shuffles and keeps a streaming Top-K per query.
+// the G head rows with shuffles and keeps a sorted Top-K list per query.
 #include <algorithm>
 
 #include "pisa_common.cuh"
@@ -25,12 +25,10 @@ namespace pisa {
 constexpr int kFRows = 128;
 constexpr int kFCols = 128;
 constexpr int kFStagesB = 2;
-constexpr int kFCap = kMaxK + 32;  // Top-K buffer per query: K kept + one 32-column batch
+constexpr int kFCap = kMaxK;  // Top-K list per query
 constexpr int kFlatThreads = 192;
 constexpr uint32_t kFTmemCols = 256;
 constexpr uint64_t kFWaitNs = 4000000000ull;
-// log2(G) for the group sizes 1, 2, 4, 8
-__device__ constexpr float kFLog2G[9] = {0.0f, 0.0f, 1.0f, 0.0f, 2.0f, 0.0f, 0.0f, 0.0f, 3.0f};
 
 template <int D, int G>
 struct FlatSmem {
@@ -50,18 +48,6 @@ __global__ void means_to_bf16_kernel(int64_t nbh, int64_t P, int64_t nb, int d, 
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t c = i % d, row = i / d, leaf = row % nb, bh = row / nb;
     mu[i] = __float2bfloat16_rn(pyr[(bh * P + leaf) * d + c]);
-  }
-}
-
-// Moves the best K of the n buffered (score, block) entries to the front,
-// best first (higher score, then lower block index).
-__device__ __noinline__ void flat_select_topk(float* ts, int32_t* tix, int n, int K) {
-  for (int r = 0; r < K; ++r) {
-    int best = r;
-    for (int u = r + 1; u < n; ++u)
-      if (ts[u] > ts[best] || (ts[u] == ts[best] && tix[u] < tix[best])) best = u;
-    const float sv = ts[r]; ts[r] = ts[best]; ts[best] = sv;
-    const int32_t iv = tix[r]; tix[r] = tix[best]; tix[best] = iv;
   }
 }
 
@@ -231,9 +217,7 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       const int64_t qb = t < pr.N ? t / pr.C : 0;  // valid columns: [0, qb)
       float m = -INFINITY, ssum = 0.0f, lse = 0.0f;
       int cnt = 0;              // entries in this query's buffer (g == 0 lane)
-      float theta = -INFINITY;  // K-th best so far, once cnt has reached K (g == 0 lane)
-      float lthr = -INFINITY;   // log2(theta / G) less a margin: a column whose every head has
-                                // log2 p at or below it cannot enter the Top-K (all G lanes)
+      float theta = -INFINITY;  // K-th best so far, once cnt has reached K
       for (int pass = 0; pass < 2 && ok; ++pass) {
         if (pass == 1) lse = m + ptx::lg2(ssum);
         for (int j = 0; j < nj; ++j) {
@@ -244,106 +228,71 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
           const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + acc * kFCols;
           const int64_t col0 = (int64_t)j * kFCols;
           if (pass == 0) {
-            // online log2-sum-exp2 per row over the complete past blocks
-            // [0, qb), 32 columns at a time
-#pragma unroll 1
+            float tm = -INFINITY;
+            float x[kFCols];
+#pragma unroll
             for (int c4 = 0; c4 < kFCols / 32; ++c4) {
               uint32_t v[32];
               ptx::tmem_ld32(taddr + c4 * 32, v);
               ptx::tmem_ld_wait();
-              const int64_t cb = col0 + c4 * 32;
-              if (cb + 32 <= qb) {
-                // every column valid: shift by the running maximum or the
-                // largest of 8 entries, packed exponent arguments and sums;
-                // an overflowed or NaN chunk is redone with its exact maximum
-                const float s8 = fmaxf(fmaxf(fmaxf(__uint_as_float(v[0]), __uint_as_float(v[1])),
-                                             fmaxf(__uint_as_float(v[2]), __uint_as_float(v[3]))),
-                                       fmaxf(fmaxf(__uint_as_float(v[4]), __uint_as_float(v[5])),
-                                             fmaxf(__uint_as_float(v[6]), __uint_as_float(v[7]))));
-                float mn = fmaxf(m, s8 * sc);
-                const float2 sc2 = make_float2(sc, sc);
-                float2 nm2 = make_float2(-mn, -mn);
-                float2 a2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                  const float2 e = __ffma2_rn(make_float2(__uint_as_float(v[2 * c]), __uint_as_float(v[2 * c + 1])),
-                                              sc2, nm2);
-                  a2[c & 1] = __fadd2_rn(a2[c & 1], make_float2(ptx::ex2(e.x), ptx::ex2(e.y)));
-                }
-                const float2 s2 = __fadd2_rn(a2[0], a2[1]);
-                float cs = s2.x + s2.y;
-                if (!(cs <= 3.0e38f)) {
-                  float mx = m;
-#pragma unroll
-                  for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(v[c]) * sc);
-                  mn = mx;
-                  cs = 0.0f;
-#pragma unroll
-                  for (int c = 0; c < 32; ++c) cs += ptx::ex2(__uint_as_float(v[c]) * sc - mn);
-                }
-                ssum = (m > -INFINITY ? ssum * ptx::ex2(m - mn) : 0.0f) + cs;
-                m = mn;
-              } else if (cb < qb) {
-                float x[32];
-                float tm = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                  x[c] = (cb + c < qb) ? __uint_as_float(v[c]) * sc : -INFINITY;
-                  tm = fmaxf(tm, x[c]);
-                }
-                if (tm > -INFINITY) {
-                  const float mn = fmaxf(m, tm);
-                  float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                  for (int c = 0; c < 32; ++c) s4[c & 3] += ptx::ex2(x[c] - mn);
-                  ssum = ssum * ptx::ex2(m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
-                  m = mn;
-                }
+              for (int c = 0; c < 32; ++c) {
+                const int col = c4 * 32 + c;
+                x[col] = (col0 + col < qb) ? __uint_as_float(v[c]) * sc : -INFINITY;
+                tm = fmaxf(tm, x[col]);
               }
             }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[acc]));
+            if (tm > -INFINITY) {
+              const float mn = fmaxf(m, tm);
+              float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+              for (int c = 0; c < kFCols; ++c) s4[c & 3] += ptx::ex2(x[c] - mn);
+              ssum = ssum * ptx::ex2(m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
+              m = mn;
+            }
           } else {
 #pragma unroll 1
             for (int c4 = 0; c4 < kFCols / 32; ++c4) {
               uint32_t v[32];
               ptx::tmem_ld32(taddr + c4 * 32, v);
               ptx::tmem_ld_wait();
-              const int64_t cb = col0 + c4 * 32;
-              // columns of E = [1, qb - 2] only; a column is looked at (its G
-              // probabilities summed) when some head's log2 p beats lthr
+              float pv[32];
+              float bmax = -INFINITY;
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
-                const int64_t col = cb + c;
-                const bool inE = col >= 1 && col <= qb - 2;
-                const float y = __uint_as_float(v[c]) * sc - lse;
-                const unsigned bal = __ballot_sync(0xffffffffu, inE && y > lthr);
-                if (bal) {  // warp-uniform
-                  float p = inE ? ptx::ex2(y) : 0.0f;
+                const int64_t col = col0 + c4 * 32 + c;
+                float p = (col < qb) ? ptx::ex2(__uint_as_float(v[c]) * sc - lse) : 0.0f;
 #pragma unroll
-                  for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-                  const unsigned mine = (bal >> (lane & ~(G - 1))) & ((1u << G) - 1u);
-                  if (g == 0 && mine && p > theta) {
-                    ts[cnt] = p;
-                    tix[cnt] = (int32_t)col;
-                    if (++cnt == kFCap) {
-                      flat_select_topk(ts, tix, cnt, K);
-                      cnt = K;
-                      theta = ts[K - 1];
+                for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                pv[c] = (col >= 1 && col <= qb - 2) ? p : -INFINITY;  // Top-K runs over E only
+                bmax = fmaxf(bmax, pv[c]);
+              }
+              // the group's first lane keeps its query's best K sorted (higher
+              // score first; a later column never passes an equal score, so
+              // ties keep the lower block index) and inserts every column
+              // above the current K-th best: O(K) per insertion, and after the
+              // first columns insertions are rare
+              if (g == 0 && bmax > theta) {
+#pragma unroll 1
+                for (int c = 0; c < 32; ++c) {
+                  const float pc = pv[c];
+                  if (pc > theta) {
+                    int pos = cnt < K ? cnt : K - 1;
+                    while (pos > 0 && ts[pos - 1] < pc) {
+                      ts[pos] = ts[pos - 1];
+                      tix[pos] = tix[pos - 1];
+                      --pos;
                     }
+                    ts[pos] = pc;
+                    tix[pos] = (int32_t)(col0 + c4 * 32 + c);
+                    if (cnt < K) ++cnt;
+                    if (cnt == K) theta = ts[K - 1];
                   }
                 }
               }
-              // the group's first lane compacts its buffer back to K and
-              // tightens the threshold; the G lanes of the query share lthr
-              if (g == 0 && cnt > K) {
-                flat_select_topk(ts, tix, cnt, K);
-                cnt = K;
-                theta = ts[K - 1];
-              }
-              if (g == 0 && cnt == K) lthr = ptx::lg2(theta) - kFLog2G[G] - 1.0e-3f;
-              lthr = __shfl_sync(0xffffffffu, lthr, lane & ~(G - 1));
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -355,7 +304,6 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       if (!ok) break;
       // output for this query: Top-K (ascending) plus F
       if (g == 0 && t < pr.N) {
-        if (cnt > K) { flat_select_topk(ts, tix, cnt, K); cnt = K; }
         // insertion sort of the kept entries by block index
         for (int u = 1; u < cnt; ++u) {
           const float sv = ts[u];

@@ -553,39 +553,17 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
       }
       float lse;
       if (pr.scorer == PISA_SCORER_LSE) {
-        // log2-sum-exp2 shifted by m0, the largest of 8 of the 64 scaled dots:
-        // m0 <= the maximum, so the largest term is >= 1 and no term that
-        // matters underflows.  Exponent arguments and sums use packed fp32x2
-        // instructions.  A sum that overflowed (a dot 128 above m0) or is NaN
-        // is recomputed with the exact maximum.
-        const float m0 = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
-                               fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7]))) * sc;
-        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m0, -m0);
-        float2 acc[4];
+        float mm[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) acc[u] = make_float2(0.0f, 0.0f);
+        for (int u = 0; u < 8; ++u) mm[u] = x[u];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float2 a = __ffma2_rn(make_float2(x[2 * j], x[2 * j + 1]), sc2, nm2);
-          acc[j & 3] = __fadd2_rn(acc[j & 3], make_float2(ptx::ex2(a.x), ptx::ex2(a.y)));
-        }
-        const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
-        const float sum = (s01.x + s01.y) + (s23.x + s23.y);
-        if (sum <= 3.0e38f) {
-          lse = m0 + ptx::lg2(sum);
-        } else {
-          float mm[8];
+        for (int j = 8; j < 64; ++j) mm[j & 7] = fmaxf(mm[j & 7], x[j]);
+        const float m = fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
+                              fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7]))) * sc;
+        float ss[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-          for (int u = 0; u < 8; ++u) mm[u] = x[u];
-#pragma unroll
-          for (int j = 8; j < 64; ++j) mm[j & 7] = fmaxf(mm[j & 7], x[j]);
-          const float m = fmaxf(fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])),
-                                fmaxf(fmaxf(mm[4], mm[5]), fmaxf(mm[6], mm[7]))) * sc;
-          float ss[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-          for (int j = 0; j < 64; ++j) ss[j & 3] += ptx::ex2(fmaf(x[j], sc, -m));
-          lse = m + ptx::lg2((ss[0] + ss[1]) + (ss[2] + ss[3]));
-        }
+        for (int j = 0; j < 64; ++j) ss[j & 3] += ptx::ex2(fmaf(x[j], sc, -m));
+        lse = m + ptx::lg2((ss[0] + ss[1]) + (ss[2] + ss[3]));
       } else {
         // PISA-1 / PISA-2: mean and centred second moment of the 64 dots
         float s1[4] = {0.0f, 0.0f, 0.0f, 0.0f};

@@ -297,8 +297,11 @@ __device__ __forceinline__ uint32_t lo_groups(const float (&bnd)[CPL], int ncur,
   return gm;
 }
 
+// Occupancy: K <= 8 runs three 8-warp CTAs per SM (a register budget of 80;
+// the walk is latency- and issue-bound, and 24 resident warps beat 16 warps
+// with more registers); larger K keep 16 warps per SM.
 template <int D, int KM, int WARPS, bool kLse>
-__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
+__global__ void __launch_bounds__(WARPS * 32, (KM <= 8 ? 24 : 16) / WARPS)
     route_haar_kernel(Prob pr, Pyr s, const uint16_t* __restrict__ q, HaarView hv, const float* __restrict__ path,
                       int32_t* __restrict__ kept2, int32_t* __restrict__ trace) {
   constexpr int G = 4;
