@@ -530,9 +530,13 @@ def side_measurements(args, dev, st, rank):
         fs = pisa.Selector(p, device=dev, mode="flat")
         t_pisa = tm(lambda: sel.prefill(q, k, stream=st), 5)
         t_flat = tm(lambda: fs.flat(q, k, stream=st), 3)
+        pp = pisa.params_from_shape(s, summaries=pisa.SUMMARIES_PREFIX)
+        ps = pisa.Selector(pp, device=dev)
+        t_prefix = tm(lambda: ps.prefill(q, k, stream=st), 5)
         sweep[str(N)] = {"pisa_ms": t_pisa, "pisa_queries_per_s": N / t_pisa * 1e3, "flat_ms": t_flat,
-                         "pisa_over_flat_speedup": t_flat / t_pisa}
-        del q, k, sel, fs
+                         "pisa_over_flat_speedup": t_flat / t_pisa,
+                         "pisa_prefix_summaries_ms": t_prefix}
+        del q, k, sel, fs, ps
     torch.cuda.empty_cache()
     # decode: 64 sequences x 131072 cached keys, 32/8 heads, K = 32
     s = W.DECODE
