@@ -25,19 +25,29 @@ namespace pisa {
 constexpr int kFRows = 128;
 constexpr int kFCols = 128;
 constexpr int kFStagesB = 2;
-constexpr int kFCap = kMaxK;  // Top-K list per query
-constexpr int kFlatThreads = 192;
+constexpr int kFCap = kMaxK;  // Top-K list per query and column slice
+// Epilogue warps: each TMEM lane quadrant (32 rows) is read by S warps, one
+// per slice of 128 / S columns; S grows with the group size so the per-slice
+// Top-K lists of the 128 / G queries of a tile fit in shared memory.
+template <int G>
+constexpr int flat_slices() { return G >= 4 ? 4 : G; }
+template <int G>
+constexpr int flat_threads() { return 32 * (2 + 4 * flat_slices<G>()); }
 constexpr uint32_t kFTmemCols = 256;
 constexpr uint64_t kFWaitNs = 4000000000ull;
 
 template <int D, int G>
 struct FlatSmem {
+  static constexpr int S = flat_slices<G>();
   uint8_t a[2][kFRows * D * 2];
   uint8_t b[kFStagesB][kFCols * D * 2];
-  float top_s[kFRows / G][kFCap];
-  int32_t top_i[kFRows / G][kFCap];
+  float top_s[S][kFRows / G][kFCap];   // per (slice, query): best K so far, score descending
+  int32_t top_i[S][kFRows / G][kFCap];
+  int32_t top_n[S][kFRows / G];
+  float2 part[S][kFRows];              // per (slice, row): online (max, sum) of pass 0
   uint64_t full_a[2], empty_a[2], full_b[kFStagesB], empty_b[kFStagesB];
   uint64_t tfull[2], tempty[2], done;
+  uint64_t ep_bar;                     // the epilogue warps' rendezvous (two phases per query tile)
   uint32_t tmem_base;
   int32_t abort, zero;
 };
@@ -65,7 +75,7 @@ __device__ __forceinline__ int flat_nj(const Prob& pr, int64_t t0, int Qt) {
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kFlatThreads, 1)
+__global__ void __launch_bounds__(flat_threads<G>(), 1)
     flat_tc_kernel(Prob pr, FlatTiles ft, int64_t nb, const __grid_constant__ CUtensorMap mumap,
                    const uint16_t* __restrict__ q, int32_t* __restrict__ out_idx, float* __restrict__ out_score,
                    int32_t* __restrict__ status) {
@@ -85,13 +95,14 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
       ptx::mbar_init(ptx::smem_u32(&sm.full_a[s]), 32);
       ptx::mbar_init(ptx::smem_u32(&sm.empty_a[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&sm.tfull[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&sm.tempty[s]), 4);
+      ptx::mbar_init(ptx::smem_u32(&sm.tempty[s]), 4 * FlatSmem<D, G>::S);
     }
     for (int s = 0; s < kFStagesB; ++s) {
       ptx::mbar_init(ptx::smem_u32(&sm.full_b[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&sm.empty_b[s]), 1);
     }
     ptx::mbar_init(ptx::smem_u32(&sm.done), 1);
+    ptx::mbar_init(ptx::smem_u32(&sm.ep_bar), 4 * FlatSmem<D, G>::S);
     sm.abort = 0;
     sm.zero = 0;
     ptx::fence_mbar_init();
@@ -201,37 +212,66 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q4 = warp & 3;
+    // warp (quadrant q4, slice sl): rows q4 * 32 + lane, columns
+    // [sl * SW, sl * SW + SW) of every 128-column tile
+    constexpr int S = FlatSmem<D, G>::S;
+    constexpr int SW = kFCols / S;  // 32, 64 or 128 columns
+    const int e = warp - 2;
+    const int q4 = e & 3, sl = e >> 2;
     const int r = q4 * 32 + lane;
     const int g = r % G, qi = r / G;
     const float sc = pr.scale2;
     const int K = pr.K, W = K + 3;
-    float* ts = sm.top_s[qi];
-    int32_t* tix = sm.top_i[qi];  // used by the g == 0 lane of each query
-    int it = 0;
+    float* ts = sm.top_s[sl][qi];
+    int32_t* tix = sm.top_i[sl][qi];  // used by the g == 0 lane of each query
+    int it = 0, eph = 0;
     bool ok = true;
+    // the epilogue warps' rendezvous: every warp arrives, then waits (bounded)
+    auto rendezvous = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.ep_bar));
+      const bool okw = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.ep_bar), eph & 1, abort, kFWaitNs);
+      ++eph;
+      return __all_sync(0xffffffffu, okw);
+    };
     for (int64_t qt = blockIdx.x; qt < QT && ok; qt += gridDim.x) {
       const int64_t bh = qt / ft.nqt, t0 = (qt % ft.nqt) * Qt;
       const int nj = flat_nj(pr, t0, Qt);
       const int64_t t = t0 + qi;
       const int64_t qb = t < pr.N ? t / pr.C : 0;  // valid columns: [0, qb)
       float m = -INFINITY, ssum = 0.0f, lse = 0.0f;
-      int cnt = 0;              // entries in this query's buffer (g == 0 lane)
-      float theta = -INFINITY;  // K-th best so far, once cnt has reached K
+      int cnt = 0;              // entries in this slice's list of the query (g == 0 lane)
+      float theta = -INFINITY;  // its K-th best, once cnt has reached K
       for (int pass = 0; pass < 2 && ok; ++pass) {
-        if (pass == 1) lse = m + ptx::lg2(ssum);
+        if (pass == 1) {
+          // the row's log2-sum-exp2 from the S slices' partials
+          sm.part[sl][r] = make_float2(m, ssum);
+          if (!rendezvous()) { ok = false; *abort = 1; break; }
+          float mm = -INFINITY;
+#pragma unroll
+          for (int u = 0; u < S; ++u) mm = fmaxf(mm, sm.part[u][r].x);
+          float ss = 0.0f;
+#pragma unroll
+          for (int u = 0; u < S; ++u) {
+            const float2 pu = sm.part[u][r];
+            if (pu.x > -INFINITY) ss += pu.y * ptx::ex2(pu.x - mm);
+          }
+          lse = mm + ptx::lg2(ss);
+          // the lists are rewritten below only after this rendezvous, which
+          // the slice-0 warps reach after merging the previous tile's lists
+        }
         for (int j = 0; j < nj; ++j) {
           const int acc = it & 1;
           const bool okw = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tfull[acc]), (it >> 1) & 1, abort, kFWaitNs);
           if (!__all_sync(0xffffffffu, okw)) { ok = false; *abort = 1; break; }
           ptx::tc_fence_after();
-          const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + acc * kFCols;
-          const int64_t col0 = (int64_t)j * kFCols;
+          const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + acc * kFCols + sl * SW;
+          const int64_t col0 = (int64_t)j * kFCols + sl * SW;
           if (pass == 0) {
             float tm = -INFINITY;
-            float x[kFCols];
+            float x[SW];
 #pragma unroll
-            for (int c4 = 0; c4 < kFCols / 32; ++c4) {
+            for (int c4 = 0; c4 < SW / 32; ++c4) {
               uint32_t v[32];
               ptx::tmem_ld32(taddr + c4 * 32, v);
               ptx::tmem_ld_wait();
@@ -249,13 +289,13 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
               const float mn = fmaxf(m, tm);
               float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-              for (int c = 0; c < kFCols; ++c) s4[c & 3] += ptx::ex2(x[c] - mn);
+              for (int c = 0; c < SW; ++c) s4[c & 3] += ptx::ex2(x[c] - mn);
               ssum = ssum * ptx::ex2(m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
               m = mn;
             }
           } else {
 #pragma unroll 1
-            for (int c4 = 0; c4 < kFCols / 32; ++c4) {
+            for (int c4 = 0; c4 < SW / 32; ++c4) {
               uint32_t v[32];
               ptx::tmem_ld32(taddr + c4 * 32, v);
               ptx::tmem_ld_wait();
@@ -270,11 +310,11 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
                 pv[c] = (col >= 1 && col <= qb - 2) ? p : -INFINITY;  // Top-K runs over E only
                 bmax = fmaxf(bmax, pv[c]);
               }
-              // the group's first lane keeps its query's best K sorted (higher
-              // score first; a later column never passes an equal score, so
-              // ties keep the lower block index) and inserts every column
-              // above the current K-th best: O(K) per insertion, and after the
-              // first columns insertions are rare
+              // the group's first lane keeps this slice's best K of its query
+              // sorted (higher score first; a later column never passes an
+              // equal score, so ties keep the lower block index) and inserts
+              // every column above the current K-th best: O(K) per insertion,
+              // and after the first columns insertions are rare
               if (g == 0 && bmax > theta) {
 #pragma unroll 1
                 for (int c = 0; c < 32; ++c) {
@@ -302,22 +342,49 @@ __global__ void __launch_bounds__(kFlatThreads, 1)
         }
       }
       if (!ok) break;
-      // output for this query: Top-K (ascending) plus F
-      if (g == 0 && t < pr.N) {
+      if (g == 0) sm.top_n[sl][qi] = cnt;
+      if (!rendezvous()) { ok = false; *abort = 1; break; }  // every slice's list is complete
+      // output (slice-0 warps): the best K of the S sorted lists (ties to the
+      // lower block index), ascending, together with F
+      if (sl == 0 && g == 0 && t < pr.N) {
+        float bs[kFCap];
+        int32_t bi[kFCap];
+        int head[S];
+#pragma unroll
+        for (int u = 0; u < S; ++u) head[u] = 0;
+        int n = 0;
+        for (; n < K; ++n) {
+          int bu = -1;
+#pragma unroll
+          for (int u = 0; u < S; ++u) {
+            if (head[u] < sm.top_n[u][qi]) {
+              const float su = sm.top_s[u][qi][head[u]];
+              const int32_t iu = sm.top_i[u][qi][head[u]];
+              if (bu < 0 || su > bs[n] || (su == bs[n] && iu < bi[n])) {
+                bu = u;
+                bs[n] = su;
+                bi[n] = iu;
+              }
+            }
+          }
+          if (bu < 0) break;
+#pragma unroll
+          for (int u = 0; u < S; ++u) head[u] += (u == bu) ? 1 : 0;
+        }
         // insertion sort of the kept entries by block index
-        for (int u = 1; u < cnt; ++u) {
-          const float sv = ts[u];
-          const int32_t iv = tix[u];
+        for (int u = 1; u < n; ++u) {
+          const float sv = bs[u];
+          const int32_t iv = bi[u];
           int w = u - 1;
-          while (w >= 0 && tix[w] > iv) { ts[w + 1] = ts[w]; tix[w + 1] = tix[w]; --w; }
-          ts[w + 1] = sv; tix[w + 1] = iv;
+          while (w >= 0 && bi[w] > iv) { bs[w + 1] = bs[w]; bi[w + 1] = bi[w]; --w; }
+          bs[w + 1] = sv; bi[w + 1] = iv;
         }
         const int64_t qrow = bh * pr.N + t;
         int32_t* oi = out_idx + qrow * W;
         float* os = out_score ? out_score + qrow * W : nullptr;
         int pos = 0;
         oi[pos] = 0; if (os) os[pos] = INFINITY; ++pos;
-        for (int u = 0; u < cnt; ++u) { oi[pos] = tix[u]; if (os) os[pos] = ts[u]; ++pos; }
+        for (int u = 0; u < n; ++u) { oi[pos] = bi[u]; if (os) os[pos] = bs[u]; ++pos; }
         if (qb - 1 > 0) { oi[pos] = (int32_t)(qb - 1); if (os) os[pos] = INFINITY; ++pos; }
         if (qb > 0) { oi[pos] = (int32_t)qb; if (os) os[pos] = INFINITY; ++pos; }
         for (; pos < W; ++pos) { oi[pos] = -1; if (os) os[pos] = -INFINITY; }
@@ -343,7 +410,7 @@ static cudaError_t launch_flat_t(const Prob& pr, int64_t nb, const void* q, cons
   ft.Qt = kFRows / G;
   ft.nqt = ceil_div64(pr.N, ft.Qt);
   note_launch();
-  kern<<<grid, kFlatThreads, smem, st>>>(pr, ft, nb, mumap, (const uint16_t*)q, out_idx, out_score, status);
+  kern<<<grid, flat_threads<G>(), smem, st>>>(pr, ft, nb, mumap, (const uint16_t*)q, out_idx, out_score, status);
   return cudaGetLastError();
 }
 
