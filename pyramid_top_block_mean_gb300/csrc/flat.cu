@@ -213,11 +213,12 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
   } else {
     // ------------------------------------------------------------ epilogue
     // warp (quadrant q4, slice sl): rows q4 * 32 + lane, columns
-    // [sl * SW, sl * SW + SW) of every 128-column tile
+    // [sl * SW, sl * SW + SW) of every 128-column tile.  A warp can only read
+    // the TMEM lane quadrant warp % 4, so q4 = warp & 3; the slices take the
+    // epilogue warps in groups of four
     constexpr int S = FlatSmem<D, G>::S;
     constexpr int SW = kFCols / S;  // 32, 64 or 128 columns
-    const int e = warp - 2;
-    const int q4 = e & 3, sl = e >> 2;
+    const int q4 = warp & 3, sl = (warp - 2) >> 2;
     const int r = q4 * 32 + lane;
     const int g = r % G, qi = r / G;
     const float sc = pr.scale2;
