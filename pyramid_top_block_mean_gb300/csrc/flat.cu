@@ -32,7 +32,45 @@ constexpr int kFCap = kMaxK;  // Top-K list per query and column slice
 template <int G>
 constexpr int flat_slices() { return G >= 4 ? 4 : G; }
 template <int G>
-constexpr int flat_threads() { return 32 * (2 + 4 * flat_slices<G>()); }
+constexpr int flat_threads() { return 32 * (3 + 4 * flat_slices<G>()); }
+
+// Bounded wait for the epilogue warps, which wait for most of a tile: after a
+// short spin they sleep between probes so that waiting warps leave issue
+// slots to the loader and MMA warps of the SM.
+__device__ __forceinline__ bool flat_wait_sleepy(uint32_t bar, uint32_t parity, volatile int32_t* abort,
+                                                 uint64_t limit_ns) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  uint32_t ns = 32;
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (it >= 8) {
+      __nanosleep(ns);
+      if (ns < 256) ns *= 2;
+    }
+    if ((it & 15u) == 0) {
+      if (*abort) return false;
+      if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
+    }
+  }
+}
+
+// Inserts (score pc, block col) into a query's best-K list (score descending;
+// an equal score never passes an earlier entry, so ties keep the lower block
+// index, columns arriving in increasing order).  Returns the new K-th best
+// once the list is full, else -INFINITY.
+__device__ __noinline__ float flat_insert(float* ts, int32_t* tix, int* cnt, int K, float pc, int32_t col) {
+  int pos = *cnt < K ? *cnt : K - 1;
+  while (pos > 0 && ts[pos - 1] < pc) {
+    ts[pos] = ts[pos - 1];
+    tix[pos] = tix[pos - 1];
+    --pos;
+  }
+  ts[pos] = pc;
+  tix[pos] = col;
+  if (*cnt < K) ++*cnt;
+  return *cnt == K ? ts[K - 1] : -INFINITY;
+}
 constexpr uint32_t kFTmemCols = 256;
 constexpr uint64_t kFWaitNs = 4000000000ull;
 
@@ -118,10 +156,10 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------- query gathers
     constexpr int CPR = D / 8, RPI = 32 / CPR;
     const int ch = lane % CPR;
-    int ia = 0, ib = 0;
+    int ia = 0;
     bool ok = true;
     for (int64_t qt = blockIdx.x; qt < QT && ok; qt += gridDim.x) {
       const int64_t bh = qt / ft.nqt, t0 = (qt % ft.nqt) * Qt;
@@ -145,32 +183,37 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(ptx::smem_u32(&sm.full_a[sa]));
       ++ia;
-      for (int pass = 0; pass < 2 && ok; ++pass)
-        for (int j = 0; j < nj; ++j) {
-          const int sb = ib % kFStagesB, ub = ib / kFStagesB;
-          int okb = 1;
-          if (lane == 0) {
-            okb = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_b[sb]), (ub & 1) ^ 1, abort, kFWaitNs);
-            if (okb) {
-              const uint32_t fb = ptx::smem_u32(&sm.full_b[sb]);
-              ptx::mbar_arrive_expect_tx(fb, kBBytes);
-              const int32_t y = (int32_t)(bh * nb + (int64_t)j * kFCols);
-#pragma unroll
-              for (int hh = 0; hh < D / 64; ++hh)
-                ptx::tma_load_2d(ptx::smem_u32(sm.b[sb]) + hh * kHalf, &mumap, 64 * hh, y, fb);
-            }
-          }
-          ok = __shfl_sync(0xffffffffu, okb, 0) != 0;
-          if (!ok) break;
-          ++ib;
-        }
     }
     if (!ok) *abort = 1;
-    // every issued load lands before the CTA can exit, whoever gave up
-    if (lane == 0)
+  } else if (warp == 2) {
+    // ------------------------------------------------------- key-mean tiles
+    if (lane == 0) {
+      int ib = 0;
+      bool ok = true;
+      for (int64_t qt = blockIdx.x; qt < QT && ok; qt += gridDim.x) {
+        const int64_t bh = qt / ft.nqt, t0 = (qt % ft.nqt) * Qt;
+        const int nj = flat_nj(pr, t0, Qt);
+        for (int pass = 0; pass < 2 && ok; ++pass)
+          for (int j = 0; j < nj; ++j) {
+            const int sb = ib % kFStagesB, ub = ib / kFStagesB;
+            ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_b[sb]), (ub & 1) ^ 1, abort, kFWaitNs);
+            if (!ok) break;
+            const uint32_t fb = ptx::smem_u32(&sm.full_b[sb]);
+            ptx::mbar_arrive_expect_tx(fb, kBBytes);
+            const int32_t y = (int32_t)(bh * nb + (int64_t)j * kFCols);
+#pragma unroll
+            for (int hh = 0; hh < D / 64; ++hh)
+              ptx::tma_load_2d(ptx::smem_u32(sm.b[sb]) + hh * kHalf, &mumap, 64 * hh, y, fb);
+            ++ib;
+          }
+      }
+      if (!ok) *abort = 1;
+      // every issued load lands before the CTA can exit, whoever gave up
       for (int k = ib > kFStagesB ? ib - kFStagesB : 0; k < ib; ++k)
         ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[k % kFStagesB]), (k / kFStagesB) & 1, &sm.zero,
                                kFWaitNs);
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ----------------------------------------------------------------- MMA
     if (lane == 0) {
@@ -218,7 +261,7 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
     // epilogue warps in groups of four
     constexpr int S = FlatSmem<D, G>::S;
     constexpr int SW = kFCols / S;  // 32, 64 or 128 columns
-    const int q4 = warp & 3, sl = (warp - 2) >> 2;
+    const int q4 = warp & 3, sl = (warp - 3) >> 2;
     const int r = q4 * 32 + lane;
     const int g = r % G, qi = r / G;
     const float sc = pr.scale2;
@@ -263,7 +306,7 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
         }
         for (int j = 0; j < nj; ++j) {
           const int acc = it & 1;
-          const bool okw = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tfull[acc]), (it >> 1) & 1, abort, kFWaitNs);
+          const bool okw = flat_wait_sleepy(ptx::smem_u32(&sm.tfull[acc]), (it >> 1) & 1, abort, kFWaitNs);
           if (!__all_sync(0xffffffffu, okw)) { ok = false; *abort = 1; break; }
           ptx::tc_fence_after();
           const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + acc * kFCols + sl * SW;
@@ -317,22 +360,9 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
               // every column above the current K-th best: O(K) per insertion,
               // and after the first columns insertions are rare
               if (g == 0 && bmax > theta) {
-#pragma unroll 1
-                for (int c = 0; c < 32; ++c) {
-                  const float pc = pv[c];
-                  if (pc > theta) {
-                    int pos = cnt < K ? cnt : K - 1;
-                    while (pos > 0 && ts[pos - 1] < pc) {
-                      ts[pos] = ts[pos - 1];
-                      tix[pos] = tix[pos - 1];
-                      --pos;
-                    }
-                    ts[pos] = pc;
-                    tix[pos] = (int32_t)(col0 + c4 * 32 + c);
-                    if (cnt < K) ++cnt;
-                    if (cnt == K) theta = ts[K - 1];
-                  }
-                }
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                  if (pv[c] > theta) theta = flat_insert(ts, tix, &cnt, K, pv[c], (int32_t)(col0 + c4 * 32 + c));
               }
             }
             ptx::tc_fence_before();
