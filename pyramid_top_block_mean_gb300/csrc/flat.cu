@@ -55,22 +55,6 @@ __device__ __forceinline__ bool flat_wait_sleepy(uint32_t bar, uint32_t parity, 
   }
 }
 
-// Inserts (score pc, block col) into a query's best-K list (score descending;
-// an equal score never passes an earlier entry, so ties keep the lower block
-// index, columns arriving in increasing order).  Returns the new K-th best
-// once the list is full, else -INFINITY.
-__device__ __noinline__ float flat_insert(float* ts, int32_t* tix, int* cnt, int K, float pc, int32_t col) {
-  int pos = *cnt < K ? *cnt : K - 1;
-  while (pos > 0 && ts[pos - 1] < pc) {
-    ts[pos] = ts[pos - 1];
-    tix[pos] = tix[pos - 1];
-    --pos;
-  }
-  ts[pos] = pc;
-  tix[pos] = col;
-  if (*cnt < K) ++*cnt;
-  return *cnt == K ? ts[K - 1] : -INFINITY;
-}
 constexpr uint32_t kFTmemCols = 256;
 constexpr uint64_t kFWaitNs = 4000000000ull;
 
@@ -83,6 +67,9 @@ struct FlatSmem {
   int32_t top_i[S][kFRows / G][kFCap];
   int32_t top_n[S][kFRows / G];
   float2 part[S][kFRows];              // per (slice, row): online (max, sum) of pass 0
+  float cut[kFRows / G];               // per query: the largest K-th best of its full slice lists (a lower
+                                       // bound on its final K-th best); non-negative, so ordered as int bits
+  float stash[4 * S][32 / G][32];      // per (epilogue warp, query): a chunk's scores awaiting insertion
   uint64_t full_a[2], empty_a[2], full_b[kFStagesB], empty_b[kFStagesB];
   uint64_t tfull[2], tempty[2], done;
   uint64_t ep_bar;                     // the epilogue warps' rendezvous (two phases per query tile)
@@ -112,7 +99,7 @@ __device__ __forceinline__ int flat_nj(const Prob& pr, int64_t t0, int Qt) {
   return (int)ceil_div64(qb_last, kFCols);
 }
 
-template <int D, int G>
+template <int D, int G, int KR>
 __global__ void __launch_bounds__(flat_threads<G>(), 1)
     flat_tc_kernel(Prob pr, FlatTiles ft, int64_t nb, const __grid_constant__ CUtensorMap mumap,
                    const uint16_t* __restrict__ q, int32_t* __restrict__ out_idx, float* __restrict__ out_score,
@@ -283,13 +270,27 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
       const int nj = flat_nj(pr, t0, Qt);
       const int64_t t = t0 + qi;
       const int64_t qb = t < pr.N ? t / pr.C : 0;  // valid columns: [0, qb)
+      const int qb32 = (int)qb;
       float m = -INFINITY, ssum = 0.0f, lse = 0.0f;
       int cnt = 0;              // entries in this slice's list of the query (g == 0 lane)
       float theta = -INFINITY;  // its K-th best, once cnt has reached K
+      // K <= 8: the list lives in the g == 0 lane's registers, sorted (best
+      // first, -inf padded); positions past K may hold stale entries below
+      // the K-th best, which the output never reads
+      float rl[8];
+      int32_t ri[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        rl[i] = -INFINITY;
+        ri[i] = -1;
+      }
       for (int pass = 0; pass < 2 && ok; ++pass) {
         if (pass == 1) {
-          // the row's log2-sum-exp2 from the S slices' partials
+          // the row's log2-sum-exp2 from the S slices' partials; the query's
+          // shared cut restarts (no slice reads it before this rendezvous,
+          // and slice 0 resets it after merging the previous tile's lists)
           sm.part[sl][r] = make_float2(m, ssum);
+          if (sl == 0 && g == 0) sm.cut[qi] = 0.0f;
           if (!rendezvous()) { ok = false; *abort = 1; break; }
           float mm = -INFINITY;
 #pragma unroll
@@ -310,8 +311,9 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
           if (!__all_sync(0xffffffffu, okw)) { ok = false; *abort = 1; break; }
           ptx::tc_fence_after();
           const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + acc * kFCols + sl * SW;
-          const int64_t col0 = (int64_t)j * kFCols + sl * SW;
+          const int col0 = j * kFCols + sl * SW;  // block indices fit in 32 bits (N <= 2^26)
           if (pass == 0) {
+            // raw dots (scale applied in the exponent; s > 0 keeps the order)
             float tm = -INFINITY;
             float x[SW];
 #pragma unroll
@@ -319,21 +321,25 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
               uint32_t v[32];
               ptx::tmem_ld32(taddr + c4 * 32, v);
               ptx::tmem_ld_wait();
+              const int nv = qb32 - (col0 + c4 * 32);  // columns c < nv are past blocks
+              if (__all_sync(0xffffffffu, nv >= 32)) {
 #pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const int col = c4 * 32 + c;
-                x[col] = (col0 + col < qb) ? __uint_as_float(v[c]) * sc : -INFINITY;
-                tm = fmaxf(tm, x[col]);
+                for (int c = 0; c < 32; ++c) x[c4 * 32 + c] = __uint_as_float(v[c]);
+              } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[c4 * 32 + c] = c < nv ? __uint_as_float(v[c]) : -INFINITY;
               }
+#pragma unroll
+              for (int c = 0; c < 32; c += 2) tm = fmaxf(tm, fmaxf(x[c4 * 32 + c], x[c4 * 32 + c + 1]));
             }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&sm.tempty[acc]));
             if (tm > -INFINITY) {
-              const float mn = fmaxf(m, tm);
+              const float mn = fmaxf(m, tm * sc);
               float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-              for (int c = 0; c < SW; ++c) s4[c & 3] += ptx::ex2(x[c] - mn);
+              for (int c = 0; c < SW; ++c) s4[c & 3] += ptx::ex2(fmaf(x[c], sc, -mn));
               ssum = ssum * ptx::ex2(m - mn) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
               m = mn;
             }
@@ -343,26 +349,105 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
               uint32_t v[32];
               ptx::tmem_ld32(taddr + c4 * 32, v);
               ptx::tmem_ld_wait();
+              const int cb = col0 + c4 * 32;
+              const int nv = qb32 - cb;                  // c < nv: past blocks (in the softmax)
+              const int elo = 1 - cb, ehi = qb32 - 2 - cb;  // elo <= c <= ehi: in E (ranked)
               float pv[32];
               float bmax = -INFINITY;
+              if (__all_sync(0xffffffffu, elo <= 0 && ehi >= 31)) {
 #pragma unroll
-              for (int c = 0; c < 32; ++c) {
-                const int64_t col = col0 + c4 * 32 + c;
-                float p = (col < qb) ? ptx::ex2(__uint_as_float(v[c]) * sc - lse) : 0.0f;
+                for (int c = 0; c < 32; ++c) {
+                  float p = ptx::ex2(fmaf(__uint_as_float(v[c]), sc, -lse));
 #pragma unroll
-                for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-                pv[c] = (col >= 1 && col <= qb - 2) ? p : -INFINITY;  // Top-K runs over E only
-                bmax = fmaxf(bmax, pv[c]);
+                  for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                  pv[c] = p;
+                }
+              } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                  float p = c < nv ? ptx::ex2(fmaf(__uint_as_float(v[c]), sc, -lse)) : 0.0f;
+#pragma unroll
+                  for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                  pv[c] = (c >= elo && c <= ehi) ? p : -INFINITY;  // Top-K runs over E only
+                }
               }
+#pragma unroll
+              for (int c = 0; c < 32; c += 2) bmax = fmaxf(bmax, fmaxf(pv[c], pv[c + 1]));
               // the group's first lane keeps this slice's best K of its query
               // sorted (higher score first; a later column never passes an
-              // equal score, so ties keep the lower block index) and inserts
-              // every column above the current K-th best: O(K) per insertion,
-              // and after the first columns insertions are rare
-              if (g == 0 && bmax > theta) {
+              // equal score, so ties keep the lower block index).  A column
+              // below the query's shared cut -- the largest K-th best of any
+              // slice's full list, hence at most the final K-th best -- cannot
+              // be kept; equal ones are, and the merge orders ties by index.
+              if constexpr (KR <= 8) {
+                // columns above the cut, one bit each; then sorted insertion of
+                // each (select-shift over the register list, ties keeping the
+                // earlier column)
+                if (g == 0) {
+                  float cut = fmaxf(theta, sm.cut[qi]);
+                  if (bmax >= cut) {
+                    uint32_t msk = 0;
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
-                  if (pv[c] > theta) theta = flat_insert(ts, tix, &cnt, K, pv[c], (int32_t)(col0 + c4 * 32 + c));
+                    for (int c = 0; c < 32; ++c) msk |= (pv[c] >= cut && pv[c] > theta) ? (1u << c) : 0u;
+                    float* st = sm.stash[warp - 3][qi % (32 / G)];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                      *reinterpret_cast<float4*>(st + c) = make_float4(pv[c], pv[c + 1], pv[c + 2], pv[c + 3]);
+                    while (msk) {
+                      const int c = __ffs(msk) - 1;
+                      msk &= msk - 1;
+                      const float x = st[c];
+                      if (!(x > theta) || x < cut) continue;
+                      bool ge[8];
+#pragma unroll
+                      for (int i = 0; i < 8; ++i) ge[i] = rl[i] >= x;
+#pragma unroll
+                      for (int i = 7; i >= 1; --i) {
+                        rl[i] = ge[i] ? rl[i] : (ge[i - 1] ? x : rl[i - 1]);
+                        ri[i] = ge[i] ? ri[i] : (ge[i - 1] ? cb + c : ri[i - 1]);
+                      }
+                      rl[0] = ge[0] ? rl[0] : x;
+                      ri[0] = ge[0] ? ri[0] : cb + c;
+                      if (cnt < K) ++cnt;
+                      if (cnt == K) {
+                        float kth = rl[0];
+#pragma unroll
+                        for (int i = 1; i < 8; ++i) kth = (i == K - 1) ? rl[i] : kth;
+                        theta = kth;
+                        cut = fmaxf(cut, theta);
+                        atomicMax(reinterpret_cast<int*>(&sm.cut[qi]), __float_as_int(theta));
+                      }
+                    }
+                  }
+                }
+              } else {
+                if (g == 0) {
+                  float cut = fmaxf(theta, sm.cut[qi]);
+                  if (bmax >= cut) {
+                    float* st = sm.stash[warp - 3][qi % (32 / G)];
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                      *reinterpret_cast<float4*>(st + c) = make_float4(pv[c], pv[c + 1], pv[c + 2], pv[c + 3]);
+                    for (int c = 0; c < 32; ++c) {
+                      const float pc = st[c];
+                      if (pc < cut || (cnt == K && !(pc > theta))) continue;
+                      int pos = cnt < K ? cnt : K - 1;
+                      while (pos > 0 && ts[pos - 1] < pc) {
+                        ts[pos] = ts[pos - 1];
+                        tix[pos] = tix[pos - 1];
+                        --pos;
+                      }
+                      ts[pos] = pc;
+                      tix[pos] = cb + c;
+                      if (cnt < K) ++cnt;
+                      if (cnt == K) {
+                        theta = ts[K - 1];
+                        cut = fmaxf(cut, theta);
+                        atomicMax(reinterpret_cast<int*>(&sm.cut[qi]), __float_as_int(theta));
+                      }
+                    }
+                  }
+                }
               }
             }
             ptx::tc_fence_before();
@@ -373,6 +458,15 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
         }
       }
       if (!ok) break;
+      if constexpr (KR <= 8) {
+        if (g == 0) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            ts[i] = rl[i];
+            tix[i] = ri[i];
+          }
+        }
+      }
       if (g == 0) sm.top_n[sl][qi] = cnt;
       if (!rendezvous()) { ok = false; *abort = 1; break; }  // every slice's list is complete
       // output (slice-0 warps): the best K of the S sorted lists (ties to the
@@ -430,11 +524,11 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
   if (threadIdx.x == 0 && sm.abort) set_status(status, PISA_DEV_TIMEOUT);
 }
 
-template <int D, int G>
+template <int D, int G, int KR>
 static cudaError_t launch_flat_t(const Prob& pr, int64_t nb, const void* q, const CUtensorMap& mumap, int32_t* out_idx,
                                  float* out_score, int32_t* status, int grid, cudaStream_t st) {
   const size_t smem = sizeof(FlatSmem<D, G>) + 1024;
-  auto kern = flat_tc_kernel<D, G>;
+  auto kern = flat_tc_kernel<D, G, KR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   FlatTiles ft;
@@ -461,7 +555,9 @@ cudaError_t launch_flat(const Prob& pr, const Pyr& s, const void* q, const float
   if (!make_tmap_rows(&mumap, mu, nbh * s.nb, pr.d, kFCols)) return cudaErrorInvalidValue;
   const int grid = num_sms > 0 ? num_sms : 148;
 #define PISA_FLAT_CASE(DD, GG) \
-  if (pr.d == DD && pr.G == GG) return launch_flat_t<DD, GG>(pr, s.nb, q, mumap, out_idx, out_score, status, grid, st);
+  if (pr.d == DD && pr.G == GG)                                                                           \
+    return pr.K <= 8 ? launch_flat_t<DD, GG, 8>(pr, s.nb, q, mumap, out_idx, out_score, status, grid, st)  \
+                     : launch_flat_t<DD, GG, kFCap>(pr, s.nb, q, mumap, out_idx, out_score, status, grid, st);
   PISA_FLAT_CASE(128, 1) PISA_FLAT_CASE(128, 2) PISA_FLAT_CASE(128, 4) PISA_FLAT_CASE(128, 8)
   PISA_FLAT_CASE(64, 1) PISA_FLAT_CASE(64, 2) PISA_FLAT_CASE(64, 4) PISA_FLAT_CASE(64, 8)
 #undef PISA_FLAT_CASE
