@@ -55,7 +55,65 @@ __device__ __forceinline__ bool flat_wait_sleepy(uint32_t bar, uint32_t parity, 
   }
 }
 
-constexpr uint32_t kFTmemCols = 256;
+// (score, block) ordering of the Top-K: higher score first, then lower block
+// (empty entries, (-inf, -1), last).
+__device__ __forceinline__ bool flat_better(float x, int32_t xi, float y, int32_t yi) {
+  return x > y || (x == y && (uint32_t)xi < (uint32_t)yi);
+}
+
+// Two lanes' sorted best-8 lists (lanes l and l ^ o) merged into the best 8
+// of their union, sorted, in both lanes: the element-wise better of one list
+// and the other reversed holds the best 8 as a bitonic sequence, which three
+// half-cleaner stages sort.
+__device__ __forceinline__ void flat_merge8_xor(float (&a)[8], int32_t (&ai)[8], int o) {
+  float b[8];
+  int32_t bi[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    b[i] = __shfl_xor_sync(0xffffffffu, a[i], o);
+    bi[i] = __shfl_xor_sync(0xffffffffu, ai[i], o);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool tb = flat_better(b[7 - i], bi[7 - i], a[i], ai[i]);
+    a[i] = tb ? b[7 - i] : a[i];
+    ai[i] = tb ? bi[7 - i] : ai[i];
+  }
+#pragma unroll
+  for (int d = 4; d >= 1; d >>= 1)
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((i & d) == 0) {
+        const bool sw = flat_better(a[i + d], ai[i + d], a[i], ai[i]);
+        const float t = a[i];
+        const int32_t ti = ai[i];
+        a[i] = sw ? a[i + d] : a[i];
+        ai[i] = sw ? ai[i + d] : ai[i];
+        a[i + d] = sw ? t : a[i + d];
+        ai[i + d] = sw ? ti : ai[i + d];
+      }
+}
+
+// Eight entries sorted by block index, ascending (empty entries, block -1,
+// last): a 19-comparator sorting network.
+__device__ __forceinline__ void flat_sort8_by_block(float (&a)[8], int32_t (&ai)[8]) {
+  constexpr int kNet[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6}, {3, 7}, {0, 1}, {2, 3},
+                               {4, 5}, {6, 7}, {2, 4}, {3, 5}, {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+  for (int c = 0; c < 19; ++c) {
+    const int i = kNet[c][0], j = kNet[c][1];
+    const bool sw = (uint32_t)ai[j] < (uint32_t)ai[i];
+    const float t = a[i];
+    const int32_t ti = ai[i];
+    a[i] = sw ? a[j] : a[i];
+    ai[i] = sw ? ai[j] : ai[i];
+    a[j] = sw ? t : a[j];
+    ai[j] = sw ? ti : ai[j];
+  }
+}
+
+constexpr int kFAcc = 4;  // TMEM accumulators: the MMA runs up to four tiles ahead of the epilogue
+constexpr uint32_t kFTmemCols = kFAcc * kFCols;
 constexpr uint64_t kFWaitNs = 4000000000ull;
 
 template <int D, int G>
@@ -65,13 +123,13 @@ struct FlatSmem {
   uint8_t b[kFStagesB][kFCols * D * 2];
   float top_s[S][kFRows / G][kFCap];   // per (slice, query): best K so far, score descending
   int32_t top_i[S][kFRows / G][kFCap];
-  int32_t top_n[S][kFRows / G];
+  int32_t top_n[S][kFRows];            // entries per list, by (slice, row of the list's lane)
   float2 part[S][kFRows];              // per (slice, row): online (max, sum) of pass 0
   float cut[kFRows / G];               // per query: the largest K-th best of its full slice lists (a lower
                                        // bound on its final K-th best); non-negative, so ordered as int bits
-  float stash[4 * S][32 / G][32];      // per (epilogue warp, query): a chunk's scores awaiting insertion
+  float stash[4 * S][1024 / G];        // per epilogue warp: a chunk's scores awaiting insertion
   uint64_t full_a[2], empty_a[2], full_b[kFStagesB], empty_b[kFStagesB];
-  uint64_t tfull[2], tempty[2], done;
+  uint64_t tfull[kFAcc], tempty[kFAcc], done;
   uint64_t ep_bar;                     // the epilogue warps' rendezvous (two phases per query tile)
   uint32_t tmem_base;
   int32_t abort, zero;
@@ -119,6 +177,8 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(ptx::smem_u32(&sm.full_a[s]), 32);
       ptx::mbar_init(ptx::smem_u32(&sm.empty_a[s]), 1);
+    }
+    for (int s = 0; s < kFAcc; ++s) {
       ptx::mbar_init(ptx::smem_u32(&sm.tfull[s]), 1);
       ptx::mbar_init(ptx::smem_u32(&sm.tempty[s]), 4 * FlatSmem<D, G>::S);
     }
@@ -215,9 +275,9 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
         if (!ok) break;
         for (int pass = 0; pass < 2 && ok; ++pass)
           for (int j = 0; j < nj; ++j) {
-            const int sb = ib % kFStagesB, acc = it & 1;
+            const int sb = ib % kFStagesB, acc = it % kFAcc;
             ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.full_b[sb]), (ib / kFStagesB) & 1, abort, kFWaitNs) &&
-                 ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tempty[acc]), ((it >> 1) & 1) ^ 1, abort, kFWaitNs);
+                 ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tempty[acc]), ((it / kFAcc) & 1) ^ 1, abort, kFWaitNs);
             if (!ok) break;
             ptx::tc_fence_after();
             const uint32_t a0 = ptx::smem_u32(sm.a[sa]), b0 = ptx::smem_u32(sm.b[sb]);
@@ -248,6 +308,11 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
     // epilogue warps in groups of four
     constexpr int S = FlatSmem<D, G>::S;
     constexpr int SW = kFCols / S;  // 32, 64 or 128 columns
+    // K <= 8 and G <= 4: a register list per lane (over the lane's columns of
+    // each chunk); otherwise one list per query, kept by its g == 0 lane
+    constexpr bool kLaneLists = KR <= 8 && G <= 4;
+    constexpr int LG = kLaneLists ? G : 1;  // lists per (slice, query)
+    const int mth = (pr.K + LG - 1) / LG - 1;  // list entry whose minimum over the query's lanes bounds its K-th best
     const int q4 = warp & 3, sl = (warp - 3) >> 2;
     const int r = q4 * 32 + lane;
     const int g = r % G, qi = r / G;
@@ -279,6 +344,7 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
       // the K-th best, which the output never reads
       float rl[8];
       int32_t ri[8];
+      float pub = 0.0f;  // the largest bound this lane has published to the query's cut
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         rl[i] = -INFINITY;
@@ -306,8 +372,8 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
           // the slice-0 warps reach after merging the previous tile's lists
         }
         for (int j = 0; j < nj; ++j) {
-          const int acc = it & 1;
-          const bool okw = flat_wait_sleepy(ptx::smem_u32(&sm.tfull[acc]), (it >> 1) & 1, abort, kFWaitNs);
+          const int acc = it % kFAcc;
+          const bool okw = flat_wait_sleepy(ptx::smem_u32(&sm.tfull[acc]), (it / kFAcc) & 1, abort, kFWaitNs);
           if (!__all_sync(0xffffffffu, okw)) { ok = false; *abort = 1; break; }
           ptx::tc_fence_after();
           const uint32_t taddr = tmem + ((uint32_t)(q4 * 32) << 16) + acc * kFCols + sl * SW;
@@ -352,102 +418,189 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
               const int cb = col0 + c4 * 32;
               const int nv = qb32 - cb;                  // c < nv: past blocks (in the softmax)
               const int elo = 1 - cb, ehi = qb32 - 2 - cb;  // elo <= c <= ehi: in E (ranked)
-              float pv[32];
-              float bmax = -INFINITY;
-              if (__all_sync(0xffffffffu, elo <= 0 && ehi >= 31)) {
+              if constexpr (kLaneLists) {
+                // every lane keeps a list of its own columns: the G lanes of a
+                // query reduce-scatter the head sum, lane g ending with
+                // columns [CPL g, CPL g + CPL) of the chunk
+                constexpr int CPL = 32 / G;
+                const bool inner = __all_sync(0xffffffffu, elo <= 0 && ehi >= 31);
+                float e[32];
+                if (inner) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                  float p = ptx::ex2(fmaf(__uint_as_float(v[c]), sc, -lse));
+                  for (int c = 0; c < 32; ++c) e[c] = ptx::ex2(fmaf(__uint_as_float(v[c]), sc, -lse));
+                } else {
 #pragma unroll
-                  for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-                  pv[c] = p;
+                  for (int c = 0; c < 32; ++c) e[c] = c < nv ? ptx::ex2(fmaf(__uint_as_float(v[c]), sc, -lse)) : 0.0f;
                 }
-              } else {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                  float p = c < nv ? ptx::ex2(fmaf(__uint_as_float(v[c]), sc, -lse)) : 0.0f;
+                for (int o = G / 2, n = 32; o >= 1; o >>= 1, n >>= 1) {
+                  const bool up = (lane & o) != 0;
 #pragma unroll
-                  for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
-                  pv[c] = (c >= elo && c <= ehi) ? p : -INFINITY;  // Top-K runs over E only
+                  for (int i = 0; i < n / 2; ++i) {
+                    const float keep = up ? e[i + n / 2] : e[i];
+                    const float send = up ? e[i] : e[i + n / 2];
+                    e[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                  }
                 }
-              }
+                const int cg = CPL * g;  // this lane's first column of the chunk
+                float bm = -INFINITY;
 #pragma unroll
-              for (int c = 0; c < 32; c += 2) bmax = fmaxf(bmax, fmaxf(pv[c], pv[c + 1]));
-              // the group's first lane keeps this slice's best K of its query
-              // sorted (higher score first; a later column never passes an
-              // equal score, so ties keep the lower block index).  A column
-              // below the query's shared cut -- the largest K-th best of any
-              // slice's full list, hence at most the final K-th best -- cannot
-              // be kept; equal ones are, and the merge orders ties by index.
-              if constexpr (KR <= 8) {
-                // columns above the cut, one bit each; then sorted insertion of
-                // each (select-shift over the register list, ties keeping the
-                // earlier column)
-                if (g == 0) {
-                  float cut = fmaxf(theta, sm.cut[qi]);
-                  if (bmax >= cut) {
-                    uint32_t msk = 0;
+                for (int i = 0; i < CPL; ++i) {
+                  if (!inner) e[i] = (cg + i >= elo && cg + i <= ehi) ? e[i] : -INFINITY;  // Top-K over E only
+                  bm = fmaxf(bm, e[i]);
+                }
+                // columns at or above the query's shared cut (the largest K-th
+                // best of its full lists, at most its final K-th best) and
+                // above the lane's own K-th best, then sorted insertion of each
+                // (select-shift over the register list; ties keep the earlier
+                // column, and the merge orders ties across lists by index)
+                // the lists of the query's G lanes are disjoint, so the
+                // smallest of their m-th bests (m = ceil(K / G) - 1) is reached
+                // by at least K columns: a lower bound on the final K-th best
+                float tm = rl[0];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) msk |= (pv[c] >= cut && pv[c] > theta) ? (1u << c) : 0u;
-                    float* st = sm.stash[warp - 3][qi % (32 / G)];
+                for (int u = 1; u < 8; ++u) tm = (u == mth) ? rl[u] : tm;
 #pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                      *reinterpret_cast<float4*>(st + c) = make_float4(pv[c], pv[c + 1], pv[c + 2], pv[c + 3]);
-                    while (msk) {
-                      const int c = __ffs(msk) - 1;
-                      msk &= msk - 1;
-                      const float x = st[c];
-                      if (!(x > theta) || x < cut) continue;
-                      bool ge[8];
+                for (int o = 1; o < G; o <<= 1) tm = fminf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+                if (g == 0 && tm > pub) {
+                  pub = tm;
+                  atomicMax(reinterpret_cast<int*>(&sm.cut[qi]), __float_as_int(tm));
+                }
+                float cut = fmaxf(fmaxf(theta, tm), sm.cut[qi]);
+                if (bm >= cut) {
+                  uint32_t msk = 0;
 #pragma unroll
-                      for (int i = 0; i < 8; ++i) ge[i] = rl[i] >= x;
+                  for (int i = 0; i < CPL; ++i) msk |= (e[i] >= cut && e[i] > theta) ? (1u << i) : 0u;
+                  float* st = sm.stash[warp - 3] + lane * CPL;
 #pragma unroll
-                      for (int i = 7; i >= 1; --i) {
-                        rl[i] = ge[i] ? rl[i] : (ge[i - 1] ? x : rl[i - 1]);
-                        ri[i] = ge[i] ? ri[i] : (ge[i - 1] ? cb + c : ri[i - 1]);
-                      }
-                      rl[0] = ge[0] ? rl[0] : x;
-                      ri[0] = ge[0] ? ri[0] : cb + c;
-                      if (cnt < K) ++cnt;
-                      if (cnt == K) {
-                        float kth = rl[0];
+                  for (int i = 0; i < CPL; i += 4)
+                    *reinterpret_cast<float4*>(st + i) = make_float4(e[i], e[i + 1], e[i + 2], e[i + 3]);
+                  while (msk) {
+                    const int i = __ffs(msk) - 1;
+                    msk &= msk - 1;
+                    const float x = st[i];
+                    if (!(x > theta) || x < cut) continue;
+                    const int32_t col = cb + cg + i;
+                    bool ge[8];
 #pragma unroll
-                        for (int i = 1; i < 8; ++i) kth = (i == K - 1) ? rl[i] : kth;
-                        theta = kth;
-                        cut = fmaxf(cut, theta);
-                        atomicMax(reinterpret_cast<int*>(&sm.cut[qi]), __float_as_int(theta));
-                      }
+                    for (int u = 0; u < 8; ++u) ge[u] = rl[u] >= x;
+#pragma unroll
+                    for (int u = 7; u >= 1; --u) {
+                      rl[u] = ge[u] ? rl[u] : (ge[u - 1] ? x : rl[u - 1]);
+                      ri[u] = ge[u] ? ri[u] : (ge[u - 1] ? col : ri[u - 1]);
+                    }
+                    rl[0] = ge[0] ? rl[0] : x;
+                    ri[0] = ge[0] ? ri[0] : col;
+                    if (cnt < K) ++cnt;
+                    if (cnt == K) {
+                      float kth = rl[0];
+#pragma unroll
+                      for (int u = 1; u < 8; ++u) kth = (u == K - 1) ? rl[u] : kth;
+                      theta = kth;
+                      cut = fmaxf(cut, theta);
+                      atomicMax(reinterpret_cast<int*>(&sm.cut[qi]), __float_as_int(theta));
                     }
                   }
                 }
               } else {
-                if (g == 0) {
-                  float cut = fmaxf(theta, sm.cut[qi]);
-                  if (bmax >= cut) {
-                    float* st = sm.stash[warp - 3][qi % (32 / G)];
+                float pv[32];
+                float bmax = -INFINITY;
+                if (__all_sync(0xffffffffu, elo <= 0 && ehi >= 31)) {
 #pragma unroll
-                    for (int c = 0; c < 32; c += 4)
-                      *reinterpret_cast<float4*>(st + c) = make_float4(pv[c], pv[c + 1], pv[c + 2], pv[c + 3]);
-                    for (int c = 0; c < 32; ++c) {
-                      const float pc = st[c];
-                      if (pc < cut || (cnt == K && !(pc > theta))) continue;
-                      int pos = cnt < K ? cnt : K - 1;
-                      while (pos > 0 && ts[pos - 1] < pc) {
-                        ts[pos] = ts[pos - 1];
-                        tix[pos] = tix[pos - 1];
-                        --pos;
+                  for (int c = 0; c < 32; ++c) {
+                    float p = ptx::ex2(fmaf(__uint_as_float(v[c]), sc, -lse));
+#pragma unroll
+                    for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                    pv[c] = p;
+                  }
+                } else {
+#pragma unroll
+                  for (int c = 0; c < 32; ++c) {
+                    float p = c < nv ? ptx::ex2(fmaf(__uint_as_float(v[c]), sc, -lse)) : 0.0f;
+#pragma unroll
+                    for (int o = 1; o < G; o <<= 1) p += __shfl_xor_sync(0xffffffffu, p, o);
+                    pv[c] = (c >= elo && c <= ehi) ? p : -INFINITY;  // Top-K runs over E only
+                  }
+                }
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) bmax = fmaxf(bmax, fmaxf(pv[c], pv[c + 1]));
+                // the group's first lane keeps this slice's best K of its query
+                // sorted (higher score first; a later column never passes an
+                // equal score, so ties keep the lower block index).  A column
+                // below the query's shared cut -- the largest K-th best of any
+                // slice's full list, hence at most the final K-th best -- cannot
+                // be kept; equal ones are, and the merge orders ties by index.
+                if constexpr (KR <= 8) {
+                  // columns above the cut, one bit each; then sorted insertion of
+                  // each (select-shift over the register list, ties keeping the
+                  // earlier column)
+                  if (g == 0) {
+                    float cut = fmaxf(theta, sm.cut[qi]);
+                    if (bmax >= cut) {
+                      uint32_t msk = 0;
+#pragma unroll
+                      for (int c = 0; c < 32; ++c) msk |= (pv[c] >= cut && pv[c] > theta) ? (1u << c) : 0u;
+                      float* st = sm.stash[warp - 3] + (qi % (32 / G)) * 32;
+#pragma unroll
+                      for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4*>(st + c) = make_float4(pv[c], pv[c + 1], pv[c + 2], pv[c + 3]);
+                      while (msk) {
+                        const int c = __ffs(msk) - 1;
+                        msk &= msk - 1;
+                        const float x = st[c];
+                        if (!(x > theta) || x < cut) continue;
+                        bool ge[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) ge[i] = rl[i] >= x;
+#pragma unroll
+                        for (int i = 7; i >= 1; --i) {
+                          rl[i] = ge[i] ? rl[i] : (ge[i - 1] ? x : rl[i - 1]);
+                          ri[i] = ge[i] ? ri[i] : (ge[i - 1] ? cb + c : ri[i - 1]);
+                        }
+                        rl[0] = ge[0] ? rl[0] : x;
+                        ri[0] = ge[0] ? ri[0] : cb + c;
+                        if (cnt < K) ++cnt;
+                        if (cnt == K) {
+                          float kth = rl[0];
+#pragma unroll
+                          for (int i = 1; i < 8; ++i) kth = (i == K - 1) ? rl[i] : kth;
+                          theta = kth;
+                          cut = fmaxf(cut, theta);
+                          atomicMax(reinterpret_cast<int*>(&sm.cut[qi]), __float_as_int(theta));
+                        }
                       }
-                      ts[pos] = pc;
-                      tix[pos] = cb + c;
-                      if (cnt < K) ++cnt;
-                      if (cnt == K) {
-                        theta = ts[K - 1];
-                        cut = fmaxf(cut, theta);
-                        atomicMax(reinterpret_cast<int*>(&sm.cut[qi]), __float_as_int(theta));
+                    }
+                  }
+                } else {
+                  if (g == 0) {
+                    float cut = fmaxf(theta, sm.cut[qi]);
+                    if (bmax >= cut) {
+                      float* st = sm.stash[warp - 3] + (qi % (32 / G)) * 32;
+#pragma unroll
+                      for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4*>(st + c) = make_float4(pv[c], pv[c + 1], pv[c + 2], pv[c + 3]);
+                      for (int c = 0; c < 32; ++c) {
+                        const float pc = st[c];
+                        if (pc < cut || (cnt == K && !(pc > theta))) continue;
+                        int pos = cnt < K ? cnt : K - 1;
+                        while (pos > 0 && ts[pos - 1] < pc) {
+                          ts[pos] = ts[pos - 1];
+                          tix[pos] = tix[pos - 1];
+                          --pos;
+                        }
+                        ts[pos] = pc;
+                        tix[pos] = cb + c;
+                        if (cnt < K) ++cnt;
+                        if (cnt == K) {
+                          theta = ts[K - 1];
+                          cut = fmaxf(cut, theta);
+                          atomicMax(reinterpret_cast<int*>(&sm.cut[qi]), __float_as_int(theta));
+                        }
                       }
                     }
                   }
                 }
+            
               }
             }
             ptx::tc_fence_before();
@@ -458,7 +611,10 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
         }
       }
       if (!ok) break;
-      if constexpr (KR <= 8) {
+      if constexpr (kLaneLists) {
+        // the slice's best 8 of the query, from its G lanes' lists
+#pragma unroll
+        for (int o = 1; o < G; o <<= 1) flat_merge8_xor(rl, ri, o);
         if (g == 0) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -466,25 +622,72 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
             tix[i] = ri[i];
           }
         }
+      } else {
+        if constexpr (KR <= 8) {
+          if (g == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              ts[i] = rl[i];
+              tix[i] = ri[i];
+            }
+          }
+        }
+        if (g == 0) sm.top_n[sl][r] = cnt;
       }
-      if (g == 0) sm.top_n[sl][qi] = cnt;
       if (!rendezvous()) { ok = false; *abort = 1; break; }  // every slice's list is complete
       // output (slice-0 warps): the best K of the S sorted lists (ties to the
       // lower block index), ascending, together with F
-      if (sl == 0 && g == 0 && t < pr.N) {
+      if constexpr (kLaneLists) {
+        if (sl == 0) {  // warp-uniform
+          // lane g takes slice g's list (S == G here); the G lanes merge them
+          float ml[8];
+          int32_t mi[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            ml[i] = sm.top_s[g][qi][i];
+            mi[i] = sm.top_i[g][qi][i];
+          }
+#pragma unroll
+          for (int o = 1; o < G; o <<= 1) flat_merge8_xor(ml, mi, o);
+          // the best K (entries past K and empty ones sort last), block order
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            if (i >= K) {
+              ml[i] = -INFINITY;
+              mi[i] = -1;
+            }
+          flat_sort8_by_block(ml, mi);
+          if (g == 0 && t < pr.N) {
+            const int64_t qrow = bh * pr.N + t;
+            int32_t* oi = out_idx + qrow * W;
+            float* os = out_score ? out_score + qrow * W : nullptr;
+            int pos = 0;
+            oi[pos] = 0; if (os) os[pos] = INFINITY; ++pos;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (mi[i] >= 0) { oi[pos] = mi[i]; if (os) os[pos] = ml[i]; ++pos; }
+            if (qb - 1 > 0) { oi[pos] = (int32_t)(qb - 1); if (os) os[pos] = INFINITY; ++pos; }
+            if (qb > 0) { oi[pos] = (int32_t)qb; if (os) os[pos] = INFINITY; ++pos; }
+            for (; pos < W; ++pos) { oi[pos] = -1; if (os) os[pos] = -INFINITY; }
+          }
+        }
+      } else if (sl == 0 && g == 0 && t < pr.N) {
         float bs[kFCap];
         int32_t bi[kFCap];
-        int head[S];
+        // lists (u, l): slice u, lane l of the query (one list per query
+        // when LG = 1); entries at top_s[u][qi][8 l ...]
+        int head[S * LG];
 #pragma unroll
-        for (int u = 0; u < S; ++u) head[u] = 0;
+        for (int u = 0; u < S * LG; ++u) head[u] = 0;
         int n = 0;
         for (; n < K; ++n) {
           int bu = -1;
 #pragma unroll
-          for (int u = 0; u < S; ++u) {
-            if (head[u] < sm.top_n[u][qi]) {
-              const float su = sm.top_s[u][qi][head[u]];
-              const int32_t iu = sm.top_i[u][qi][head[u]];
+          for (int u = 0; u < S * LG; ++u) {
+            const int us = u / LG, ul = u % LG;
+            if (head[u] < sm.top_n[us][qi * G + ul]) {
+              const float su = sm.top_s[us][qi][ul * 8 + head[u]];
+              const int32_t iu = sm.top_i[us][qi][ul * 8 + head[u]];
               if (bu < 0 || su > bs[n] || (su == bs[n] && iu < bi[n])) {
                 bu = u;
                 bs[n] = su;
@@ -494,7 +697,7 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
           }
           if (bu < 0) break;
 #pragma unroll
-          for (int u = 0; u < S; ++u) head[u] += (u == bu) ? 1 : 0;
+          for (int u = 0; u < S * LG; ++u) head[u] += (u == bu) ? 1 : 0;
         }
         // insertion sort of the kept entries by block index
         for (int u = 1; u < n; ++u) {
