@@ -42,6 +42,7 @@ constexpr int kTileKeys = 128;  // MMA N: leaves 2p and 2p+1
 constexpr int kStagesA = 4;  // query-row tiles in flight
 constexpr int kStagesB = 3;  // key tiles
 constexpr int kAcc = 4;      // TMEM accumulators (4 x 128 columns)
+static_assert(kAcc == kStagesA, "a query-row stage is released by its tile's accumulator barrier");
 constexpr int kGroup = 4;
 constexpr int kProdWarps = 8;          // warps 0-7 gather 16 query-head rows each
 constexpr int kProdRows = kTileRows / kProdWarps;
@@ -68,7 +69,7 @@ template <int D>
 struct LeafTcSmem {
   uint8_t a[kStagesA][kTileRows * D * 2];
   uint8_t b[kStagesB][kTileKeys * D * 2];
-  uint64_t full_a[kStagesA], empty_a[kStagesA], full_b[kStagesB], empty_b[kStagesB];
+  uint64_t full_a[kStagesA], full_b[kStagesB], empty_b[kStagesB];
   uint64_t tfull[kAcc], tempty[kAcc], done;
   uint32_t tmem_base;
   int32_t abort;
@@ -303,7 +304,6 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesA; ++s) {
       ptx::mbar_init(ptx::smem_u32(&sm.full_a[s]), 32 * kProdWarps);
-      ptx::mbar_init(ptx::smem_u32(&sm.empty_a[s]), 1);
     }
     for (int s = 0; s < kStagesB; ++s) {
       ptx::mbar_init(ptx::smem_u32(&sm.full_b[s]), 1);
@@ -377,7 +377,10 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
       const int bh = info.x;
       const int b = bh / (int)pr.Hkv, h = bh - b * (int)pr.Hkv;
       const int sa = it % kStagesA, use = it / kStagesA;
-      ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.empty_a[sa]), (use & 1) ^ 1, abort, kWaitLimitNs);
+      // the stage is free once the MMAs of its previous tile have completed,
+      // which is when that tile's accumulator is announced full (one stage per
+      // accumulator)
+      ok = ptx::mbar_wait_bounded(ptx::smem_u32(&sm.tfull[sa]), (use & 1) ^ 1, abort, kWaitLimitNs);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; return false; }
       // gather this warp's query-head rows
       const uint32_t abase = ptx::smem_u32(sm.a[sa]) + dlane;
@@ -466,16 +469,21 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
     if (lane == 0) {
       int it = 0, bcount = 0, last_bh = -1, last_p = -1, sb = 0;
       bool ok = true;
-      // descriptors two tiles ahead (three rotating slots, as in the producers)
+      // descriptors four tiles ahead (five rotating slots: a prefetched value
+      // is never copied between registers, which would wait for it)
       const int4 kNoTile = make_int4(-1, 0, 0, 0);
       TileIter ti(T), ahead(T);
+      int4 d0 = ti.valid() ? tile_info[ti.i] : kNoTile, d1, d2, d3, d4;
       if (ahead.valid()) ahead.next();
-      int4 d0 = ti.valid() ? tile_info[ti.i] : kNoTile;
-      int4 d1 = ahead.valid() ? tile_info[ahead.i] : kNoTile, d2;
-      auto step = [&](const int4& info, const int4& ninfo, int4& slot2) -> bool {
+      d1 = ahead.valid() ? tile_info[ahead.i] : kNoTile;
+      if (ahead.valid()) ahead.next();
+      d2 = ahead.valid() ? tile_info[ahead.i] : kNoTile;
+      if (ahead.valid()) ahead.next();
+      d3 = ahead.valid() ? tile_info[ahead.i] : kNoTile;
+      auto step = [&](const int4& info, const int4& ninfo, int4& slot4) -> bool {
         if (!ti.valid()) return false;
         if (ahead.valid()) ahead.next();
-        slot2 = ahead.valid() ? tile_info[ahead.i] : kNoTile;
+        slot4 = ahead.valid() ? tile_info[ahead.i] : kNoTile;
         const int sa = it % kStagesA, use = it / kStagesA;
         const int acc = it % kAcc, uacc = it / kAcc;
         if (info.x != last_bh || info.w != last_p) {
@@ -500,14 +508,13 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
           const uint32_t off = (k >> 2) * kHalf + (k & 3) * 32;
           ptx::mma_bf16(d, ptx::desc_sw128(a0 + off), ptx::desc_sw128(b0 + off), kIdesc, k > 0 ? 1u : 0u);
         }
-        ptx::mma_commit(ptx::smem_u32(&sm.empty_a[sa]));
         ptx::mma_commit(ptx::smem_u32(&sm.tfull[acc]));
         if (ninfo.x != info.x || ninfo.w != info.w) ptx::mma_commit(ptx::smem_u32(&sm.empty_b[sb]));
         ++it;
         ti.next();
         return true;
       };
-      while (step(d0, d1, d2) && step(d1, d2, d0) && step(d2, d0, d1)) {
+      while (step(d0, d1, d4) && step(d1, d2, d0) && step(d2, d3, d1) && step(d3, d4, d2) && step(d4, d0, d3)) {
       }
       if (!ok) *abort = 1;
       // every MMA has finished before TMEM is released
