@@ -34,10 +34,13 @@
 // A warp walks two queries (16 lanes of bookkeeping each).  Per level and
 // query, every candidate needs one DD row (and, at the start level, its MU
 // row); eight rows at a time are multiplied against the query's four head
-// vectors as m16n8k16 MMAs with A = 8 nodes x the two halves of the d dims
-// and B = the 4 heads x the two halves, of which the two half-diagonal
-// blocks are used.  Rows are stored half-interleaved so the eight lanes of a
-// node read one whole 128-byte line per load.
+// vectors as m16n8k16 MMAs with A = the 8 rows' first halves (MMA rows 0-7)
+// and second halves (rows 8-15) and B = the 4 heads x the two halves, of which
+// the two half-diagonal blocks are used.  Rows are stored so that a lane's A
+// fragments of two consecutive MMAs are one 32-byte load (the four lanes of a
+// row read one whole 128-byte line per load, and no fragment register is
+// moved before its MMA), and the lane of (row r, head h) ends with that row's
+// whole dot with head h.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -63,11 +66,29 @@ __device__ __forceinline__ int row_exponent(float mx) {
   return min(126, max(-126, 14 - E));
 }
 
-// Position of dim c within a stored row of D elements: 128-byte line bb holds
-// dims [32 bb, 32 bb + 32) of the first half, then the same dims of the second.
+// Position (in elements) of dim c within a stored row of D elements.  For
+// k-step kk (16 dims of each half, hd = D / 2) and quad thread t, the f16 pairs
+//   {c0, c0+1}, {hd+c0, hd+c0+1}, {c0+8, c0+9}, {hd+c0+8, hd+c0+9},  c0 = 16 kk + 2 t,
+// are that thread's A fragment (a0, a1, a2, a3) of the MMA in which row r
+// holds the first half of node r and row r + 8 its second half.  The 16-byte
+// fragments of k-steps 2m and 2m + 1 of thread t are adjacent, at byte
+// 128 m + 32 t: one 32-byte load per thread and k-step pair, and the quad's
+// four loads cover one whole 128-byte line.
 __device__ __forceinline__ int row_pos(int c, int D) {
   const int hd = D / 2;
-  return ((c % hd) / 32) * 64 + (c / hd) * 32 + (c & 31);
+  const int s = c / hd, cc = c % hd;
+  const int kk = cc >> 4, kp = cc & 15;
+  const int t = (kp & 7) >> 1;
+  const int word = ((kp >> 3) << 1) | s;
+  const int chunk = ((kk >> 1) * 4 + t) * 2 + (kk & 1);
+  return (chunk * 4 + word) * 2 + (kp & 1);
+}
+
+// 32 bytes from global memory (read-only path), as two 16-byte fragments.
+__device__ __forceinline__ void ldg_frag2(const void* p, uint4& a, uint4& b) {
+  asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+               : "l"(p));
 }
 
 __device__ __forceinline__ uint32_t orderable_key_h(float f) {
@@ -100,13 +121,12 @@ __device__ __forceinline__ float comp4(const float4& v, int g) {
   return g == 0 ? v.x : (g == 1 ? v.y : (g == 2 ? v.z : v.w));
 }
 
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ float ex2_fast(float x) {
@@ -221,62 +241,39 @@ struct HaarView {
 // and query scales not yet applied) go to sm[u].y[slot]; with kAdd they are
 // added to it instead, and only the groups of eight slots whose bit is set in
 // gmask (one bit per group, both queries) are done: the residual pass.
+// For a group of eight slots, lane (r, t) loads its A fragments from slot r's
+// row (one 16-byte chunk per k-step) and, after the k-steps, holds
+// D[r][2t] + D[r + 8][2t + 1]: the dot of slot r's row with head t.
 template <int D, int NC, bool kAdd>
 __device__ __forceinline__ void haar_pass(HaarQPad<NC>* smw, const int (&cur)[2], const uint16_t* __restrict__ rows,
                                           const int64_t (&pbase)[2], int64_t rowoff, const int (&nw)[2],
-                                          uint32_t gmask, const uint32_t (&bq)[2][D / 64][4], int lane) {
-  constexpr int NB = D / 64;
+                                          uint32_t gmask, const uint32_t (&bq)[2][D / 32][2], int lane) {
+  constexpr int NK = D / 32;
   const int grp = lane >> 2, tig = lane & 3;
   const int nmax = max(nw[0], nw[1]);
-  const int64_t loff = rowoff * D + (grp & 1) * 32 + 8 * tig;
-  const bool roleA = !(grp & 1) && tig < 2, roleB = (grp & 1) && tig >= 2;
+  const int64_t loff = rowoff * D + 16 * tig;
 #pragma unroll
   for (int r0 = 0; r0 < NC; r0 += 8) {
     if (r0 >= nmax) break;
     if (kAdd && !((gmask >> (r0 / 8)) & 1u)) continue;  // warp-uniform
-    uint32_t ro[2][2];
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int w = r0 + 4 * rr + (grp >> 1);
-        ro[u][rr] = (uint32_t)(w < nw[u] ? smw[u].cand[cur[u]][w] : 0) * (uint32_t)D;
-      }
-    uint4 hv[2][2][NB];
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb)
-          hv[u][rr][bb] = __ldg(reinterpret_cast<const uint4*>(rows + pbase[u] + loff + ro[u][rr] + 64 * bb));
-    float d[2][4];
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) d[u][e] = 0.0f;
-#pragma unroll
-    for (int bb = 0; bb < NB; ++bb)
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const uint4 h0 = hv[u][0][bb], h1 = hv[u][1][bb];
-        mma_f16_16816(d[u], h0.x, h1.x, h0.y, h1.y, bq[u][bb][0], bq[u][bb][1]);
-        mma_f16_16816(d[u], h0.z, h1.z, h0.w, h1.w, bq[u][bb][2], bq[u][bb][3]);
-      }
+    const int w = r0 + grp;
+    uint4 a[2][NK];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      // add the two halves: partner lane = lane ^ 6 (group ^ 1, t ^ 2)
-      const float x0 = __shfl_xor_sync(0xffffffffu, roleA ? d[u][2] : d[u][0], 6);
-      const float x1 = __shfl_xor_sync(0xffffffffu, roleA ? d[u][3] : d[u][1], 6);
-      const int w = r0 + (roleA ? 0 : 4) + (grp >> 1);
-      if ((roleA || roleB) && w < nw[u]) {
-        float2 v = roleA ? make_float2(d[u][0] + x0, d[u][1] + x1) : make_float2(d[u][2] + x0, d[u][3] + x1);
-        float2* dst = reinterpret_cast<float2*>(reinterpret_cast<float*>(&smw[u].y[w]) + 2 * (tig & 1));
-        if (kAdd) {
-          const float2 o = *dst;
-          v = make_float2(o.x + v.x, o.y + v.y);
-        }
-        *dst = v;
+      const uint32_t ro = (uint32_t)(w < nw[u] ? smw[u].cand[cur[u]][w] : 0) * (uint32_t)D;
+      const uint16_t* rp = rows + pbase[u] + loff + ro;
+#pragma unroll
+      for (int m = 0; m < NK / 2; ++m) ldg_frag2(rp + 64 * m, a[u][2 * m], a[u][2 * m + 1]);
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int kk = 0; kk < NK; ++kk) mma_f16_16816(d, a[u][kk], bq[u][kk][0], bq[u][kk][1]);
+      if (w < nw[u]) {
+        float* dst = reinterpret_cast<float*>(&smw[u].y[w]) + tig;
+        const float v = d[0] + d[3];
+        *dst = kAdd ? *dst + v : v;
       }
     }
   }
@@ -307,7 +304,7 @@ __global__ void __launch_bounds__(WARPS * 32, (KM <= 8 ? 24 : 16) / WARPS)
   constexpr int G = 4;
   constexpr int NC = 2 * KM;
   constexpr int CPL = NC / 16;
-  constexpr int NB = D / 64;
+  constexpr int NK = D / 32;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   HaarQPad<NC>& sm = reinterpret_cast<HaarQPad<NC>*>(smem_raw)[threadIdx.x / 16];
   HaarQPad<NC>* smw = reinterpret_cast<HaarQPad<NC>*>(smem_raw) + (threadIdx.x / 32) * 2;
@@ -349,11 +346,12 @@ __global__ void __launch_bounds__(WARPS * 32, (KM <= 8 ? 24 : 16) / WARPS)
   const int l0w = max(l0, l0o);
   if (l0w == 0) return;  // warp-uniform
 
-  // B fragments of both queries: column grp = (head grp % 4, half grp / 4),
-  // converted to fp16 with a power-of-two scale per query (exact for bf16
-  // inputs in range); per-query head norms for the residual bound.
+  // B fragments of both queries: lane (r, t) holds column r = 2 h + s (half s
+  // of head h) at k = 2t, 2t+1 and 2t+8, 2t+9 of every k-step, converted to
+  // fp16 with one power-of-two scale per query (exact for bf16 inputs in
+  // range); per-query head norms for the residual bound.
   const uint32_t qw = (blockIdx.x * WARPS + threadIdx.x / 32) * 2;
-  uint32_t bq[2][NB][4];
+  uint32_t bq[2][NK][2];
   int64_t pbase[2], mbase[2];
   float qfac[2], bfac[2];
 #pragma unroll
@@ -361,40 +359,41 @@ __global__ void __launch_bounds__(WARPS * 32, (KM <= 8 ? 24 : 16) / WARPS)
     const uint32_t qu = min(qw + u, nq - 1);
     const uint32_t tu = qu % N32, bhu = qu / N32;
     const uint32_t Hkv = (uint32_t)pr.Hkv;
-    const int64_t qrow = ((int64_t)((bhu / Hkv) * (uint32_t)pr.Hq + (bhu % Hkv) * G + (grp & 3)) * pr.N + tu) * D +
-                         (grp >> 2) * (D / 2) + 8 * tig;
-    float f[NB][8];
+    const int64_t head = (int64_t)((bhu / Hkv) * (uint32_t)pr.Hq + (bhu % Hkv) * G + (grp >> 1));
+    const uint16_t* qp = q + (head * pr.N + tu) * D + (grp & 1) * (D / 2) + 2 * tig;
+    float f[NK][4];
     float mx = 0.0f, ss = 0.0f;
 #pragma unroll
-    for (int bb = 0; bb < NB; ++bb) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(q + qrow + 32 * bb));
-      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    for (int kk = 0; kk < NK; ++kk) {
+      const uint32_t w0 = __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk));
+      const uint32_t w1 = __ldg(reinterpret_cast<const uint32_t*>(qp + 16 * kk + 8));
+      f[kk][0] = __uint_as_float(w0 << 16);
+      f[kk][1] = __uint_as_float(w0 & 0xffff0000u);
+      f[kk][2] = __uint_as_float(w1 << 16);
+      f[kk][3] = __uint_as_float(w1 & 0xffff0000u);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        f[bb][2 * e] = __uint_as_float(wv[e] << 16);
-        f[bb][2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        mx = fmaxf(mx, fabsf(f[bb][e]));
-        ss = fmaf(f[bb][e], f[bb][e], ss);
+        mx = fmaxf(mx, fabsf(f[kk][e]));
+        ss = fmaf(f[kk][e], f[kk][e], ss);
       }
     }
     mx = warp_max(mx);
     const int e = row_exponent(mx);
     const float sc = pow2f(e);
 #pragma unroll
-    for (int bb = 0; bb < NB; ++bb)
-#pragma unroll
-      for (int w = 0; w < 4; ++w) bq[u][bb][w] = pack_f16x2(f[bb][2 * w] * sc, f[bb][2 * w + 1] * sc);
+    for (int kk = 0; kk < NK; ++kk) {
+      bq[u][kk][0] = pack_f16x2(f[kk][0] * sc, f[kk][1] * sc);
+      bq[u][kk][1] = pack_f16x2(f[kk][2] * sc, f[kk][3] * sc);
+    }
     qfac[u] = pow2f(-e) * pr.scale2;
-    // |q_h|^2: lanes of head h are grp in {h, h + 4}, any tig
+    // |q_h|^2 over the lanes of head h (quad threads and both halves), then
+    // the sum of the four heads' norms
     ss += __shfl_xor_sync(0xffffffffu, ss, 1);
     ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+    ss += __shfl_xor_sync(0xffffffffu, ss, 4);
     float hn = sqrtf(ss);
-    hn += __shfl_xor_sync(0xffffffffu, hn, 4);
     hn += __shfl_xor_sync(0xffffffffu, hn, 8);
+    hn += __shfl_xor_sync(0xffffffffu, hn, 16);
     bfac[u] = hn * pr.scale2;  // bound per unit of residual norm: sum over heads of s |q_h| (log2 units)
     pbase[u] = (int64_t)bhu * hv.P2 * D;
     mbase[u] = (int64_t)bhu * hv.P2;
