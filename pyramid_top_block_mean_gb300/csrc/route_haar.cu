@@ -237,7 +237,8 @@ struct HaarView {
 };
 
 // Dots of fp16 rows of the candidates of both queries of the warp: query
-// u's candidates are smw[u].cand[cur[u]][0, nw[u]).  The raw MMA results (row
+// u's candidates are slots [0, nw[u]), slot i held by lane 16 u + i % 16 as
+// its cv[i / 16].  The raw MMA results (row
 // and query scales not yet applied) go to sm[u].y[slot]; with kAdd they are
 // added to it instead, and only the groups of eight slots whose bit is set in
 // gmask (one bit per group, both queries) are done: the residual pass.
@@ -245,7 +246,7 @@ struct HaarView {
 // row (one 16-byte chunk per k-step) and, after the k-steps, holds
 // D[r][2t] + D[r + 8][2t + 1]: the dot of slot r's row with head t.
 template <int D, int NC, bool kAdd>
-__device__ __forceinline__ void haar_pass(HaarQPad<NC>* smw, const int (&cur)[2], const uint16_t* __restrict__ rows,
+__device__ __forceinline__ void haar_pass(HaarQPad<NC>* smw, const int (&cv)[NC / 16], const uint16_t* __restrict__ rows,
                                           const int64_t (&pbase)[2], int64_t rowoff, const int (&nw)[2],
                                           uint32_t gmask, const uint32_t (&bq)[2][D / 32][2], int lane) {
   constexpr int NK = D / 32;
@@ -260,7 +261,9 @@ __device__ __forceinline__ void haar_pass(HaarQPad<NC>* smw, const int (&cur)[2]
     uint4 a[2][NK];
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
-      const uint32_t ro = (uint32_t)(w < nw[u] ? smw[u].cand[cur[u]][w] : 0) * (uint32_t)D;
+      // slot w of query u is lane 16 u + w % 16's candidate w / 16 (uniform per group)
+      const int node = __shfl_sync(0xffffffffu, cv[r0 >> 4], 16 * u + (w & 15));
+      const uint32_t ro = (uint32_t)(w < nw[u] ? node : 0) * (uint32_t)D;
       const uint16_t* rp = rows + pbase[u] + loff + ro;
 #pragma unroll
       for (int m = 0; m < NK / 2; ++m) ldg_frag2(rp + 64 * m, a[u][2 * m], a[u][2 * m + 1]);
@@ -427,20 +430,19 @@ __global__ void __launch_bounds__(WARPS * 32, (KM <= 8 ? 24 : 16) / WARPS)
       xv[sl] = (valid && !start) ? sm.x[cur][i] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     const int nwu[2] = {__shfl_sync(0xffffffffu, ncur, 0), __shfl_sync(0xffffffffu, ncur, 16)};
-    const int curu[2] = {__shfl_sync(0xffffffffu, cur, 0), __shfl_sync(0xffffffffu, cur, 16)};
 
     // start level: the candidates' own dots from their MU rows (hi pass,
     // then the residual pass for the groups whose rounding bound is too wide)
     const unsigned st_b = __ballot_sync(0xffffffffu, start);
     if (st_b) {
       const int ns[2] = {(st_b & 1u) ? nwu[0] : 0, (st_b >> 16) ? nwu[1] : 0};
-      haar_pass<D, NC, false>(smw, curu, hv.mu_hi, pbase, rowoff, ns, 0u, bq, lane);
+      haar_pass<D, NC, false>(smw, cv, hv.mu_hi, pbase, rowoff, ns, 0u, bq, lane);
       float bnd[CPL];
 #pragma unroll
       for (int sl = 0; sl < CPL; ++sl) bnd[sl] = start ? mybf * mt[sl].y : 0.0f;
       const uint32_t gm = lo_groups<CPL>(bnd, ncur, ll);
       __syncwarp();
-      if (gm) haar_pass<D, NC, true>(smw, curu, hv.mu_lo, pbase, rowoff, ns, gm, bq, lane);
+      if (gm) haar_pass<D, NC, true>(smw, cv, hv.mu_lo, pbase, rowoff, ns, gm, bq, lane);
       __syncwarp();
 #pragma unroll
       for (int sl = 0; sl < CPL; ++sl) {
@@ -455,14 +457,14 @@ __global__ void __launch_bounds__(WARPS * 32, (KM <= 8 ? 24 : 16) / WARPS)
     }
 
     // every level: the candidates' DD rows give both children's dots
-    haar_pass<D, NC, false>(smw, curu, hv.dd_hi, pbase, rowoff, nwu, 0u, bq, lane);
+    haar_pass<D, NC, false>(smw, cv, hv.dd_hi, pbase, rowoff, nwu, 0u, bq, lane);
     {
       float bnd[CPL];
 #pragma unroll
       for (int sl = 0; sl < CPL; ++sl) bnd[sl] = mybf * mt[sl].w;
       const uint32_t gm = lo_groups<CPL>(bnd, ncur, ll);
       __syncwarp();
-      if (gm) haar_pass<D, NC, true>(smw, curu, hv.dd_lo, pbase, rowoff, nwu, gm, bq, lane);
+      if (gm) haar_pass<D, NC, true>(smw, cv, hv.dd_lo, pbase, rowoff, nwu, gm, bq, lane);
     }
     __syncwarp();
 
