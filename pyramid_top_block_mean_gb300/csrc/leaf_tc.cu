@@ -700,6 +700,18 @@ __global__ void __launch_bounds__(256) finalize_small_kernel(Prob pr, const int3
       const float v = val[c] ? leaf_score[(qi * K + slot) * 2 + (c & 1)] : -INFINITY;
       sc[c] = v != v ? -INFINITY : v;  // NaN ranks as -inf (a total order)
     }
+    // rank keys: the orderable score with its low 4 bits replaced by the
+    // reversed candidate slot, so keys are distinct and, among scores equal to
+    // 2^-19 relative (far inside the 1e-3 tie margin), the lower slot -- the
+    // lower leaf, candidates running in ascending leaf order -- ranks first;
+    // candidates outside E get key 0 and never rank above a valid one
+    uint32_t key[NCM];
+#pragma unroll
+    for (int c = 0; c < NCM; ++c) {
+      const uint32_t u = __float_as_uint(sc[c]);
+      const uint32_t ok = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+      key[c] = val[c] ? ((ok & ~15u) | (uint32_t)(15 - c)) : 0u;
+    }
     int32_t* oi = si + threadIdx.x * W;
     float* os = ss + threadIdx.x * W;
     int pos = 1;
@@ -707,7 +719,7 @@ __global__ void __launch_bounds__(256) finalize_small_kernel(Prob pr, const int3
     for (int c = 0; c < NCM; ++c) {
       int rank = 0;
 #pragma unroll
-      for (int j = 0; j < NCM; ++j) rank += (val[j] && beats(sc[j], lf[j], sc[c], lf[c])) ? 1 : 0;
+      for (int j = 0; j < NCM; ++j) rank += key[j] > key[c] ? 1 : 0;
       if (val[c] && rank < K && pos <= K) {  // candidates run in ascending leaf order
         oi[pos] = lf[c];
         os[pos] = sc[c] * kLn2;
