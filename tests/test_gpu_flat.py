@@ -76,8 +76,12 @@ def run_flat(pisa, s, q, k):
     return sel.out_idx.reshape(-1, W_).cpu().numpy(), sel.out_score.reshape(-1, W_).cpu().double().numpy()
 
 
+# Top-K list paths of the kernel: per-lane register lists (G <= 4, K <= 8;
+# G = 4, 1, 2 below), one register list per query (G = 8, K <= 8), lists in
+# shared memory (K > 8, with G = 8 and G = 4)
 @pytest.mark.parametrize("N,Hq,Hkv,d,K", [(4096, 16, 4, 128, 8), (4096 + 37, 4, 4, 128, 8),
-                                          (3000, 8, 1, 64, 32), (2500, 4, 2, 128, 5), (700, 2, 1, 64, 3)])
+                                          (3000, 8, 1, 64, 32), (2500, 4, 2, 128, 5), (700, 2, 1, 64, 3),
+                                          (2048 + 5, 8, 1, 128, 6), (3000, 16, 4, 64, 12)])
 def test_flat_matches_oracle(pisa, N, Hq, Hkv, d, K):
     s = W.Shape(B=2, N=N, Hq=Hq, Hkv=Hkv, d=d, K=K)
     q, k = W.iid(s, N % 89)
