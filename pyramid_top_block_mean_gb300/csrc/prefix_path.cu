@@ -22,86 +22,125 @@
 // q . (key sum) / n and q . mu_s.  ref is the finite-masked root summary (the
 // reference of the routing over difference rows) or zero.
 //
-// One warp per (sequence, key head, leaf block); its 64 queries share the
-// block's path siblings, which are staged in shared memory.  Lanes split
-// into G heads x 32/G dim groups: each lane keeps a running sum of the
-// block's keys over its dims, takes its partial dots with its head's query
-// row, and the dim groups reduce with shuffles.
+// One CTA of four warps per (sequence, key head, leaf block): the block's
+// queries are split among the warps (a quarter each, in order), which share
+// the block's path siblings staged in shared memory.  A warp starts its
+// running key sum from the sums of the earlier warps' key rows, exchanged
+// through shared memory, so the four walk their queries concurrently.
+// Lanes split into G heads x 32/G dim groups: each lane keeps the running
+// sum over its dims, takes its partial dots with its head's query row, and
+// the dim groups reduce with shuffles.
 #include "pisa_common.cuh"
 #include "pisa_internal.h"
 
 namespace pisa {
 
+constexpr int kPathWarps = 4;
+
+// Dim of a lane's j-th element: with at least four dims per lane, lane dg of
+// the DG lanes of a head owns the 4-dim chunks dg, dg + DG, dg + 2 DG, ...,
+// so that the DG lanes of a head read consecutive 16-byte chunks of a row
+// (coalesced in global memory, conflict-free in shared memory); with two, the
+// pair 2 dg, 2 dg + 1.
+template <int D, int DG, int DPL>
+__device__ __forceinline__ int path_dim(int dg, int j) {
+  if constexpr (DPL >= 4) return 4 * (dg + DG * (j >> 2)) + (j & 3);
+  return dg * DPL + j;
+}
+
+// Loads the lane's DPL elements of one row (bf16 or fp32) as floats.
+template <int D, int DG, int DPL>
+__device__ __forceinline__ void path_row(const char* row, bool bf16, size_t esz, int dg, float (&v)[DPL]) {
+  if constexpr (DPL >= 4) {
+#pragma unroll
+    for (int m = 0; m < DPL / 4; ++m) load4(row + (size_t)path_dim<D, DG, DPL>(dg, 4 * m) * esz, bf16, v + 4 * m);
+  } else {
+    load2(row + (size_t)path_dim<D, DG, DPL>(dg, 0) * esz, bf16, v);
+  }
+}
+
 template <int D, int G>
-__global__ void __launch_bounds__(128) path_dots_kernel(Prob pr, Pyr s, const void* __restrict__ q,
-                                                        const void* __restrict__ k,
-                                                        const float* __restrict__ pyr, int ref_root,
-                                                        float* __restrict__ out) {
+__global__ void __launch_bounds__(kPathWarps * 32) path_dots_kernel(Prob pr, Pyr s, const void* __restrict__ q,
+                                                                    const void* __restrict__ k,
+                                                                    const float* __restrict__ pyr, int ref_root,
+                                                                    float* __restrict__ out) {
   constexpr int DG = 32 / G;   // dim groups (lanes per head)
-  constexpr int DPL = D / DG;  // dims per lane: 4 .. 32
+  constexpr int DPL = D / DG;  // dims per lane: 2 .. 32
   extern __shared__ __align__(16) float sib_smem[];
   const int lane = threadIdx.x & 31, warp = threadIdx.x / 32;
   const int g = lane / DG, dg = lane % DG;
   const int L = s.L;
-  float* sib = sib_smem + (size_t)warp * L * D;  // [L][D]; row l - 1 for level l >= 2
+  float* sib = sib_smem;                           // [L][D]; row l - 1 for level l >= 2
+  float* ksw = sib + (size_t)L * D;                // [kPathWarps][D]: each warp's key-row sum
+  float* obuf = ksw + (size_t)kPathWarps * D;      // [kPathWarps][L][2][G]: a query's outputs
   const int64_t nblk = pr.B * pr.Hkv * s.nb;
-  const int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + warp;
-  if (w >= nblk) return;  // warp-uniform
+  const int64_t w = blockIdx.x;
+  if (w >= nblk) return;  // CTA-uniform
   const int64_t bh = w / s.nb, qb = w % s.nb;
   const int64_t b = bh / pr.Hkv, h = bh % pr.Hkv;
   const float* ph = pyr + bh * s.P * D;
   const bool bf16 = pr.dtype == PISA_BF16;
-  const int d0 = dg * DPL;
 
-  // reference row and the path's left siblings (complete nodes), lane's dims
-  float ref[DPL];
-#pragma unroll
-  for (int c = 0; c < DPL; ++c) {
-    const float r = ref_root ? ph[(s.P - 1) * D + d0 + c] : 0.0f;
-    ref[c] = isfinite(r) ? r : 0.0f;
-  }
+  // the path's left siblings (complete nodes), staged once per block
   for (int l = 2; l <= L; ++l) {
     const int64_t jc = qb >> (l - 2);
     if (jc & 1) {
       const float* row = ph + (s.off[l - 2] + jc - 1) * D;
-      for (int c = lane; c < D; c += 32) sib[(l - 1) * D + c] = row[c];
+      for (int c = threadIdx.x; c < D; c += kPathWarps * 32) sib[(l - 1) * D + c] = row[c];
     }
   }
-  __syncwarp();
-
-  float ks[DPL];
+  // reference row, lane's dims
+  float ref[DPL];
 #pragma unroll
-  for (int c = 0; c < DPL; ++c) ks[c] = 0.0f;
+  for (int j = 0; j < DPL; ++j) {
+    const float r = ref_root ? ph[(s.P - 1) * D + path_dim<D, DG, DPL>(dg, j)] : 0.0f;
+    ref[j] = isfinite(r) ? r : 0.0f;
+  }
+
   const int64_t t0 = qb * s.C;
   const int nt = (int)(s.N - t0 < s.C ? s.N - t0 : s.C);
+  const int per = (s.C + kPathWarps - 1) / kPathWarps;
+  const int r0 = min(nt, warp * per), r1 = min(nt, r0 + per);
   const size_t esz = bf16 ? 2 : 4;
-  const char* krow0 = reinterpret_cast<const char*>(k) + ((bh * s.N + t0) * D + d0) * esz;
-  const char* qrow0 = reinterpret_cast<const char*>(q) + (((b * pr.Hq + h * G + g) * pr.N + t0) * D + d0) * esz;
-  for (int r = 0; r < nt; ++r) {
+  const char* krow0 = reinterpret_cast<const char*>(k) + (bh * s.N + t0) * D * esz;
+  const char* qrow0 = reinterpret_cast<const char*>(q) + ((b * pr.Hq + h * G + g) * pr.N + t0) * D * esz;
+
+  // this warp's key rows summed, then the sums of the earlier warps' rows
+  float ks[DPL];
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) ks[j] = 0.0f;
+  for (int r = r0; r < r1; ++r) {
+    float kv[DPL];
+    path_row<D, DG, DPL>(krow0 + (size_t)r * D * esz, bf16, esz, dg, kv);
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) ks[j] += kv[j];
+  }
+  if (g == 0)
+#pragma unroll
+    for (int j = 0; j < DPL; ++j) ksw[warp * D + path_dim<D, DG, DPL>(dg, j)] = ks[j];
+  __syncthreads();
+#pragma unroll
+  for (int j = 0; j < DPL; ++j) {
+    float sacc = 0.0f;  // the earlier warps' sums, in warp order
+    for (int u = 0; u < warp; ++u) sacc += ksw[u * D + path_dim<D, DG, DPL>(dg, j)];
+    ks[j] = sacc;
+  }
+
+  float* ob = obuf + (size_t)warp * L * 2 * G;
+  const int nout = L * 2 * G;  // floats per query
+  for (int r = r0; r < r1; ++r) {
     const int64_t t = t0 + r;
-    float qv[DPL];
-    if constexpr (DPL >= 4) {
+    float qv[DPL], kv[DPL];
+    path_row<D, DG, DPL>(krow0 + (size_t)r * D * esz, bf16, esz, dg, kv);
+    path_row<D, DG, DPL>(qrow0 + (size_t)r * D * esz, bf16, esz, dg, qv);
 #pragma unroll
-      for (int c = 0; c < DPL; c += 4) {
-        float kv[4];
-        load4(krow0 + ((int64_t)r * D + c) * esz, bf16, kv);
-        load4(qrow0 + ((int64_t)r * D + c) * esz, bf16, qv + c);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) ks[c + e] += kv[e];
-      }
-    } else {
-      float kv[2];
-      load2(krow0 + (int64_t)r * D * esz, bf16, kv);
-      load2(qrow0 + (int64_t)r * D * esz, bf16, qv);
-      ks[0] += kv[0];
-      ks[1] += kv[1];
-    }
+    for (int j = 0; j < DPL; ++j) ks[j] += kv[j];
     // partial dots: q . key sum, q . ref, q . sibling of every odd level
     float dk = 0.0f, dr = 0.0f;
 #pragma unroll
-    for (int c = 0; c < DPL; ++c) {
-      dk = fmaf(qv[c], ks[c], dk);
-      dr = fmaf(qv[c], ref[c], dr);
+    for (int j = 0; j < DPL; ++j) {
+      dk = fmaf(qv[j], ks[j], dk);
+      dr = fmaf(qv[j], ref[j], dr);
     }
 #pragma unroll
     for (int o = DG / 2; o >= 1; o >>= 1) {
@@ -111,19 +150,18 @@ __global__ void __launch_bounds__(128) path_dots_kernel(Prob pr, Pyr s, const vo
     const float n1 = (float)(r + 1);
     float P = dk / n1 - dr;  // q . (prefix(1) - ref)
     float cnt = n1;
-    float* orow = out + (((w / s.nb) * s.N + t) * L) * 2 * G;  // [L][2][G] of this query
     if (dg == 0) {
-      orow[0 * 2 * G + 0 * G + g] = P * pr.scale2;
-      orow[0 * 2 * G + 1 * G + g] = 0.0f;
+      ob[0 * 2 * G + 0 * G + g] = P * pr.scale2;
+      ob[0 * 2 * G + 1 * G + g] = 0.0f;
     }
     for (int l = 2; l <= L; ++l) {
       const int64_t jc = qb >> (l - 2);
       float S = 0.0f;
       if (jc & 1) {  // warp-uniform
         float ds = 0.0f;
-        const float* srow = sib + (l - 1) * D + d0;
+        const float* srow = sib + (l - 1) * D;
 #pragma unroll
-        for (int c = 0; c < DPL; ++c) ds = fmaf(qv[c], srow[c], ds);
+        for (int j = 0; j < DPL; ++j) ds = fmaf(qv[j], srow[path_dim<D, DG, DPL>(dg, j)], ds);
 #pragma unroll
         for (int o = DG / 2; o >= 1; o >>= 1) ds += __shfl_xor_sync(0xffffffffu, ds, o);
         S = ds - dr;
@@ -132,10 +170,15 @@ __global__ void __launch_bounds__(128) path_dots_kernel(Prob pr, Pyr s, const vo
         cnt += ns;
       }
       if (dg == 0) {
-        orow[(l - 1) * 2 * G + 0 * G + g] = P * pr.scale2;
-        orow[(l - 1) * 2 * G + 1 * G + g] = S * pr.scale2;
+        ob[(l - 1) * 2 * G + 0 * G + g] = P * pr.scale2;
+        ob[(l - 1) * 2 * G + 1 * G + g] = S * pr.scale2;
       }
     }
+    // the query's [L][2][G] outputs leave as whole rows
+    __syncwarp();
+    float* orow = out + ((bh * s.N + t) * L) * 2 * G;
+    for (int e = lane; e < nout; e += 32) orow[e] = ob[e];
+    __syncwarp();
   }
 }
 
@@ -146,14 +189,13 @@ size_t path_dots_bytes(const Prob& pr, const Pyr& s) {
 template <int D, int G>
 static cudaError_t launch_path_t(const Prob& pr, const Pyr& s, const void* q, const void* k, const float* pyr,
                                  int ref_root, float* out, cudaStream_t st) {
-  constexpr int WARPS = 4;
-  const size_t smem = (size_t)WARPS * s.L * D * sizeof(float);
+  const size_t smem = ((size_t)(s.L + kPathWarps) * D + (size_t)kPathWarps * s.L * 2 * G) * sizeof(float);
   auto kern = path_dots_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t nblk = pr.B * pr.Hkv * s.nb;
   note_launch();
-  kern<<<(unsigned)ceil_div64(nblk, WARPS), WARPS * 32, smem, st>>>(pr, s, q, k, pyr, ref_root, out);
+  kern<<<(unsigned)nblk, kPathWarps * 32, smem, st>>>(pr, s, q, k, pyr, ref_root, out);
   return cudaGetLastError();
 }
 
