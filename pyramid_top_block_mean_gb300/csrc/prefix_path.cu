@@ -22,57 +22,34 @@
 // q . (key sum) / n and q . mu_s.  ref is the finite-masked root summary (the
 // reference of the routing over difference rows) or zero.
 //
-// One CTA of four warps per (sequence, key head, leaf block): the block's
-// queries are split among the warps (a quarter each, in order), which share
-// the block's path siblings staged in shared memory.  A warp starts its
-// running key sum from the sums of the earlier warps' key rows, exchanged
-// through shared memory, so the four walk their queries concurrently.
-// Lanes split into G heads x 32/G dim groups: each lane keeps the running
-// sum over its dims, takes its partial dots with its head's query row, and
-// the dim groups reduce with shuffles.
+// One CTA per (sequence, key head, leaf block); a thread per (query, head)
+// pair of the block (two per thread for G = 4).  The CTA stages in shared
+// memory the prefix sums of the block's keys (row t = the sum of keys
+// t0 .. t0 + t), the path's complete left siblings of the odd levels, and the
+// reference row; each thread then takes its pair's whole dots in one pass
+// over its query row, one accumulator per dot (no cross-lane reductions):
+// the prefix-sum row of its position, the reference, and every staged
+// sibling.  The level recurrence and the output row follow per thread.
 #include "pisa_common.cuh"
 #include "pisa_internal.h"
 
 namespace pisa {
 
-constexpr int kPathWarps = 4;
-
-// Dim of a lane's j-th element: with at least four dims per lane, lane dg of
-// the DG lanes of a head owns the 4-dim chunks dg, dg + DG, dg + 2 DG, ...,
-// so that the DG lanes of a head read consecutive 16-byte chunks of a row
-// (coalesced in global memory, conflict-free in shared memory); with two, the
-// pair 2 dg, 2 dg + 1.
-template <int D, int DG, int DPL>
-__device__ __forceinline__ int path_dim(int dg, int j) {
-  if constexpr (DPL >= 4) return 4 * (dg + DG * (j >> 2)) + (j & 3);
-  return dg * DPL + j;
-}
-
-// Loads the lane's DPL elements of one row (bf16 or fp32) as floats.
-template <int D, int DG, int DPL>
-__device__ __forceinline__ void path_row(const char* row, bool bf16, size_t esz, int dg, float (&v)[DPL]) {
-  if constexpr (DPL >= 4) {
-#pragma unroll
-    for (int m = 0; m < DPL / 4; ++m) load4(row + (size_t)path_dim<D, DG, DPL>(dg, 4 * m) * esz, bf16, v + 4 * m);
-  } else {
-    load2(row + (size_t)path_dim<D, DG, DPL>(dg, 0) * esz, bf16, v);
-  }
-}
+constexpr int kPathThreads = 128;
+constexpr int kPathMaxOdd = 20;  // odd levels of a path: at most L - 1 <= 20 (N <= 2^26)
 
 template <int D, int G>
-__global__ void __launch_bounds__(kPathWarps * 32) path_dots_kernel(Prob pr, Pyr s, const void* __restrict__ q,
-                                                                    const void* __restrict__ k,
-                                                                    const float* __restrict__ pyr, int ref_root,
-                                                                    float* __restrict__ out) {
-  constexpr int DG = 32 / G;   // dim groups (lanes per head)
-  constexpr int DPL = D / DG;  // dims per lane: 2 .. 32
-  extern __shared__ __align__(16) float sib_smem[];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x / 32;
-  const int g = lane / DG, dg = lane % DG;
+__global__ void __launch_bounds__(kPathThreads) path_dots_kernel(Prob pr, Pyr s, const void* __restrict__ q,
+                                                                const void* __restrict__ k,
+                                                                const float* __restrict__ pyr, int ref_root,
+                                                                float* __restrict__ out) {
+  constexpr int DP = D + 4;  // padded row stride: the rows of consecutive positions start 4 banks apart
+  extern __shared__ __align__(16) float path_smem[];
+  float* ksum = path_smem;                      // [C][DP]: prefix sums of the block's keys
+  float* sib = ksum + (size_t)s.C * DP;         // [kPathMaxOdd][D]: row l - 2 = level l's sibling (odd levels)
+  float* refr = sib + (size_t)kPathMaxOdd * D;  // [D]
+  const int tid = threadIdx.x;
   const int L = s.L;
-  float* sib = sib_smem;                           // [L][D]; row l - 1 for level l >= 2
-  float* ksw = sib + (size_t)L * D;                // [kPathWarps][D]: each warp's key-row sum
-  float* obuf = ksw + (size_t)kPathWarps * D;      // [kPathWarps][L][2][G]: a query's outputs
   const int64_t nblk = pr.B * pr.Hkv * s.nb;
   const int64_t w = blockIdx.x;
   if (w >= nblk) return;  // CTA-uniform
@@ -80,105 +57,79 @@ __global__ void __launch_bounds__(kPathWarps * 32) path_dots_kernel(Prob pr, Pyr
   const int64_t b = bh / pr.Hkv, h = bh % pr.Hkv;
   const float* ph = pyr + bh * s.P * D;
   const bool bf16 = pr.dtype == PISA_BF16;
+  const size_t esz = bf16 ? 2 : 4;
+  const int64_t t0 = qb * s.C;
+  const int nt = (int)(s.N - t0 < s.C ? s.N - t0 : s.C);
 
-  // the path's left siblings (complete nodes), staged once per block
+  // siblings of the odd levels (which levels: CTA-uniform), the reference row
   for (int l = 2; l <= L; ++l) {
     const int64_t jc = qb >> (l - 2);
     if (jc & 1) {
       const float* row = ph + (s.off[l - 2] + jc - 1) * D;
-      for (int c = threadIdx.x; c < D; c += kPathWarps * 32) sib[(l - 1) * D + c] = row[c];
+      for (int c = tid; c < D; c += kPathThreads) sib[(l - 2) * D + c] = row[c];
     }
   }
-  // reference row, lane's dims
-  float ref[DPL];
-#pragma unroll
-  for (int j = 0; j < DPL; ++j) {
-    const float r = ref_root ? ph[(s.P - 1) * D + path_dim<D, DG, DPL>(dg, j)] : 0.0f;
-    ref[j] = isfinite(r) ? r : 0.0f;
+  for (int c = tid; c < D; c += kPathThreads) {
+    const float r = ref_root ? ph[(s.P - 1) * D + c] : 0.0f;
+    refr[c] = isfinite(r) ? r : 0.0f;
   }
-
-  const int64_t t0 = qb * s.C;
-  const int nt = (int)(s.N - t0 < s.C ? s.N - t0 : s.C);
-  const int per = (s.C + kPathWarps - 1) / kPathWarps;
-  const int r0 = min(nt, warp * per), r1 = min(nt, r0 + per);
-  const size_t esz = bf16 ? 2 : 4;
-  const char* krow0 = reinterpret_cast<const char*>(k) + (bh * s.N + t0) * D * esz;
-  const char* qrow0 = reinterpret_cast<const char*>(q) + ((b * pr.Hq + h * G + g) * pr.N + t0) * D * esz;
-
-  // this warp's key rows summed, then the sums of the earlier warps' rows
-  float ks[DPL];
-#pragma unroll
-  for (int j = 0; j < DPL; ++j) ks[j] = 0.0f;
-  for (int r = r0; r < r1; ++r) {
-    float kv[DPL];
-    path_row<D, DG, DPL>(krow0 + (size_t)r * D * esz, bf16, esz, dg, kv);
-#pragma unroll
-    for (int j = 0; j < DPL; ++j) ks[j] += kv[j];
+  // prefix sums of the block's keys, one thread per dim
+  const char* kb = reinterpret_cast<const char*>(k) + (bh * s.N + t0) * D * esz;
+  for (int c = tid; c < D; c += kPathThreads) {
+    float run = 0.0f;
+    for (int t = 0; t < nt; ++t) {
+      const char* e = kb + ((size_t)t * D + c) * esz;
+      run += bf16 ? bf16_to_f(*reinterpret_cast<const uint16_t*>(e)) : *reinterpret_cast<const float*>(e);
+      ksum[t * DP + c] = run;
+    }
   }
-  if (g == 0)
-#pragma unroll
-    for (int j = 0; j < DPL; ++j) ksw[warp * D + path_dim<D, DG, DPL>(dg, j)] = ks[j];
   __syncthreads();
-#pragma unroll
-  for (int j = 0; j < DPL; ++j) {
-    float sacc = 0.0f;  // the earlier warps' sums, in warp order
-    for (int u = 0; u < warp; ++u) sacc += ksw[u * D + path_dim<D, DG, DPL>(dg, j)];
-    ks[j] = sacc;
-  }
 
-  float* ob = obuf + (size_t)warp * L * 2 * G;
-  const int nout = L * 2 * G;  // floats per query
-  for (int r = r0; r < r1; ++r) {
-    const int64_t t = t0 + r;
-    float qv[DPL], kv[DPL];
-    path_row<D, DG, DPL>(krow0 + (size_t)r * D * esz, bf16, esz, dg, kv);
-    path_row<D, DG, DPL>(qrow0 + (size_t)r * D * esz, bf16, esz, dg, qv);
-#pragma unroll
-    for (int j = 0; j < DPL; ++j) ks[j] += kv[j];
-    // partial dots: q . key sum, q . ref, q . sibling of every odd level
+  for (int pi = tid; pi < s.C * G; pi += kPathThreads) {
+    const int t = pi / G, g = pi % G;
+    if (t >= nt) continue;
+    const char* qr = reinterpret_cast<const char*>(q) + (((b * pr.Hq + h * G + g) * pr.N + t0 + t) * D) * esz;
+    const float* kr = ksum + t * DP;
     float dk = 0.0f, dr = 0.0f;
+    float ds[kPathMaxOdd];
 #pragma unroll
-    for (int j = 0; j < DPL; ++j) {
-      dk = fmaf(qv[j], ks[j], dk);
-      dr = fmaf(qv[j], ref[j], dr);
-    }
+    for (int i = 0; i < kPathMaxOdd; ++i) ds[i] = 0.0f;
+#pragma unroll 2
+    for (int c = 0; c < D; c += 4) {
+      float qv[4];
+      load4(qr + (size_t)c * esz, bf16, qv);
+      const float4 kk = *reinterpret_cast<const float4*>(kr + c);
+      const float4 rr = *reinterpret_cast<const float4*>(refr + c);
+      dk = fmaf(qv[0], kk.x, fmaf(qv[1], kk.y, fmaf(qv[2], kk.z, fmaf(qv[3], kk.w, dk))));
+      dr = fmaf(qv[0], rr.x, fmaf(qv[1], rr.y, fmaf(qv[2], rr.z, fmaf(qv[3], rr.w, dr))));
 #pragma unroll
-    for (int o = DG / 2; o >= 1; o >>= 1) {
-      dk += __shfl_xor_sync(0xffffffffu, dk, o);
-      dr += __shfl_xor_sync(0xffffffffu, dr, o);
+      for (int i = 0; i < kPathMaxOdd; ++i)
+        if (i + 2 <= L && ((qb >> i) & 1)) {  // level i + 2 has a left sibling (CTA-uniform)
+          const float4 sv = *reinterpret_cast<const float4*>(sib + i * D + c);
+          ds[i] = fmaf(qv[0], sv.x, fmaf(qv[1], sv.y, fmaf(qv[2], sv.z, fmaf(qv[3], sv.w, ds[i]))));
+        }
     }
-    const float n1 = (float)(r + 1);
+    // level recurrence (see the file comment), outputs [L][2] of this head
+    const float n1 = (float)(t + 1);
     float P = dk / n1 - dr;  // q . (prefix(1) - ref)
     float cnt = n1;
-    if (dg == 0) {
-      ob[0 * 2 * G + 0 * G + g] = P * pr.scale2;
-      ob[0 * 2 * G + 1 * G + g] = 0.0f;
-    }
-    for (int l = 2; l <= L; ++l) {
+    float* orow = out + ((bh * s.N + t0 + t) * L) * 2 * G;
+    orow[g] = P * pr.scale2;
+    orow[G + g] = 0.0f;
+#pragma unroll
+    for (int l = 2; l <= kPathMaxOdd + 1; ++l) {
+      if (l > L) break;
       const int64_t jc = qb >> (l - 2);
       float S = 0.0f;
-      if (jc & 1) {  // warp-uniform
-        float ds = 0.0f;
-        const float* srow = sib + (l - 1) * D;
-#pragma unroll
-        for (int j = 0; j < DPL; ++j) ds = fmaf(qv[j], srow[path_dim<D, DG, DPL>(dg, j)], ds);
-#pragma unroll
-        for (int o = DG / 2; o >= 1; o >>= 1) ds += __shfl_xor_sync(0xffffffffu, ds, o);
-        S = ds - dr;
+      if (jc & 1) {
+        S = ds[l - 2] - dr;
         const float ns = (float)((int64_t)s.C << (l - 2));
         P = (ns * S + cnt * P) / (ns + cnt);
         cnt += ns;
       }
-      if (dg == 0) {
-        ob[(l - 1) * 2 * G + 0 * G + g] = P * pr.scale2;
-        ob[(l - 1) * 2 * G + 1 * G + g] = S * pr.scale2;
-      }
+      orow[(l - 1) * 2 * G + g] = P * pr.scale2;
+      orow[(l - 1) * 2 * G + G + g] = S * pr.scale2;
     }
-    // the query's [L][2][G] outputs leave as whole rows
-    __syncwarp();
-    float* orow = out + ((bh * s.N + t) * L) * 2 * G;
-    for (int e = lane; e < nout; e += 32) orow[e] = ob[e];
-    __syncwarp();
   }
 }
 
@@ -189,13 +140,14 @@ size_t path_dots_bytes(const Prob& pr, const Pyr& s) {
 template <int D, int G>
 static cudaError_t launch_path_t(const Prob& pr, const Pyr& s, const void* q, const void* k, const float* pyr,
                                  int ref_root, float* out, cudaStream_t st) {
-  const size_t smem = ((size_t)(s.L + kPathWarps) * D + (size_t)kPathWarps * s.L * 2 * G) * sizeof(float);
+  if (s.L - 1 > kPathMaxOdd) return cudaErrorInvalidValue;  // beyond the size limit
+  const size_t smem = ((size_t)s.C * (D + 4) + (size_t)(kPathMaxOdd + 1) * D) * sizeof(float);
   auto kern = path_dots_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t nblk = pr.B * pr.Hkv * s.nb;
   note_launch();
-  kern<<<(unsigned)nblk, kPathWarps * 32, smem, st>>>(pr, s, q, k, pyr, ref_root, out);
+  kern<<<(unsigned)nblk, kPathThreads, smem, st>>>(pr, s, q, k, pyr, ref_root, out);
   return cudaGetLastError();
 }
 
