@@ -94,20 +94,35 @@ __global__ void __launch_bounds__(kPathThreads) path_dots_kernel(Prob pr, Pyr s,
     float ds[kPathMaxOdd];
 #pragma unroll
     for (int i = 0; i < kPathMaxOdd; ++i) ds[i] = 0.0f;
-#pragma unroll 2
-    for (int c = 0; c < D; c += 4) {
-      float qv[4];
-      load4(qr + (size_t)c * esz, bf16, qv);
-      const float4 kk = *reinterpret_cast<const float4*>(kr + c);
-      const float4 rr = *reinterpret_cast<const float4*>(refr + c);
-      dk = fmaf(qv[0], kk.x, fmaf(qv[1], kk.y, fmaf(qv[2], kk.z, fmaf(qv[3], kk.w, dk))));
-      dr = fmaf(qv[0], rr.x, fmaf(qv[1], rr.y, fmaf(qv[2], rr.z, fmaf(qv[3], rr.w, dr))));
+    for (int c = 0; c < D; c += 8) {
+      // eight query elements per load (16 bytes of bf16)
+      float qv[8];
+      if (bf16) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(qr + (size_t)c * 2));
+        const uint32_t wv[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int i = 0; i < kPathMaxOdd; ++i)
-        if (i + 2 <= L && ((qb >> i) & 1)) {  // level i + 2 has a left sibling (CTA-uniform)
-          const float4 sv = *reinterpret_cast<const float4*>(sib + i * D + c);
-          ds[i] = fmaf(qv[0], sv.x, fmaf(qv[1], sv.y, fmaf(qv[2], sv.z, fmaf(qv[3], sv.w, ds[i]))));
+        for (int e = 0; e < 4; ++e) {
+          qv[2 * e] = __uint_as_float(wv[e] << 16);
+          qv[2 * e + 1] = __uint_as_float(wv[e] & 0xffff0000u);
         }
+      } else {
+        load4(qr + (size_t)c * 4, false, qv);
+        load4(qr + (size_t)(c + 4) * 4, false, qv + 4);
+      }
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float* qh = qv + 4 * hh;
+        const float4 kk = *reinterpret_cast<const float4*>(kr + c + 4 * hh);
+        const float4 rr = *reinterpret_cast<const float4*>(refr + c + 4 * hh);
+        dk = fmaf(qh[0], kk.x, fmaf(qh[1], kk.y, fmaf(qh[2], kk.z, fmaf(qh[3], kk.w, dk))));
+        dr = fmaf(qh[0], rr.x, fmaf(qh[1], rr.y, fmaf(qh[2], rr.z, fmaf(qh[3], rr.w, dr))));
+#pragma unroll
+        for (int i = 0; i < kPathMaxOdd; ++i)
+          if (i + 2 <= L && ((qb >> i) & 1)) {  // level i + 2 has a left sibling (CTA-uniform)
+            const float4 sv = *reinterpret_cast<const float4*>(sib + i * D + c + 4 * hh);
+            ds[i] = fmaf(qh[0], sv.x, fmaf(qh[1], sv.y, fmaf(qh[2], sv.z, fmaf(qh[3], sv.w, ds[i]))));
+          }
+      }
     }
     // level recurrence (see the file comment), outputs [L][2] of this head
     const float n1 = (float)(t + 1);
