@@ -173,40 +173,46 @@ __global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const i
 }
 
 // Exclusive scans of the pair counts and of the tiles per bucket (one CTA),
-// in rounds of 4096 buckets: coalesced loads into shared memory, four
-// consecutive buckets per thread, warp-shuffle scans of the thread sums, and
-// a running carry between rounds.  Q (rows per tile / G) is a power of two.
+// in rounds of 1024 x 32 buckets (one round up to 32768 buckets): each thread
+// takes 32 consecutive buckets with 16-byte loads and stores, warp-shuffle
+// scans combine the thread sums, and a carry runs between rounds.  Q (rows
+// per tile / G) is a power of two.
+constexpr int kScanPer = 32;
 __global__ void __launch_bounds__(1024) scan_kernel(int64_t nb, int32_t Q, const int32_t* __restrict__ counts,
                                                     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_off) {
-  constexpr int kRound = 4096;
-  __shared__ int32_t cs[kRound], ts[kRound];
   __shared__ int32_t wp[32], wt[32];
   __shared__ int32_t carry[2];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int qs = __ffs(Q) - 1;
   if (tid == 0) { carry[0] = 0; carry[1] = 0; }
-  for (int64_t base = 0; base < nb; base += kRound) {
+  __syncthreads();
+  for (int64_t base = 0; base < nb; base += 1024 * kScanPer) {
+    const int64_t b0 = base + (int64_t)tid * kScanPer;
+    // a whole run in range is 128-byte aligned (the arrays start 256-byte
+    // aligned); the counts are read twice (sums, then offsets) rather than
+    // held across the block scan
+    const bool whole = b0 + kScanPer <= nb;
+    int32_t sp = 0, st = 0;
+    if (whole) {
 #pragma unroll
-    for (int j = 0; j < kRound / 1024; ++j) {
-      const int64_t i = base + j * 1024 + tid;
-      const int32_t c = i < nb ? counts[i] : 0;
-      cs[j * 1024 + tid] = c;
-      ts[j * 1024 + tid] = (c + Q - 1) >> qs;
+      for (int j = 0; j < kScanPer / 4; ++j) {
+        const int4 v = reinterpret_cast<const int4*>(counts + b0)[j];
+        sp += (v.x + v.y) + (v.z + v.w);
+        st += (((v.x + Q - 1) >> qs) + ((v.y + Q - 1) >> qs)) + (((v.z + Q - 1) >> qs) + ((v.w + Q - 1) >> qs));
+      }
+    } else {
+      for (int j = 0; j < kScanPer; ++j) {
+        const int32_t c = b0 + j < nb ? counts[b0 + j] : 0;
+        sp += c;
+        st += (c + Q - 1) >> qs;
+      }
     }
-    __syncthreads();
-    int32_t pc[4], pt[4], sp = 0, st = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      pc[j] = sp; pt[j] = st;
-      sp += cs[4 * tid + j];
-      st += ts[4 * tid + j];
-    }
-    // inclusive warp scans of the thread sums
+    // inclusive warp scans of the thread sums, then of the warp totals
     int32_t ip = sp, it = st;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int32_t a = __shfl_up_sync(0xffffffffu, ip, o), b = __shfl_up_sync(0xffffffffu, it, o);
-      if (lane >= o) { ip += a; it += b; }
+      const int32_t x = __shfl_up_sync(0xffffffffu, ip, o), y = __shfl_up_sync(0xffffffffu, it, o);
+      if (lane >= o) { ip += x; it += y; }
     }
     if (lane == 31) { wp[wid] = ip; wt[wid] = it; }
     __syncthreads();
@@ -214,26 +220,36 @@ __global__ void __launch_bounds__(1024) scan_kernel(int64_t nb, int32_t Q, const
       int32_t x = wp[lane], y = wt[lane];
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
-        const int32_t a = __shfl_up_sync(0xffffffffu, x, o), b = __shfl_up_sync(0xffffffffu, y, o);
-        if (lane >= o) { x += a; y += b; }
+        const int32_t xx = __shfl_up_sync(0xffffffffu, x, o), yy = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) { x += xx; y += yy; }
       }
       wp[lane] = x - wp[lane];  // exclusive warp offsets
       wt[lane] = y - wt[lane];
     }
     __syncthreads();
-    const int32_t op = carry[0] + wp[wid] + (ip - sp), ot = carry[1] + wt[wid] + (it - st);
+    int32_t op = carry[0] + wp[wid] + (ip - sp), ot = carry[1] + wt[wid] + (it - st);
+    if (whole) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      cs[4 * tid + j] = op + pc[j];
-      ts[4 * tid + j] = ot + pt[j];
+      for (int j = 0; j < kScanPer / 4; ++j) {
+        const int4 v = reinterpret_cast<const int4*>(counts + b0)[j];
+        int4 vo, vt;
+        vo.x = op; vt.x = ot; op += v.x; ot += (v.x + Q - 1) >> qs;
+        vo.y = op; vt.y = ot; op += v.y; ot += (v.y + Q - 1) >> qs;
+        vo.z = op; vt.z = ot; op += v.z; ot += (v.z + Q - 1) >> qs;
+        vo.w = op; vt.w = ot; op += v.w; ot += (v.w + Q - 1) >> qs;
+        reinterpret_cast<int4*>(offsets + b0)[j] = vo;
+        reinterpret_cast<int4*>(tile_off + b0)[j] = vt;
+      }
+    } else {
+      for (int j = 0; j < kScanPer; ++j) {
+        const int32_t c = b0 + j < nb ? counts[b0 + j] : 0;
+        if (b0 + j < nb) { offsets[b0 + j] = op; tile_off[b0 + j] = ot; }
+        op += c;
+        ot += (c + Q - 1) >> qs;
+      }
     }
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < kRound / 1024; ++j) {
-      const int64_t i = base + j * 1024 + tid;
-      if (i < nb) { offsets[i] = cs[j * 1024 + tid]; tile_off[i] = ts[j * 1024 + tid]; }
-    }
-    if (tid == 1023) { carry[0] = op + sp; carry[1] = ot + st; }
+    __syncthreads();  // every thread has read carry and the warp offsets
+    if (tid == 1023) { carry[0] = op; carry[1] = ot; }
     __syncthreads();
   }
   if (tid == 0) { offsets[nb] = carry[0]; tile_off[nb] = carry[1]; }
@@ -671,7 +687,7 @@ __global__ void __launch_bounds__(256) finalize_kernel(Prob pr, const int32_t* _
 
 // One thread per query for K <= 8: the <= 16 candidates are ranked in
 // registers (the loads and stores of consecutive threads are contiguous).
-__global__ void __launch_bounds__(256) finalize_small_kernel(Prob pr, const int32_t* __restrict__ kept2,
+__global__ void __launch_bounds__(256, 1) finalize_small_kernel(Prob pr, const int32_t* __restrict__ kept2,
                                                              const float* __restrict__ leaf_score,
                                                              int32_t* __restrict__ out_idx,
                                                              float* __restrict__ out_score) {
@@ -712,15 +728,39 @@ __global__ void __launch_bounds__(256) finalize_small_kernel(Prob pr, const int3
       const uint32_t ok = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
       key[c] = val[c] ? ((ok & ~15u) | (uint32_t)(15 - c)) : 0u;
     }
+    // the K-th largest key: a bitonic sort (descending) of a copy in
+    // registers, 80 compare-exchanges with indices fixed at compile time;
+    // with fewer than K valid candidates it is an invalid key (0)
+    uint32_t sk[NCM];
+#pragma unroll
+    for (int c = 0; c < NCM; ++c) sk[c] = key[c];
+#pragma unroll
+    for (int kb = 2; kb <= NCM; kb <<= 1) {
+#pragma unroll
+      for (int j = kb >> 1; j > 0; j >>= 1) {
+#pragma unroll
+        for (int i = 0; i < NCM; ++i) {
+          const int l = i ^ j;
+          if (l > i) {
+            const uint32_t a = sk[i], b = sk[l];
+            const bool desc = (i & kb) == 0;
+            sk[i] = desc ? max(a, b) : min(a, b);
+            sk[l] = desc ? min(a, b) : max(a, b);
+          }
+        }
+      }
+    }
+    uint32_t thr = 0;
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j == K - 1) thr = sk[j];
     int32_t* oi = si + threadIdx.x * W;
     float* os = ss + threadIdx.x * W;
     int pos = 1;
 #pragma unroll
     for (int c = 0; c < NCM; ++c) {
-      int rank = 0;
-#pragma unroll
-      for (int j = 0; j < NCM; ++j) rank += key[j] > key[c] ? 1 : 0;
-      if (val[c] && rank < K && pos <= K) {  // candidates run in ascending leaf order
+      // valid keys are distinct and non-zero: exactly min(K, valid) reach thr
+      if (val[c] && key[c] >= thr && pos <= K) {  // candidates run in ascending leaf order
         oi[pos] = lf[c];
         os[pos] = sc[c] * kLn2;
         ++pos;
