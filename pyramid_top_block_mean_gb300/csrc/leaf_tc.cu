@@ -707,13 +707,36 @@ __global__ void __launch_bounds__(256, 1) finalize_small_kernel(Prob pr, const i
     float sc[NCM];
     int32_t lf[NCM];
     bool val[NCM];
+    // K = 8: the query's nodes and leaf scores are two and four aligned
+    // 16-byte vectors (rows of 32 and 64 bytes)
+    int32_t pv[KM];
+    float rv[NCM];
+    if (K == KM) {
+      const int4* kp = reinterpret_cast<const int4*>(kept2 + qi * KM);
+      const float4* lp = reinterpret_cast<const float4*>(leaf_score + qi * NCM);
+#pragma unroll
+      for (int j = 0; j < KM / 4; ++j) {
+        const int4 v = kp[j];
+        pv[4 * j] = v.x; pv[4 * j + 1] = v.y; pv[4 * j + 2] = v.z; pv[4 * j + 3] = v.w;
+      }
+#pragma unroll
+      for (int j = 0; j < NCM / 4; ++j) {
+        const float4 v = lp[j];
+        rv[4 * j] = v.x; rv[4 * j + 1] = v.y; rv[4 * j + 2] = v.z; rv[4 * j + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < KM; ++j) pv[j] = j < K ? kept2[qi * K + j] : -1;
+#pragma unroll
+      for (int c = 0; c < NCM; ++c) rv[c] = (c >> 1) < K ? leaf_score[(qi * K + (c >> 1)) * 2 + (c & 1)] : 0.0f;
+    }
 #pragma unroll
     for (int c = 0; c < NCM; ++c) {
-      const int slot = c >> 1;
-      const int32_t p = slot < K ? kept2[qi * K + slot] : -1;
+      const int32_t p = pv[c >> 1];
       lf[c] = p >= 0 ? 2 * p + (c & 1) : -1;
       val[c] = p >= 0 && lf[c] >= 1 && lf[c] <= qb - 2;
-      const float v = val[c] ? leaf_score[(qi * K + slot) * 2 + (c & 1)] : -INFINITY;
+      // a score slot whose node is not eligible was never written: ignored
+      const float v = val[c] ? rv[c] : -INFINITY;
       sc[c] = v != v ? -INFINITY : v;  // NaN ranks as -inf (a total order)
     }
     // rank keys: the orderable score with its low 4 bits replaced by the
