@@ -94,3 +94,53 @@ def test_sweep_point_matches_oracle(pisa, N):
     if N >= 4 * CHUNK:
         assert rep.n >= 100000
     assert rep.ok(), str(rep)
+
+
+def test_two_sequences_256k_matches_oracle(pisa):
+    """Two sequences of 262,144 tokens (the sweep's heads and sizes, B = 2):
+    65,536 buckets, so the bucket scan takes two rounds of 32,768 and the
+    second sequence's buckets follow the first's.  Checked: 3,000 random
+    positions, 64 on each side of every chunk boundary and the last 128
+    positions, for every (sequence, key head)."""
+    base = W.sweep(1 << 18)
+    s = W.Shape(B=2, N=base.N, Hq=base.Hq, Hkv=base.Hkv, d=base.d, K=base.K, dtype=base.dtype)
+    q, k = W.iid(s, 5)
+    p = pisa.params_from_shape(s)
+    sel = pisa.Selector(p)
+    L = pisa.pyramid_levels(p)
+    qd, kd = q.cuda(), k.cuda()
+    tr = torch.full((s.B, s.Hkv, s.N, L, s.K), -7, dtype=torch.int32, device="cuda")
+    pisa.build_pyramid(p, kd, sel.pyramid)
+    pisa.prefill_route(p, qd, sel.pyramid, sel.ws, tr)
+    pisa.prefill_leaves(p, qd, kd, sel.ws, sel.out_idx, sel.out_score)
+    torch.cuda.synchronize()
+    assert sel.device_status() == 0
+
+    gen = np.random.default_rng(29)
+    ts = set(gen.integers(0, s.N, 3000).tolist()) | set(range(s.N - 128, s.N))
+    for c in range(1, s.N // CHUNK):
+        ts |= set(range(c * CHUNK - 64, c * CHUNK + 64))
+    ts = np.array(sorted(ts))
+    bs = np.repeat(np.arange(s.B), s.Hkv * len(ts))
+    hs = np.tile(np.repeat(np.arange(s.Hkv), len(ts)), s.B)
+    tt = np.tile(ts, s.B * s.Hkv)
+    rows = torch.from_numpy((bs * s.Hkv + hs) * s.N + tt).cuda()
+    W_ = s.K + 3
+    idx = sel.out_idx.reshape(-1, W_)[rows].cpu().numpy()
+    score = sel.out_score.reshape(-1, W_)[rows].cpu().double().numpy()
+    trace = tr.reshape(s.B * s.Hkv * s.N, L, s.K)[rows].cpu().numpy()
+    del tr, sel, qd, kd
+    torch.cuda.empty_cache()
+
+    o = oracle.Oracle.from_shape(s)
+    kn = k.double().numpy()
+    pyr = o.pyramid(kn)
+    qv = q.reshape(s.B, s.Hkv, s.G, s.N, s.d)
+    keys = [(int(b), int(h), int(t)) for b, h, t in zip(bs, hs, tt)]
+    qsel = qv[torch.from_numpy(bs), torch.from_numpy(hs), :, torch.from_numpy(tt)].double().numpy()
+    rep = Report()
+    ref = o.select(qsel, kn, pyr, sel=keys, qrows=True)
+    compare(o, qsel, kn, pyr, ref, idx, score, trace, keys, rep, qmode="rows")
+    print(f"B=2 N={s.N}: {rep}")
+    assert rep.n == len(keys)
+    assert rep.ok(), str(rep)
