@@ -46,6 +46,7 @@ struct DecSmem {
   int32_t kept2[kMaxK];
   int32_t leaf[kMaxCand];
   float lscore[kMaxCand];
+  alignas(16) uint32_t key[kMaxCand];  // rank keys of the current list (0 past its end)
   int32_t scan[4];
   int32_t nkept2, nl;
   uint64_t bar_rows, bar_leaf[kDecWarps][kNBuf];
@@ -60,6 +61,31 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       "{%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Rank key of list entry `slot` (lists run in ascending node / leaf order):
+// the orderable score with its low 6 bits replaced by the reversed slot, so
+// keys are distinct and non-zero, a higher score ranks first, and among
+// scores equal to 2^-17 relative (far inside the 1e-3 tie margin) the lower
+// slot -- the lower index -- ranks first.  NaN ranks as -inf, -0 as +0.
+__device__ __forceinline__ uint32_t rank_key(float sc, int slot) {
+  if (sc != sc) sc = -INFINITY;
+  if (sc == 0.0f) sc = 0.0f;
+  const uint32_t u = __float_as_uint(sc);
+  const uint32_t ok = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (ok & ~63u) | (uint32_t)(63 - slot);
+}
+
+// Number of keys of sm_keys[0, 64) above k (16-byte loads; unused entries
+// hold 0, below every key).
+__device__ __forceinline__ int rank_above(const uint32_t* sm_keys, int n, uint32_t k) {
+  const uint4* kv = reinterpret_cast<const uint4*>(sm_keys);
+  int rank = 0;
+  for (int j = 0; j < (n + 3) / 4; ++j) {
+    const uint4 v = kv[j];
+    rank += (v.x > k ? 1 : 0) + (v.y > k ? 1 : 0) + (v.z > k ? 1 : 0) + (v.w > k ? 1 : 0);
+  }
+  return rank;
 }
 
 // Exclusive scan of one value per thread over threads [0, 64).
@@ -305,15 +331,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
           }
           sm.score[tid] = sc != sc ? -INFINITY : sc;  // NaN ranks as -inf
         }
+        if (tid < kMaxCand) sm.key[tid] = tid < nc ? rank_key(sm.score[tid], tid) : 0u;
         __syncthreads();
         // Top-K and expansion, in index order
         int keep = 0, nchild = 0;
         if (tid < nc) {
-          const float si = sm.score[tid];
-          const int32_t ci = sm.cand[tid];
-          int rank = 0;
-          for (int j = 0; j < nc; ++j) rank += beats(sm.score[j], sm.cand[j], si, ci) ? 1 : 0;
-          keep = rank < K;
+          keep = rank_above(sm.key, nc, sm.key[tid]) < K;
           nchild = keep ? (level > 2 ? e0 + e1 : 1) : 0;
         }
         int total;
@@ -629,12 +652,10 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(Prob pr, Pyr s, con
       return;
     }
     // Top-K of the candidate leaves plus the forced blocks, ascending
+    if (tid < kMaxCand) sm.key[tid] = tid < nl ? rank_key(sm.lscore[tid], tid) : 0u;
+    __syncthreads();
     int keep = 0;
-    if (tid < nl) {
-      int rank = 0;
-      for (int j = 0; j < nl; ++j) rank += beats(sm.lscore[j], sm.leaf[j], sm.lscore[tid], sm.leaf[tid]) ? 1 : 0;
-      keep = rank < K;
-    }
+    if (tid < nl) keep = rank_above(sm.key, nl, sm.key[tid]) < K;
     int nkept;
     const int kp = scan64(tid < 64 ? keep : 0, sm.scan, &nkept);
     if (keep && kp < K) {  // the ranking order is total: at most K are kept
