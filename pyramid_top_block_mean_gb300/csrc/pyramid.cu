@@ -240,18 +240,22 @@ __global__ void __launch_bounds__(256) build_upper_kernel(Prob pr, Pyr s, const 
 
 // Levels 6..L with the whole of level 5 in shared memory (when it fits):
 // each level is computed from the previous one in shared memory, into the
-// other of two buffers, and written out; one CTA per (sequence, key head),
-// one __syncthreads per level instead of a round trip through L2.
+// other of two buffers, and written out; one CTA of 1024 threads per
+// (sequence, key head), one __syncthreads per level instead of a round trip
+// through L2.
 constexpr size_t kUpperSmemMax = 200 * 1024;
 
 static size_t build_upper_smem(int d, int64_t n5) { return (size_t)(n5 + (n5 + 1) / 2) * d * 4; }
 
+constexpr int kUpperThreads = 1024;
+
 template <int D>
-__global__ void __launch_bounds__(256) build_upper_smem_kernel(Prob pr, Pyr s, const int32_t* __restrict__ seq_lens,
-                                                               float* __restrict__ pyr) {
+__global__ void __launch_bounds__(kUpperThreads) build_upper_smem_kernel(Prob pr, Pyr s,
+                                                                         const int32_t* __restrict__ seq_lens,
+                                                                         float* __restrict__ pyr) {
   extern __shared__ float4 usm4[];
   float* usm = reinterpret_cast<float*>(usm4);
-  constexpr int TPN = D / 4, NPP = 256 / TPN;  // threads per node (four dims each), nodes per pass
+  constexpr int TPN = D / 4, NPP = kUpperThreads / TPN;  // threads per node (four dims each), nodes per pass
   const int64_t b = blockIdx.y, h = blockIdx.x;
   const int64_t len = seq_len_of(seq_lens, b, s.N);
   float* ph = pyr + (b * pr.Hkv + h) * s.P * D;
@@ -259,12 +263,26 @@ __global__ void __launch_bounds__(256) build_upper_smem_kernel(Prob pr, Pyr s, c
   const int n5 = (int)s.size[kLowerLevels - 1];
   float* const buf0 = usm;                     // level 5, then 7, 9, ...
   float* const buf1 = usm + (int64_t)n5 * D;    // levels 6, 8, ...
+  __shared__ uint64_t bar;
+  __shared__ int32_t abort_flag;
   {
-    const float4* src = reinterpret_cast<const float4*>(ph + s.off[kLowerLevels - 1] * D);
-    float4* dst = reinterpret_cast<float4*>(buf0);
-    for (int i = threadIdx.x; i < n5 * D / 4; i += 256) dst[i] = src[i];
+    // level 5 by bulk copies of at most 32 KB (rows are 16-byte multiples)
+    const uint32_t bytes = (uint32_t)n5 * D * 4;
+    if (threadIdx.x == 0) {
+      abort_flag = 0;
+      ptx::mbar_init(ptx::smem_u32(&bar), 1);
+      ptx::fence_mbar_init();
+      ptx::mbar_arrive_expect_tx(ptx::smem_u32(&bar), bytes);
+      const unsigned char* src = reinterpret_cast<const unsigned char*>(ph + s.off[kLowerLevels - 1] * D);
+      for (uint32_t o = 0; o < bytes; o += 32768)
+        ptx::bulk_g2s(ptx::smem_u32(reinterpret_cast<unsigned char*>(buf0) + o), src + o,
+                      bytes - o < 32768 ? bytes - o : 32768, ptx::smem_u32(&bar));
+    }
+    __syncthreads();
+    if (!ptx::mbar_wait_bounded(ptx::smem_u32(&bar), 0, &abort_flag, kBuildWaitNs)) abort_flag = 1;
+    __syncthreads();
+    if (abort_flag) return;  // a copy that never lands leaves levels >= 6 unwritten
   }
-  __syncthreads();
   int cur = 0;
   for (int level = kLowerLevels + 1; level <= s.L; ++level) {
     const int n = (int)s.size[level - 1];
@@ -312,7 +330,7 @@ cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, co
     e = cudaFuncSetAttribute(ukern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)usmem);
     if (e != cudaSuccess) return e;
     note_launch();
-    ukern<<<g2, 256, usmem, st>>>(pr, s, seq_lens, pyr);
+    ukern<<<g2, kUpperThreads, usmem, st>>>(pr, s, seq_lens, pyr);
     return cudaGetLastError();
   }
   note_launch();
