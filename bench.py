@@ -270,7 +270,7 @@ def stage_rooflines(s, work, stage_ms, pk):
                   "traffic": load_traffic(traffic_name) if traffic_name else None})
         return r
     out = {
-        "build": one("build_lower_kernel + build_upper_kernel", work["pyramid_bytes"], 0.0, stage_ms["build"],
+        "build": one("build_lower_kernel + build_upper_smem_kernel", work["pyramid_bytes"], 0.0, stage_ms["build"],
                      "build_lower_kernel"),
         "route": one("route stage (pyramid split + routing kernel)", work["route_bytes"], work["route_flops"],
                      stage_ms["route"], ROUTE_KERNEL),
