@@ -120,7 +120,31 @@ constexpr int kQueriesPerCta = 2048;
 constexpr int kSmemBins = 16384;
 static_assert(((1 << kChunkShift) % kQueriesPerCta) == 0, "a CTA's queries stay in one chunk");
 
-__global__ void __launch_bounds__(512) count_smem_kernel(BucketArgs a, const int32_t* __restrict__ kept2,
+// Histogram pass over a CTA's ne entries (thread t of kBucketThreads takes
+// entries t + kBucketThreads j):
+// the entries of a chunk are loaded into registers first, so a thread keeps
+// 32 loads in flight instead of one per shared-memory atomic.  f(e, p) is
+// called for every entry e < ne with its node p.
+constexpr int kEntryChunk = 32;
+constexpr int kBucketThreads = 512;  // threads of the shared-memory histogram kernels
+template <class F>
+__device__ __forceinline__ void for_entry_chunks(const int32_t* __restrict__ src, int ne, F&& f) {
+  for (int e0 = 0; e0 < ne; e0 += kBucketThreads * kEntryChunk) {
+    int32_t pv[kEntryChunk];
+#pragma unroll
+    for (int j = 0; j < kEntryChunk; ++j) {
+      const int e = e0 + (int)threadIdx.x + kBucketThreads * j;
+      pv[j] = e < ne ? src[e] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < kEntryChunk; ++j) {
+      const int e = e0 + (int)threadIdx.x + kBucketThreads * j;
+      if (e < ne) f(e, pv[j]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kBucketThreads) count_smem_kernel(BucketArgs a, const int32_t* __restrict__ kept2,
                                                         int32_t* __restrict__ counts) {
   extern __shared__ int32_t hist[];
   const int n2 = (int)a.n2, K = a.K;
@@ -129,18 +153,17 @@ __global__ void __launch_bounds__(512) count_smem_kernel(BucketArgs a, const int
   for (int i = threadIdx.x; i < n2; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int32_t* src = kept2 + (bh * a.N + t0) * K;
-  for (int e = threadIdx.x; e < ne; e += blockDim.x) {
-    const int32_t p = src[e];
+  for_entry_chunks(src, ne, [&](int e, int32_t p) {
     const int qn = e / K;
     if (entry_counts(a, src + qn * K, e - qn * K, p)) atomicAdd(&hist[p], 1);
-  }
+  });
   __syncthreads();
   int32_t* dst = counts + (bh * a.nchunk + (t0 >> kChunkShift)) * a.n2;
   for (int i = threadIdx.x; i < n2; i += blockDim.x)
     if (hist[i]) atomicAdd(&dst[i], hist[i]);
 }
 
-__global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const int32_t* __restrict__ kept2,
+__global__ void __launch_bounds__(kBucketThreads) scatter_smem_kernel(BucketArgs a, const int32_t* __restrict__ kept2,
                                                           const int32_t* __restrict__ offsets,
                                                           int32_t* __restrict__ cursor, int32_t* __restrict__ pairs) {
   extern __shared__ int32_t hist[];
@@ -150,11 +173,10 @@ __global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const i
   for (int i = threadIdx.x; i < n2; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const int32_t* src = kept2 + (bh * a.N + t0) * K;
-  for (int e = threadIdx.x; e < ne; e += blockDim.x) {
-    const int32_t p = src[e];
+  for_entry_chunks(src, ne, [&](int e, int32_t p) {
     const int qn = e / K;
     if (entry_counts(a, src + qn * K, e - qn * K, p)) atomicAdd(&hist[p], 1);
-  }
+  });
   __syncthreads();
   // reserve this CTA's range in every bucket it touches
   const int64_t b0 = (bh * a.nchunk + (t0 >> kChunkShift)) * a.n2;
@@ -163,13 +185,10 @@ __global__ void __launch_bounds__(512) scatter_smem_kernel(BucketArgs a, const i
     if (c) hist[i] = offsets[b0 + i] + atomicAdd(&cursor[b0 + i], c);
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < ne; e += blockDim.x) {
-    const int32_t p = src[e];
+  for_entry_chunks(src, ne, [&](int e, int32_t p) {
     const int qn = e / K;
-    if (entry_counts(a, src + qn * K, e - qn * K, p)) {
-      pairs[atomicAdd(&hist[p], 1)] = encode_pair(a, t0 + qn, e - qn * K);
-    }
-  }
+    if (entry_counts(a, src + qn * K, e - qn * K, p)) pairs[atomicAdd(&hist[p], 1)] = encode_pair(a, t0 + qn, e - qn * K);
+  });
 }
 
 // Exclusive scans of the pair counts and of the tiles per bucket (one CTA),
@@ -871,12 +890,12 @@ cudaError_t launch_buckets(const BucketJob& j, int num_sms, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   note_launch();
-  if (smem_bins) count_smem_kernel<<<gs, 512, hbytes, st>>>(a, j.lists, j.counts);
+  if (smem_bins) count_smem_kernel<<<gs, kBucketThreads, hbytes, st>>>(a, j.lists, j.counts);
   else count_kernel<<<g1, 256, 0, st>>>(a, j.lists, j.counts);
   note_launch();
   scan_kernel<<<1, 1024, 0, st>>>(j.nbuckets, j.Q, j.counts, j.offsets, j.tile_off);
   note_launch();
-  if (smem_bins) scatter_smem_kernel<<<gs, 512, hbytes, st>>>(a, j.lists, j.offsets, j.cursor, j.pairs);
+  if (smem_bins) scatter_smem_kernel<<<gs, kBucketThreads, hbytes, st>>>(a, j.lists, j.offsets, j.cursor, j.pairs);
   else scatter_kernel<<<g1, 256, 0, st>>>(a, j.lists, j.offsets, j.cursor, j.pairs);
   const unsigned g2 = (unsigned)std::min<int64_t>(ceil_div64(j.nbuckets, 256), (int64_t)num_sms * 8);
   note_launch();
