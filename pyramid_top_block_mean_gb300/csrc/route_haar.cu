@@ -73,7 +73,8 @@ __device__ __forceinline__ int row_exponent(float mx) {
 // holds the first half of node r and row r + 8 its second half.  The 16-byte
 // fragments of k-steps 2m and 2m + 1 of thread t are adjacent, at byte
 // 128 m + 32 t: one 32-byte load per thread and k-step pair, and the quad's
-// four loads cover one whole 128-byte line.
+// four loads cover one whole 128-byte line.  The prep kernel writes rows through
+// the inverse map (inv_row_pos), so each lane stores a contiguous piece.
 __device__ __forceinline__ int row_pos(int c, int D) {
   const int hd = D / 2;
   const int s = c / hd, cc = c % hd;
@@ -82,6 +83,15 @@ __device__ __forceinline__ int row_pos(int c, int D) {
   const int word = ((kp >> 3) << 1) | s;
   const int chunk = ((kk >> 1) * 4 + t) * 2 + (kk & 1);
   return (chunk * 4 + word) * 2 + (kp & 1);
+}
+
+// The dim stored at position p of a row (the inverse of row_pos).
+__device__ __forceinline__ int inv_row_pos(int p, int D) {
+  const int chunk = p >> 3, word = (p >> 1) & 3;
+  const int kk = ((chunk >> 3) << 1) | (chunk & 1);
+  const int t = (chunk >> 1) & 3;
+  const int kp = ((word >> 1) << 3) | (t << 1) | (p & 1);
+  return (word & 1) * (D / 2) + kk * 16 + kp;
 }
 
 // 32 bytes from global memory (read-only path), as two 16-byte fragments.
@@ -171,12 +181,14 @@ __global__ void haar_prep_kernel(int64_t BH, Pyr s, int D, const float* __restri
     while (l < s.L && r2 >= s.off[l] - n1) ++l;  // s.off[l] is the first row of level l + 1
     const int64_t j = r2 - (s.off[l - 1] - n1);
     const float* pb = pyr + bh * s.P * D;
+    // lane L produces stored positions [per L, per L + per) of the row, so
+    // each row is written with one coalesced store per array
     float v[4];
     float mx = 0.0f;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       if (m >= per) break;
-      const int c = lane + 32 * m;
+      const int c = inv_row_pos(per * lane + m, D);
       float x;
       if (kind == 0) {
         const float ref = pb[(s.P - 1) * D + c];
@@ -194,18 +206,24 @@ __global__ void haar_prep_kernel(int64_t BH, Pyr s, int D, const float* __restri
     float ss = 0.0f;
     __half* hi = (kind == 0 ? mu_hi : dd_hi) + r * D;
     __half* lo = (kind == 0 ? mu_lo : dd_lo) + r * D;
+    uint32_t hw[2] = {0u, 0u}, lw2[2] = {0u, 0u};
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       if (m >= per) break;
-      const int c = lane + 32 * m;
       const float xs = v[m] * sc;
       const __half h = __float2half_rn(xs);
       const __half lw = __float2half_rn(xs - __half2float(h));
       const float lf = __half2float(lw);
       ss = fmaf(lf, lf, ss);
-      const int p = row_pos(c, D);
-      hi[p] = h;
-      lo[p] = lw;
+      hw[m >> 1] |= (uint32_t)__half_as_ushort(h) << (16 * (m & 1));
+      lw2[m >> 1] |= (uint32_t)__half_as_ushort(lw) << (16 * (m & 1));
+    }
+    if (per == 4) {
+      reinterpret_cast<uint2*>(hi)[lane] = make_uint2(hw[0], hw[1]);
+      reinterpret_cast<uint2*>(lo)[lane] = make_uint2(lw2[0], lw2[1]);
+    } else {
+      reinterpret_cast<uint32_t*>(hi)[lane] = hw[0];
+      reinterpret_cast<uint32_t*>(lo)[lane] = lw2[0];
     }
     ss = warp_sum(ss);
     if (lane == 0) meta[r * 2 + kind] = make_float2(pow2f(-e), sqrtf(ss) * pow2f(-e));
