@@ -104,6 +104,7 @@ __device__ __forceinline__ int64_t bucket_of(const BucketArgs& a, int64_t qi, in
 }
 
 __global__ void count_kernel(BucketArgs a, const int32_t* __restrict__ kept2, int32_t* __restrict__ counts) {
+  pdl_wait();
   const int64_t n = a.nq * a.K;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t p = kept2[i];
@@ -146,6 +147,7 @@ __device__ __forceinline__ void for_entry_chunks(const int32_t* __restrict__ src
 
 __global__ void __launch_bounds__(kBucketThreads) count_smem_kernel(BucketArgs a, const int32_t* __restrict__ kept2,
                                                         int32_t* __restrict__ counts) {
+  pdl_wait();
   extern __shared__ int32_t hist[];
   const int n2 = (int)a.n2, K = a.K;
   const int64_t bh = blockIdx.y, t0 = (int64_t)blockIdx.x * kQueriesPerCta;
@@ -166,6 +168,7 @@ __global__ void __launch_bounds__(kBucketThreads) count_smem_kernel(BucketArgs a
 __global__ void __launch_bounds__(kBucketThreads) scatter_smem_kernel(BucketArgs a, const int32_t* __restrict__ kept2,
                                                           const int32_t* __restrict__ offsets,
                                                           int32_t* __restrict__ cursor, int32_t* __restrict__ pairs) {
+  pdl_wait();
   extern __shared__ int32_t hist[];
   const int n2 = (int)a.n2, K = a.K;
   const int64_t bh = blockIdx.y, t0 = (int64_t)blockIdx.x * kQueriesPerCta;
@@ -199,6 +202,7 @@ __global__ void __launch_bounds__(kBucketThreads) scatter_smem_kernel(BucketArgs
 constexpr int kScanPer = 32;
 __global__ void __launch_bounds__(1024) scan_kernel(int64_t nb, int32_t Q, const int32_t* __restrict__ counts,
                                                     int32_t* __restrict__ offsets, int32_t* __restrict__ tile_off) {
+  pdl_wait();
   __shared__ int32_t wp[32], wt[32];
   __shared__ int32_t carry[2];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
@@ -276,6 +280,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(int64_t nb, int32_t Q, const
 
 __global__ void scatter_kernel(BucketArgs a, const int32_t* __restrict__ kept2, const int32_t* __restrict__ offsets,
                                int32_t* __restrict__ cursor, int32_t* __restrict__ pairs) {
+  pdl_wait();
   const int64_t n = a.nq * a.K;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int32_t p = kept2[i];
@@ -291,6 +296,7 @@ __global__ void scatter_kernel(BucketArgs a, const int32_t* __restrict__ kept2, 
 __global__ void tiles_kernel(int64_t nb, int64_t n2, int64_t nchunk, int32_t Q, const int32_t* __restrict__ counts,
                              const int32_t* __restrict__ offsets, const int32_t* __restrict__ tile_off,
                              int4* __restrict__ tile_info) {
+  pdl_wait();
   for (int64_t j = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; j < nb; j += (int64_t)gridDim.x * blockDim.x) {
     const int32_t n = counts[j], t0 = tile_off[j], p0 = offsets[j];
     const int32_t bh = (int32_t)((j / n2) / nchunk), node = (int32_t)(j % n2);
@@ -334,6 +340,7 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
                    const uint16_t* __restrict__ q, const int4* __restrict__ tile_info,
                    const int32_t* __restrict__ tile_total, const int32_t* __restrict__ pairs,
                    float* __restrict__ leaf_score, int32_t* __restrict__ status, LeafWaits waits) {
+  pdl_wait();
   const uint64_t kWaitLimitNs = waits.limit_ns;  // shadows the default: every wait below is bounded by it
   extern __shared__ unsigned char smem_raw[];
   LeafTcSmem<D>& sm = *reinterpret_cast<LeafTcSmem<D>*>(
@@ -663,6 +670,7 @@ __global__ void __launch_bounds__(kLeafTcThreads, 1)
 __global__ void __launch_bounds__(256) finalize_kernel(Prob pr, const int32_t* __restrict__ kept2,
                                                        const float* __restrict__ leaf_score,
                                                        int32_t* __restrict__ out_idx, float* __restrict__ out_score) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t qi = (int64_t)blockIdx.x * 8 + threadIdx.x / 32;
   if (qi >= pr.B * pr.Hkv * pr.N) return;
@@ -730,6 +738,7 @@ __global__ void __launch_bounds__(256, 1) finalize_small_kernel(Prob pr, const i
                                                              const float* __restrict__ leaf_score,
                                                              int32_t* __restrict__ out_idx,
                                                              float* __restrict__ out_score) {
+  pdl_wait();
   constexpr int KM = 8, NCM = 2 * KM, WM = KM + 3;
   // each thread builds its row in shared memory; the block then writes its
   // rows out contiguously
@@ -884,17 +893,18 @@ static cudaError_t launch_leaf_tc_t(const Prob& pr, const PrefillWs& w, char* ws
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   note_launch();
-  kern<<<grid, kLeafTcThreads, smem, st>>>(pr, kmap, (const uint16_t*)q,
-                                           (const int4*)(ws + w.tile_info),
-                                           (const int32_t*)(ws + w.tile_off) + w.nbuckets,
-                                           (const int32_t*)(ws + w.pairs), (float*)(ws + w.leaf_score),
-                                           (int32_t*)(ws + w.status), waits);
+  e = launch_pdl(kern, dim3(grid), dim3(kLeafTcThreads), smem, st, pr, kmap, (const uint16_t*)q,
+                 (const int4*)(ws + w.tile_info), (const int32_t*)(ws + w.tile_off) + w.nbuckets,
+                 (const int32_t*)(ws + w.pairs), (float*)(ws + w.leaf_score), (int32_t*)(ws + w.status), waits);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 cudaError_t launch_buckets(const BucketJob& j, int num_sms, cudaStream_t st) {
   BucketArgs a{j.nq, j.N, j.n2, j.nchunk, j.width, j.shift, j.dedup};
-  // counts, offsets and cursor are contiguous: clear all three at once
+  // counts, offsets and cursor are contiguous: clear all three at once (the
+  // first counting kernel follows this memset as a plain launch; the later
+  // ones overlap their launch with the kernel before them)
   cudaError_t e = cudaMemsetAsync(j.counts, 0, j.clear_bytes, st);
   if (e != cudaSuccess) return e;
   const int64_t n = j.nq * j.width;
@@ -913,14 +923,19 @@ cudaError_t launch_buckets(const BucketJob& j, int num_sms, cudaStream_t st) {
   if (smem_bins) count_smem_kernel<<<gs, kBucketThreads, hbytes, st>>>(a, j.lists, j.counts);
   else count_kernel<<<g1, 256, 0, st>>>(a, j.lists, j.counts);
   note_launch();
-  scan_kernel<<<1, 1024, 0, st>>>(j.nbuckets, j.Q, j.counts, j.offsets, j.tile_off);
+  e = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, st, j.nbuckets, j.Q, j.counts, j.offsets, j.tile_off);
+  if (e != cudaSuccess) return e;
   note_launch();
-  if (smem_bins) scatter_smem_kernel<<<gs, kBucketThreads, hbytes, st>>>(a, j.lists, j.offsets, j.cursor, j.pairs);
-  else scatter_kernel<<<g1, 256, 0, st>>>(a, j.lists, j.offsets, j.cursor, j.pairs);
+  if (smem_bins)
+    e = launch_pdl(scatter_smem_kernel, gs, dim3(kBucketThreads), hbytes, st, a, j.lists, j.offsets, j.cursor,
+                   j.pairs);
+  else
+    e = launch_pdl(scatter_kernel, dim3(g1), dim3(256), 0, st, a, j.lists, j.offsets, j.cursor, j.pairs);
+  if (e != cudaSuccess) return e;
   const unsigned g2 = (unsigned)std::min<int64_t>(ceil_div64(j.nbuckets, 256), (int64_t)num_sms * 8);
   note_launch();
-  tiles_kernel<<<g2, 256, 0, st>>>(j.nbuckets, j.n2, j.nchunk, j.Q, j.counts, j.offsets, j.tile_off, j.tile_info);
-  return cudaGetLastError();
+  return launch_pdl(tiles_kernel, dim3(g2), dim3(256), 0, st, j.nbuckets, j.n2, j.nchunk, j.Q, j.counts,
+                    j.offsets, j.tile_off, j.tile_info);
 }
 
 cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, char* ws, const void* q,
@@ -956,12 +971,10 @@ cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, cha
   }
   note_launch();
   if (pr.K <= 8)
-    finalize_small_kernel<<<(unsigned)ceil_div64(nq, 256), 256, 0, st>>>(pr, kept2, (const float*)(ws + w.leaf_score),
-                                                                         out_idx, out_score);
-  else
-    finalize_kernel<<<(unsigned)ceil_div64(nq, 8), 256, 0, st>>>(pr, kept2, (const float*)(ws + w.leaf_score),
-                                                                out_idx, out_score);
-  return cudaGetLastError();
+    return launch_pdl(finalize_small_kernel, dim3((unsigned)ceil_div64(nq, 256)), dim3(256), 0, st, pr, kept2,
+                      (const float*)(ws + w.leaf_score), out_idx, out_score);
+  return launch_pdl(finalize_kernel, dim3((unsigned)ceil_div64(nq, 8)), dim3(256), 0, st, pr, kept2,
+                    (const float*)(ws + w.leaf_score), out_idx, out_score);
 }
 
 }  // namespace pisa

@@ -198,6 +198,10 @@ __device__ __forceinline__ int64_t leaf_row(const KeyPages& kp, int64_t Hkv, int
   return ((int64_t)kp.table[b * kp.max_pages + leaf] * Hkv + h) * C;
 }
 
+// Kernels launched with launch_pdl start here: wait until the previous grid
+// on the stream has completed and its memory operations are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Record the first device fault in the workspace status word.
 __device__ __forceinline__ void set_status(int32_t* status, int32_t code) {
   if (status) atomicCAS(status, 0, code);

@@ -78,6 +78,28 @@ int sm_count(int device);
 // Counts one kernel launch (process-wide, relaxed atomic); called before every launch.
 void note_launch();
 
+// Launches a kernel of the prefill chain with programmatic stream
+// serialization: its launch and prologue may overlap the tail of the kernel
+// before it on the stream.  Every kernel launched this way calls pdl_wait()
+// before it touches memory, which blocks until the previous grid has
+// completed and its writes are visible; without a preceding kernel it
+// returns at once.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // 2D TMA view [rows, d] of a bf16 tensor: box of 64 columns x box_rows rows,
 // 128-byte swizzle (the K-major operand layout of the tcgen05 MMAs).
 bool make_tmap_rows(CUtensorMap* m, const void* base, int64_t rows, int d, int box_rows);

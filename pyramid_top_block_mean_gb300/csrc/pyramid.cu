@@ -85,6 +85,7 @@ template <int D, bool kPaged>
 __global__ void __launch_bounds__(kBuildThreads) build_lower_kernel(Prob pr, Pyr s, const void* __restrict__ k,
                                                                    KeyPages kp, const int32_t* __restrict__ seq_lens,
                                                                    float* __restrict__ pyr, int32_t* __restrict__ status) {
+  pdl_wait();
   constexpr int LPR = leaves_per_round<D>();
   constexpr int kRounds = kLeavesPerCta / LPR;
   extern __shared__ unsigned char bsm_raw[];
@@ -206,6 +207,7 @@ __global__ void __launch_bounds__(kBuildThreads) build_lower_kernel(Prob pr, Pyr
 template <int D>
 __global__ void __launch_bounds__(256) build_upper_kernel(Prob pr, Pyr s, const int32_t* __restrict__ seq_lens,
                                                           float* __restrict__ pyr) {
+  pdl_wait();
   // D / 4 threads per node, four consecutive dims each (float4); the node
   // counts are computed once per node, and the loop over a level's nodes is
   // unrolled so several child loads are in flight
@@ -253,6 +255,7 @@ template <int D>
 __global__ void __launch_bounds__(kUpperThreads) build_upper_smem_kernel(Prob pr, Pyr s,
                                                                          const int32_t* __restrict__ seq_lens,
                                                                          float* __restrict__ pyr) {
+  pdl_wait();
   extern __shared__ float4 usm4[];
   float* usm = reinterpret_cast<float*>(usm4);
   constexpr int TPN = D / 4, NPP = kUpperThreads / TPN;  // threads per node (four dims each), nodes per pass
@@ -320,8 +323,7 @@ cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, co
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   note_launch();
-  kern<<<g1, kBuildThreads, smem, st>>>(pr, s, k, kp, seq_lens, pyr, status);
-  e = cudaGetLastError();
+  e = launch_pdl(kern, g1, dim3(kBuildThreads), smem, st, pr, s, k, kp, seq_lens, pyr, status);
   if (e != cudaSuccess || s.L <= kLowerLevels) return e;
   dim3 g2((unsigned)pr.Hkv, (unsigned)pr.B);
   const size_t usmem = build_upper_smem(pr.d, s.size[kLowerLevels - 1]);
@@ -330,13 +332,11 @@ cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, co
     e = cudaFuncSetAttribute(ukern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)usmem);
     if (e != cudaSuccess) return e;
     note_launch();
-    ukern<<<g2, kUpperThreads, usmem, st>>>(pr, s, seq_lens, pyr);
-    return cudaGetLastError();
+    return launch_pdl(ukern, g2, dim3(kUpperThreads), usmem, st, pr, s, seq_lens, pyr);
   }
   note_launch();
-  if (pr.d == 128) build_upper_kernel<128><<<g2, 256, 0, st>>>(pr, s, seq_lens, pyr);
-  else build_upper_kernel<64><<<g2, 256, 0, st>>>(pr, s, seq_lens, pyr);
-  return cudaGetLastError();
+  return launch_pdl(pr.d == 128 ? build_upper_kernel<128> : build_upper_kernel<64>, g2, dim3(256), 0, st, pr, s,
+                    seq_lens, pyr);
 }
 
 }  // namespace pisa

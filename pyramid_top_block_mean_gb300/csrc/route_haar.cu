@@ -66,26 +66,17 @@ __device__ __forceinline__ int row_exponent(float mx) {
   return min(126, max(-126, 14 - E));
 }
 
-// Position (in elements) of dim c within a stored row of D elements.  For
-// k-step kk (16 dims of each half, hd = D / 2) and quad thread t, the f16 pairs
+// Stored row layout (D elements).  For k-step kk (16 dims of each half,
+// hd = D / 2) and quad thread t, the f16 pairs
 //   {c0, c0+1}, {hd+c0, hd+c0+1}, {c0+8, c0+9}, {hd+c0+8, hd+c0+9},  c0 = 16 kk + 2 t,
 // are that thread's A fragment (a0, a1, a2, a3) of the MMA in which row r
 // holds the first half of node r and row r + 8 its second half.  The 16-byte
 // fragments of k-steps 2m and 2m + 1 of thread t are adjacent, at byte
 // 128 m + 32 t: one 32-byte load per thread and k-step pair, and the quad's
-// four loads cover one whole 128-byte line.  The prep kernel writes rows through
-// the inverse map (inv_row_pos), so each lane stores a contiguous piece.
-__device__ __forceinline__ int row_pos(int c, int D) {
-  const int hd = D / 2;
-  const int s = c / hd, cc = c % hd;
-  const int kk = cc >> 4, kp = cc & 15;
-  const int t = (kp & 7) >> 1;
-  const int word = ((kp >> 3) << 1) | s;
-  const int chunk = ((kk >> 1) * 4 + t) * 2 + (kk & 1);
-  return (chunk * 4 + word) * 2 + (kp & 1);
-}
-
-// The dim stored at position p of a row (the inverse of row_pos).
+// four loads cover one whole 128-byte line.  inv_row_pos(p) is the dim held
+// at position p (so the prep kernel writes each lane's piece contiguously):
+// p = 8 chunk + 2 word + (kp & 1) with chunk = 8 (kk >> 1) + 2 t + (kk & 1),
+// word = 2 (kp >> 3) + (half of the row), kp = dim within the k-step.
 __device__ __forceinline__ int inv_row_pos(int p, int D) {
   const int chunk = p >> 3, word = (p >> 1) & 3;
   const int kk = ((chunk >> 3) << 1) | (chunk & 1);
@@ -167,6 +158,7 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __global__ void haar_prep_kernel(int64_t BH, Pyr s, int D, const float* __restrict__ pyr, __half* __restrict__ mu_hi,
                                  __half* __restrict__ mu_lo, __half* __restrict__ dd_hi, __half* __restrict__ dd_lo,
                                  float2* __restrict__ meta) {
+  pdl_wait();
   const int64_t n1 = s.size[0];
   const int64_t P2 = s.P - n1;
   const int64_t nrow = BH * P2 * 2;
@@ -322,6 +314,7 @@ template <int D, int KM, int WARPS, bool kLse>
 __global__ void __launch_bounds__(WARPS * 32, (KM <= 8 ? 24 : 16) / WARPS)
     route_haar_kernel(Prob pr, Pyr s, const uint16_t* __restrict__ q, HaarView hv, const float* __restrict__ path,
                       int32_t* __restrict__ kept2, int32_t* __restrict__ trace) {
+  pdl_wait();
   constexpr int G = 4;
   constexpr int NC = 2 * KM;
   constexpr int CPL = NC / 16;
@@ -624,9 +617,8 @@ static cudaError_t launch_route_haar_t(const Prob& pr, const Pyr& s, const void*
   if (e != cudaSuccess) return e;
   const int64_t nq = pr.B * pr.Hkv * pr.N;
   note_launch();
-  kern<<<(unsigned)ceil_div64(nq, 2 * WARPS), WARPS * 32, smem, st>>>(pr, s, (const uint16_t*)q, hv, path, kept2,
-                                                                        trace);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3((unsigned)ceil_div64(nq, 2 * WARPS)), dim3(WARPS * 32), smem, st, pr, s,
+                    (const uint16_t*)q, hv, path, kept2, trace);
 }
 
 bool route_haar_supported(const Prob& pr) {
@@ -653,10 +645,9 @@ cudaError_t launch_route_haar(const Prob& pr, const Pyr& s, const void* q, const
   if (P2 > 0) {
     const int64_t warps = BH * P2 * 2;
     note_launch();
-    haar_prep_kernel<<<(unsigned)std::min<int64_t>(ceil_div64(warps, 8), 16384), 256, 0, st>>>(
-        BH, s, pr.d, pyr, (__half*)rows, (__half*)(rows + arr), (__half*)(rows + 2 * arr), (__half*)(rows + 3 * arr),
-        reinterpret_cast<float2*>(meta));
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(haar_prep_kernel, dim3((unsigned)std::min<int64_t>(ceil_div64(warps, 8), 16384)),
+                               dim3(256), 0, st, BH, s, pr.d, pyr, (__half*)rows, (__half*)(rows + arr),
+                               (__half*)(rows + 2 * arr), (__half*)(rows + 3 * arr), reinterpret_cast<float2*>(meta));
     if (e != cudaSuccess) return e;
   }
 #define PISA_RH_CASE(DD, LSE)                                                                            \
