@@ -137,6 +137,7 @@ struct FlatSmem {
 
 __global__ void means_to_bf16_kernel(int64_t nbh, int64_t P, int64_t nb, int d, const float* __restrict__ pyr,
                                      __nv_bfloat16* __restrict__ mu) {
+  pdl_wait();
   const int64_t n = nbh * nb * d;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t c = i % d, row = i / d, leaf = row % nb, bh = row / nb;
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(flat_threads<G>(), 1)
     flat_tc_kernel(Prob pr, FlatTiles ft, int64_t nb, const __grid_constant__ CUtensorMap mumap,
                    const uint16_t* __restrict__ q, int32_t* __restrict__ out_idx, float* __restrict__ out_score,
                    int32_t* __restrict__ status) {
+  pdl_wait();
   extern __shared__ unsigned char smem_raw[];
   FlatSmem<D, G>& sm = *reinterpret_cast<FlatSmem<D, G>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                     ~static_cast<uintptr_t>(1023));
@@ -738,8 +740,8 @@ static cudaError_t launch_flat_t(const Prob& pr, int64_t nb, const void* q, cons
   ft.Qt = kFRows / G;
   ft.nqt = ceil_div64(pr.N, ft.Qt);
   note_launch();
-  kern<<<grid, flat_threads<G>(), smem, st>>>(pr, ft, nb, mumap, (const uint16_t*)q, out_idx, out_score, status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(flat_threads<G>()), smem, st, pr, ft, nb, mumap, (const uint16_t*)q, out_idx,
+                    out_score, status);
 }
 
 cudaError_t launch_flat(const Prob& pr, const Pyr& s, const void* q, const float* pyr, char* ws, int32_t* out_idx,
@@ -750,9 +752,8 @@ cudaError_t launch_flat(const Prob& pr, const Pyr& s, const void* q, const float
   const int64_t nbh = pr.B * pr.Hkv;
   const int64_t n = nbh * s.nb * pr.d;
   note_launch();
-  means_to_bf16_kernel<<<(unsigned)std::min<int64_t>(ceil_div64(n, 256), 4096), 256, 0, st>>>(nbh, s.P, s.nb, pr.d,
-                                                                                               pyr, mu);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(means_to_bf16_kernel, dim3((unsigned)std::min<int64_t>(ceil_div64(n, 256), 4096)),
+                             dim3(256), 0, st, nbh, s.P, s.nb, pr.d, pyr, mu);
   if (e != cudaSuccess) return e;
   CUtensorMap mumap;
   if (!make_tmap_rows(&mumap, mu, nbh * s.nb, pr.d, kFCols)) return cudaErrorInvalidValue;
