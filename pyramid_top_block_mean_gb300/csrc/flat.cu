@@ -740,8 +740,8 @@ static cudaError_t launch_flat_t(const Prob& pr, int64_t nb, const void* q, cons
   ft.Qt = kFRows / G;
   ft.nqt = ceil_div64(pr.N, ft.Qt);
   note_launch();
-  return launch_pdl(kern, dim3(grid), dim3(flat_threads<G>()), smem, st, pr, ft, nb, mumap, (const uint16_t*)q, out_idx,
-                    out_score, status);
+  return launch_pdl(true, kern, dim3(grid), dim3(flat_threads<G>()), smem, st, pr, ft, nb, mumap, (const uint16_t*)q,
+                    out_idx, out_score, status);
 }
 
 cudaError_t launch_flat(const Prob& pr, const Pyr& s, const void* q, const float* pyr, char* ws, int32_t* out_idx,
@@ -752,7 +752,7 @@ cudaError_t launch_flat(const Prob& pr, const Pyr& s, const void* q, const float
   const int64_t nbh = pr.B * pr.Hkv;
   const int64_t n = nbh * s.nb * pr.d;
   note_launch();
-  cudaError_t e = launch_pdl(means_to_bf16_kernel, dim3((unsigned)std::min<int64_t>(ceil_div64(n, 256), 4096)),
+  cudaError_t e = launch_pdl(false, means_to_bf16_kernel, dim3((unsigned)std::min<int64_t>(ceil_div64(n, 256), 4096)),
                              dim3(256), 0, st, nbh, s.P, s.nb, pr.d, pyr, mu);
   if (e != cudaSuccess) return e;
   CUtensorMap mumap;

@@ -893,7 +893,7 @@ static cudaError_t launch_leaf_tc_t(const Prob& pr, const PrefillWs& w, char* ws
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   note_launch();
-  e = launch_pdl(kern, dim3(grid), dim3(kLeafTcThreads), smem, st, pr, kmap, (const uint16_t*)q,
+  e = launch_pdl(true, kern, dim3(grid), dim3(kLeafTcThreads), smem, st, pr, kmap, (const uint16_t*)q,
                  (const int4*)(ws + w.tile_info), (const int32_t*)(ws + w.tile_off) + w.nbuckets,
                  (const int32_t*)(ws + w.pairs), (float*)(ws + w.leaf_score), (int32_t*)(ws + w.status), waits);
   if (e != cudaSuccess) return e;
@@ -923,18 +923,18 @@ cudaError_t launch_buckets(const BucketJob& j, int num_sms, cudaStream_t st) {
   if (smem_bins) count_smem_kernel<<<gs, kBucketThreads, hbytes, st>>>(a, j.lists, j.counts);
   else count_kernel<<<g1, 256, 0, st>>>(a, j.lists, j.counts);
   note_launch();
-  e = launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, st, j.nbuckets, j.Q, j.counts, j.offsets, j.tile_off);
+  e = launch_pdl(true, scan_kernel, dim3(1), dim3(1024), 0, st, j.nbuckets, j.Q, j.counts, j.offsets, j.tile_off);
   if (e != cudaSuccess) return e;
   note_launch();
   if (smem_bins)
-    e = launch_pdl(scatter_smem_kernel, gs, dim3(kBucketThreads), hbytes, st, a, j.lists, j.offsets, j.cursor,
+    e = launch_pdl(true, scatter_smem_kernel, gs, dim3(kBucketThreads), hbytes, st, a, j.lists, j.offsets, j.cursor,
                    j.pairs);
   else
-    e = launch_pdl(scatter_kernel, dim3(g1), dim3(256), 0, st, a, j.lists, j.offsets, j.cursor, j.pairs);
+    e = launch_pdl(true, scatter_kernel, dim3(g1), dim3(256), 0, st, a, j.lists, j.offsets, j.cursor, j.pairs);
   if (e != cudaSuccess) return e;
   const unsigned g2 = (unsigned)std::min<int64_t>(ceil_div64(j.nbuckets, 256), (int64_t)num_sms * 8);
   note_launch();
-  return launch_pdl(tiles_kernel, dim3(g2), dim3(256), 0, st, j.nbuckets, j.n2, j.nchunk, j.Q, j.counts,
+  return launch_pdl(true, tiles_kernel, dim3(g2), dim3(256), 0, st, j.nbuckets, j.n2, j.nchunk, j.Q, j.counts,
                     j.offsets, j.tile_off, j.tile_info);
 }
 
@@ -971,9 +971,9 @@ cudaError_t launch_leaf_tc(const Prob& pr, const Pyr& s, const PrefillWs& w, cha
   }
   note_launch();
   if (pr.K <= 8)
-    return launch_pdl(finalize_small_kernel, dim3((unsigned)ceil_div64(nq, 256)), dim3(256), 0, st, pr, kept2,
+    return launch_pdl(true, finalize_small_kernel, dim3((unsigned)ceil_div64(nq, 256)), dim3(256), 0, st, pr, kept2,
                       (const float*)(ws + w.leaf_score), out_idx, out_score);
-  return launch_pdl(finalize_kernel, dim3((unsigned)ceil_div64(nq, 8)), dim3(256), 0, st, pr, kept2,
+  return launch_pdl(true, finalize_kernel, dim3((unsigned)ceil_div64(nq, 8)), dim3(256), 0, st, pr, kept2,
                     (const float*)(ws + w.leaf_score), out_idx, out_score);
 }
 

@@ -78,14 +78,17 @@ int sm_count(int device);
 // Counts one kernel launch (process-wide, relaxed atomic); called before every launch.
 void note_launch();
 
-// Launches a kernel of the prefill chain with programmatic stream
-// serialization: its launch and prologue may overlap the tail of the kernel
-// before it on the stream.  Every kernel launched this way calls pdl_wait()
-// before it touches memory, which blocks until the previous grid has
-// completed and its writes are visible; without a preceding kernel it
-// returns at once.
+// Launches a kernel of the prefill chain.  With pdl (every kernel of a call
+// but its first) the launch uses programmatic stream serialization: its
+// launch and prologue may overlap the tail of the kernel before it, which
+// is part of the same call.  A call's first kernel is launched plainly, so
+// it keeps full ordering after whatever the caller queued on the stream
+// (copies, event waits).  Every kernel launched here calls pdl_wait()
+// before it touches memory; it blocks until the previous grid has
+// completed and its writes are visible, and returns at once after a plain
+// launch.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+cudaError_t launch_pdl(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                        Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -96,7 +99,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 

@@ -323,7 +323,7 @@ cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, co
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   note_launch();
-  e = launch_pdl(kern, g1, dim3(kBuildThreads), smem, st, pr, s, k, kp, seq_lens, pyr, status);
+  e = launch_pdl(false, kern, g1, dim3(kBuildThreads), smem, st, pr, s, k, kp, seq_lens, pyr, status);
   if (e != cudaSuccess || s.L <= kLowerLevels) return e;
   dim3 g2((unsigned)pr.Hkv, (unsigned)pr.B);
   const size_t usmem = build_upper_smem(pr.d, s.size[kLowerLevels - 1]);
@@ -332,10 +332,10 @@ cudaError_t launch_build_pyramid(const Prob& pr, const Pyr& s, const void* k, co
     e = cudaFuncSetAttribute(ukern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)usmem);
     if (e != cudaSuccess) return e;
     note_launch();
-    return launch_pdl(ukern, g2, dim3(kUpperThreads), usmem, st, pr, s, seq_lens, pyr);
+    return launch_pdl(true, ukern, g2, dim3(kUpperThreads), usmem, st, pr, s, seq_lens, pyr);
   }
   note_launch();
-  return launch_pdl(pr.d == 128 ? build_upper_kernel<128> : build_upper_kernel<64>, g2, dim3(256), 0, st, pr, s,
+  return launch_pdl(true, pr.d == 128 ? build_upper_kernel<128> : build_upper_kernel<64>, g2, dim3(256), 0, st, pr, s,
                     seq_lens, pyr);
 }
 

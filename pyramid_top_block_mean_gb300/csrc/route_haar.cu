@@ -610,14 +610,15 @@ __global__ void __launch_bounds__(WARPS * 32, (KM <= 8 ? 24 : 16) / WARPS)
 
 template <int D, int KM, int WARPS, bool kLse>
 static cudaError_t launch_route_haar_t(const Prob& pr, const Pyr& s, const void* q, const HaarView& hv,
-                                       const float* path, int32_t* kept2, int32_t* trace, cudaStream_t st) {
+                                       const float* path, int32_t* kept2, int32_t* trace, bool after_prep,
+                                       cudaStream_t st) {
   const size_t smem = sizeof(HaarQPad<2 * KM>) * 2 * WARPS;
   auto kern = route_haar_kernel<D, KM, WARPS, kLse>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int64_t nq = pr.B * pr.Hkv * pr.N;
   note_launch();
-  return launch_pdl(kern, dim3((unsigned)ceil_div64(nq, 2 * WARPS)), dim3(WARPS * 32), smem, st, pr, s,
+  return launch_pdl(after_prep, kern, dim3((unsigned)ceil_div64(nq, 2 * WARPS)), dim3(WARPS * 32), smem, st, pr, s,
                     (const uint16_t*)q, hv, path, kept2, trace);
 }
 
@@ -645,16 +646,16 @@ cudaError_t launch_route_haar(const Prob& pr, const Pyr& s, const void* q, const
   if (P2 > 0) {
     const int64_t warps = BH * P2 * 2;
     note_launch();
-    cudaError_t e = launch_pdl(haar_prep_kernel, dim3((unsigned)std::min<int64_t>(ceil_div64(warps, 8), 16384)),
+    cudaError_t e = launch_pdl(false, haar_prep_kernel, dim3((unsigned)std::min<int64_t>(ceil_div64(warps, 8), 16384)),
                                dim3(256), 0, st, BH, s, pr.d, pyr, (__half*)rows, (__half*)(rows + arr),
                                (__half*)(rows + 2 * arr), (__half*)(rows + 3 * arr), reinterpret_cast<float2*>(meta));
     if (e != cudaSuccess) return e;
   }
 #define PISA_RH_CASE(DD, LSE)                                                                            \
   if (pr.d == DD && (pr.scorer == PISA_SCORER_LSE) == LSE) {                                             \
-    if (pr.K <= 8) return launch_route_haar_t<DD, 8, 8, LSE>(pr, s, q, hv, path, kept2, trace, st);            \
-    if (pr.K <= 16) return launch_route_haar_t<DD, 16, 8, LSE>(pr, s, q, hv, path, kept2, trace, st);          \
-    return launch_route_haar_t<DD, 32, 4, LSE>(pr, s, q, hv, path, kept2, trace, st);                          \
+    if (pr.K <= 8) return launch_route_haar_t<DD, 8, 8, LSE>(pr, s, q, hv, path, kept2, trace, P2 > 0, st);            \
+    if (pr.K <= 16) return launch_route_haar_t<DD, 16, 8, LSE>(pr, s, q, hv, path, kept2, trace, P2 > 0, st);          \
+    return launch_route_haar_t<DD, 32, 4, LSE>(pr, s, q, hv, path, kept2, trace, P2 > 0, st);                          \
   }
   PISA_RH_CASE(128, true) PISA_RH_CASE(64, true) PISA_RH_CASE(128, false) PISA_RH_CASE(64, false)
 #undef PISA_RH_CASE
