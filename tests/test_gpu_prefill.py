@@ -74,6 +74,22 @@ def test_pyramid_matches_direct_means(pisa, N, d, dtype, G):
     assert err <= pyramid_tolerance(s, kn), err
 
 
+def test_pyramid_long_sequence_matches_direct_means(pisa):
+    """524,325 keys (ragged), d = 128: levels 5 and 6 exceed the shared-memory
+    budget of the upper build, so the levels above 5 take the path through
+    L2; every node against the oracle's direct means."""
+    s = W.Shape(B=1, N=(1 << 19) + 37, Hq=1, Hkv=1, d=128, K=4, dtype="bf16")
+    q, k = W.iid(s, 7)
+    p = pisa.params_from_shape(s)
+    sel = pisa.Selector(p)
+    sel.build(k.cuda())
+    torch.cuda.synchronize()
+    got = sel.pyramid.cpu().double().numpy()
+    want = oracle.Oracle.from_shape(s).pyramid(k)
+    err = np.abs(got - want).max()
+    assert err <= pyramid_tolerance(s, k.double().numpy()), err
+
+
 def test_tiny_fp32_K4(pisa):
     s = W.TINY
     q, k = W.iid(s, 0)
