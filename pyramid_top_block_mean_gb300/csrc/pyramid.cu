@@ -28,34 +28,6 @@ __device__ __forceinline__ int64_t seq_len_of(const int32_t* seq_lens, int64_t b
   return v < 0 ? 0 : (v > N ? N : v);
 }
 
-// Mean of the `count` keys starting at `keys` for DPT consecutive dims, summed
-// in key order with IEEE fp32 adds (the decode update uses the same routine).
-template <int DPT>
-__device__ __forceinline__ void leaf_mean_dims(const void* keys, int64_t row_stride_elems,
-                                               bool bf16, int64_t count, float (&out)[DPT]) {
-#pragma unroll
-  for (int c = 0; c < DPT; ++c) out[c] = 0.0f;
-  if (count <= 0) return;
-#pragma unroll 4
-  for (int64_t i = 0; i < count; ++i) {
-    float v[DPT];
-    if (bf16) {
-      const uint16_t* p = reinterpret_cast<const uint16_t*>(keys) + i * row_stride_elems;
-#pragma unroll
-      for (int c = 0; c < DPT; c += 4) load4(p + c, true, v + c);
-    } else {
-      const float* p = reinterpret_cast<const float*>(keys) + i * row_stride_elems;
-#pragma unroll
-      for (int c = 0; c < DPT; c += 4) load4(p + c, false, v + c);
-    }
-#pragma unroll
-    for (int c = 0; c < DPT; ++c) out[c] = __fadd_rn(out[c], v[c]);
-  }
-  const float n = (float)count;
-#pragma unroll
-  for (int c = 0; c < DPT; ++c) out[c] = __fdiv_rn(out[c], n);
-}
-
 // Shared memory of build_lower: two stages of one round's leaves (the raw
 // keys, copied whole), the CTA's 16 leaf means, and the stages' barriers.
 constexpr int kBuildThreads = 256;
@@ -78,9 +50,9 @@ static size_t build_lower_smem(int d, bool bf16, int C) {
 // with one bulk copy per leaf (a leaf's C rows are contiguous in the cache
 // and in a page), two rounds ahead of the reduction, so each CTA keeps tens
 // of kilobytes of HBM reads in flight; every thread then sums its dimension
-// over the leaf's keys in key order with IEEE fp32 adds, exactly as
-// leaf_mean_dims does (the decode update recomputes leaves with it, and the
-// two must agree bit for bit).
+// over the leaf's keys in key order with IEEE fp32 adds and one division,
+// as the decode step recomputes its current leaf (decode.cu), so an
+// incrementally updated pyramid equals a fresh build bit for bit.
 template <int D, bool kPaged>
 __global__ void __launch_bounds__(kBuildThreads) build_lower_kernel(Prob pr, Pyr s, const void* __restrict__ k,
                                                                    KeyPages kp, const int32_t* __restrict__ seq_lens,
